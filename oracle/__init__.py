@@ -1,0 +1,120 @@
+"""fp64 CPU oracle for softmax / RMSNorm / cross-entropy forward.
+
+TEST INFRASTRUCTURE ONLY.  The arithmetic lives in ``oracle.c`` (plain C,
+double precision, one row at a time); this module compiles it with gcc and
+marshals numpy arrays through ctypes.  Only the test suite, the smoke check and
+the benchmark's CPU-baseline leg may import this package.  The CUDA library
+never imports, links or calls it, and this package imports nothing from the
+CUDA library.
+
+Every function takes and returns float64 numpy arrays.  Inputs in fp32 or bf16
+must be widened to float64 by the caller (an exact conversion); nothing here
+rounds to a narrower type.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+LIBRARY = os.path.join(_BUILD_DIR, "liboracle.so")
+
+# No fused multiply-add contraction, no fast-math: the same doubles on any host.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_library(source: str = SOURCE, output: str = LIBRARY) -> str:
+    """Compile ``source`` into the shared library ``output`` with gcc."""
+    os.makedirs(os.path.dirname(output), exist_ok=True)
+    tmp = output + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, source, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, output)
+    return output
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` unless an up-to-date library is already present."""
+    if force or not os.path.exists(LIBRARY) or os.path.getmtime(LIBRARY) < os.path.getmtime(SOURCE):
+        compile_library()
+    return LIBRARY
+
+
+def bind(path: str):
+    """Load a compiled oracle library and declare its three entry points."""
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lp = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    lib.oracle_softmax_fwd.argtypes = [dp, dp, i64, i64]
+    lib.oracle_softmax_fwd.restype = None
+    lib.oracle_rmsnorm_fwd.argtypes = [dp, dp, dp, dp, i64, i64, ctypes.c_double]
+    lib.oracle_rmsnorm_fwd.restype = None
+    lib.oracle_xent_fwd.argtypes = [dp, lp, dp, dp, i64, i64]
+    lib.oracle_xent_fwd.restype = None
+    return lib
+
+
+def library():
+    """The process-wide oracle library, compiled on first use."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = bind(build())
+        return _lib
+
+
+def _f64(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    return a
+
+
+def _ptr(a: np.ndarray, ctype=ctypes.c_double):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def softmax_fwd(x, lib=None) -> np.ndarray:
+    """Row-wise softmax of a 2-D float64 array (M x N)."""
+    lib = lib or library()
+    x = _f64(x)
+    M, N = x.shape
+    y = np.empty_like(x)
+    lib.oracle_softmax_fwd(_ptr(x), _ptr(y), M, N)
+    return y
+
+
+def rmsnorm_fwd(x, w, eps: float, lib=None):
+    """Row-wise RMSNorm of a 2-D float64 array; returns (y, rstd)."""
+    lib = lib or library()
+    x = _f64(x)
+    w = _f64(w)
+    M, N = x.shape
+    if w.shape != (N,):
+        raise ValueError(f"w must have shape ({N},), got {w.shape}")
+    y = np.empty_like(x)
+    rstd = np.empty(M, dtype=np.float64)
+    lib.oracle_rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), M, N, float(eps))
+    return y, rstd
+
+
+def xent_fwd(x, target, lib=None):
+    """Row-wise cross-entropy of logits x (M x N) against int64 targets [M];
+    returns (loss, lse)."""
+    lib = lib or library()
+    x = _f64(x)
+    M, N = x.shape
+    t = np.ascontiguousarray(target, dtype=np.int64)
+    if t.shape != (M,):
+        raise ValueError(f"target must have shape ({M},), got {t.shape}")
+    loss = np.empty(M, dtype=np.float64)
+    lse = np.empty(M, dtype=np.float64)
+    lib.oracle_xent_fwd(_ptr(x), _ptr(t, ctypes.c_int64), _ptr(loss), _ptr(lse), M, N)
+    return loss, lse

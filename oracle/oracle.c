@@ -1,0 +1,110 @@
+/*
+ * fp64 CPU oracle for the three row-wise reductions: softmax forward,
+ * RMSNorm forward and cross-entropy forward over a row-major M x N matrix.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the definition that the CUDA
+ * library is checked against.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load it.  It shares no code, header, table
+ * or helper with the CUDA path, and the CUDA path never calls it.
+ *
+ * Source.  The QbitAI article on QuACK ("无需CUDA代码，给H100加速33%-50%",
+ * ramisays.com / senqingzn.com) names the three operators in its section
+ * "让内存密集型内核达到“光速”" (making memory-bound kernels reach speed of light):
+ * RMSNorm, softmax and cross-entropy loss, the reductions of large-language-
+ * model layers.  The article never writes the formulas down, so each function
+ * below is the textbook definition that those operator names denote, written
+ * out with no blocking, fusion or reordering:
+ *
+ *   softmax   m = max_j x_j,  y_j = exp(x_j - m) / sum_k exp(x_k - m)
+ *   RMSNorm   rstd = 1 / sqrt((1/N) sum_j x_j^2 + eps),  y_j = x_j * rstd * w_j
+ *   x-entropy lse = m + log sum_j exp(x_j - m),  loss = lse - x_t
+ *
+ * All inputs arrive already widened to double (exact for fp32 and bf16 data);
+ * every operation is done in double with libm's exp, log and sqrt.  Each row
+ * is handled on its own, one element at a time, in index order.
+ *
+ * Readings where the article is silent:
+ *   - RMSNorm: eps is added to the mean of squares inside the square root; the
+ *     mean divides by N; the weight multiplies plainly (no 1+w, no bias);
+ *     rstd = 1/sqrt(ms + eps) is the per-row scalar returned.
+ *   - Cross-entropy: no reduction over rows, no ignore index, no smoothing;
+ *     a target outside [0, N) gives a NaN loss for that row.
+ *   - Softmax max-shift: the shift by the row maximum is part of the textbook
+ *     definition used here; mathematically it changes nothing, and it keeps
+ *     exp() finite for the large-magnitude rows the tests use.
+ *
+ * Compiled with -ffp-contract=off so that no multiply-add is fused and the
+ * results are the same on x86-64 and aarch64 hosts.
+ */
+#include <math.h>
+#include <stdint.h>
+
+/* Softmax forward, one row after another (article section
+ * "让内存密集型内核达到“光速”": softmax named as a reduction operator; section
+ * "内存吞吐量": the conventional three sweeps over the row -- row maximum, sum of
+ * shifted exponentials, normalisation -- which is the order taken here). */
+void oracle_softmax_fwd(const double *x, double *y, int64_t M, int64_t N)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        const double *xi = x + i * N;
+        double *yi = y + i * N;
+
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j)
+            if (xi[j] > m) m = xi[j];
+
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            s += exp(xi[j] - m);
+
+        for (int64_t j = 0; j < N; ++j)
+            yi[j] = exp(xi[j] - m) / s;
+    }
+}
+
+/* RMSNorm forward (article section "让内存密集型内核达到“光速”": RMSNorm named
+ * as a reduction operator; the section "内存吞吐量" benchmarks it).  rstd may be
+ * NULL when the caller does not want it. */
+void oracle_rmsnorm_fwd(const double *x, const double *w, double *y,
+                        double *rstd, int64_t M, int64_t N, double eps)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        const double *xi = x + i * N;
+        double *yi = y + i * N;
+
+        double sum_sq = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            sum_sq += xi[j] * xi[j];
+        double ms = sum_sq / (double)N;
+        double r = 1.0 / sqrt(ms + eps);
+
+        for (int64_t j = 0; j < N; ++j)
+            yi[j] = xi[j] * r * w[j];
+        if (rstd) rstd[i] = r;
+    }
+}
+
+/* Cross-entropy loss forward (article section "让内存密集型内核达到“光速”":
+ * cross-entropy loss named as the third reduction operator).  Per row:
+ * lse = log sum_j exp(x_j) computed with the max shift, loss = lse - x_t.
+ * lse may be NULL when the caller does not want it. */
+void oracle_xent_fwd(const double *x, const int64_t *target, double *loss,
+                     double *lse, int64_t M, int64_t N)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        const double *xi = x + i * N;
+
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j)
+            if (xi[j] > m) m = xi[j];
+
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            s += exp(xi[j] - m);
+
+        double l = m + log(s);
+        int64_t t = target[i];
+        loss[i] = (t >= 0 && t < N) ? l - xi[t] : NAN;
+        if (lse) lse[i] = l;
+    }
+}

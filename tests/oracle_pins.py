@@ -1,0 +1,290 @@
+"""Pins that tie the fp64 oracle to the operators' definitions.
+
+Each ``pin_*`` function takes a loaded oracle library (``oracle.bind(path)``)
+and raises AssertionError when the library disagrees with a fact fixed by the
+mathematics: a hand-derived closed form, an invariant of the operator, or a
+50-digit brute force written here independently of the C code.  They are run
+against the real oracle (all must pass) and against deliberately broken copies
+of it (each copy must fail at least one), so a plausible slip in the oracle --
+a dropped term, a wrong sign, a wrong index, a transposed operand -- cannot
+pass unnoticed.
+
+The article (QbitAI on QuACK, section 让内存密集型内核达到“光速”) names the three
+operators but prints no formula and no worked example; these checks therefore
+follow the textbook definitions of softmax, RMSNorm and cross-entropy.
+"""
+from __future__ import annotations
+
+import ast
+import json
+import math
+import os
+import decimal
+from decimal import Decimal
+
+import numpy as np
+
+import oracle
+
+_CTX = decimal.Context(prec=50)
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "closed_forms.json")
+
+
+# --------------------------------------------------------------------------
+# 50-digit evaluation of the closed-form expressions in the golden fixture
+# --------------------------------------------------------------------------
+def dec(expr: str) -> Decimal:
+    """Evaluate an expression built from numbers, + - * /, ln(), sqrt(), exp()."""
+
+    def ev(node):
+        if isinstance(node, ast.Expression):
+            return ev(node.body)
+        if isinstance(node, ast.Constant) and isinstance(node.value, (int, float)):
+            return Decimal(str(node.value))
+        if isinstance(node, ast.UnaryOp) and isinstance(node.op, ast.USub):
+            return -ev(node.operand)
+        if isinstance(node, ast.BinOp):
+            a, b = ev(node.left), ev(node.right)
+            if isinstance(node.op, ast.Add):
+                return _CTX.add(a, b)
+            if isinstance(node.op, ast.Sub):
+                return _CTX.subtract(a, b)
+            if isinstance(node.op, ast.Mult):
+                return _CTX.multiply(a, b)
+            if isinstance(node.op, ast.Div):
+                return _CTX.divide(a, b)
+        if isinstance(node, ast.Call) and isinstance(node.func, ast.Name) and len(node.args) == 1:
+            a = ev(node.args[0])
+            fn = {"ln": _CTX.ln, "sqrt": _CTX.sqrt, "exp": _CTX.exp}.get(node.func.id)
+            if fn is not None:
+                return fn(a)
+        raise ValueError(f"unsupported expression: {expr!r}")
+
+    return ev(ast.parse(expr, mode="eval"))
+
+
+def golden_cases(op: str):
+    with open(GOLDEN) as f:
+        return [c for c in json.load(f)["cases"] if c["op"] == op]
+
+
+def _close(got, want, rel, what):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, f"{what}: shape {got.shape} != {want.shape}"
+    err = np.abs(got - want)
+    bound = rel * np.maximum(np.abs(want), 1e-300)
+    bad = ~(err <= bound)
+    assert not bad.any(), f"{what}: max rel err {float(np.max(err / np.maximum(np.abs(want), 1e-300)))} > {rel}"
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------
+# Independent 50-digit brute force, unshifted, written from the definitions
+# --------------------------------------------------------------------------
+def brute_softmax(x):
+    out = []
+    for row in x:
+        e = [_CTX.exp(Decimal(float(v))) for v in row]
+        s = sum(e, Decimal(0))
+        out.append([float(_CTX.divide(v, s)) for v in e])
+    return np.array(out)
+
+
+def brute_rmsnorm(x, w, eps):
+    ys, rs = [], []
+    for row in x:
+        n = len(row)
+        sq = sum((Decimal(float(v)) * Decimal(float(v)) for v in row), Decimal(0))
+        r = _CTX.divide(Decimal(1), _CTX.sqrt(_CTX.divide(sq, Decimal(n)) + Decimal(float(eps))))
+        ys.append([float(Decimal(float(v)) * r * Decimal(float(wj))) for v, wj in zip(row, w)])
+        rs.append(float(r))
+    return np.array(ys), np.array(rs)
+
+
+def brute_xent(x, t):
+    loss, lse = [], []
+    for row, ti in zip(x, t):
+        s = sum((_CTX.exp(Decimal(float(v))) for v in row), Decimal(0))
+        l = _CTX.ln(s)
+        lse.append(float(l))
+        loss.append(float(l - Decimal(float(row[ti]))))
+    return np.array(loss), np.array(lse)
+
+
+# --------------------------------------------------------------------------
+# Softmax pins
+# --------------------------------------------------------------------------
+def pin_softmax_golden(lib):
+    for c in golden_cases("softmax"):
+        x = np.array([[float(dec(e)) for e in r] for r in c["x"]])
+        want = np.array([[float(dec(e)) for e in r] for r in c["y"]])
+        _close(oracle.softmax_fwd(x, lib), want, c.get("rel", 1e-14), f"softmax golden {c['derivation']}")
+
+
+def pin_softmax_rows_sum_to_one(lib):
+    for seed, scale in [(1, 1.0), (2, 30.0)]:
+        x = _rng(seed).normal(0.0, scale, size=(16, 37))
+        y = oracle.softmax_fwd(x, lib)
+        assert np.all(y >= 0), "softmax: negative probability"
+        assert np.max(np.abs(y.sum(axis=1) - 1.0)) <= 1e-12, "softmax: row sum != 1"
+
+
+def pin_softmax_shift_invariance(lib):
+    x = _rng(3).normal(size=(8, 29))
+    y0 = oracle.softmax_fwd(x, lib)
+    for c in (-50.0, 3.25, 1.0e3):
+        y1 = oracle.softmax_fwd(x + c, lib)
+        assert np.max(np.abs(y1 - y0)) <= 1e-11, f"softmax: not shift invariant for c={c}"
+
+
+def pin_softmax_constant_row(lib):
+    for n, c in [(10, 7.5), (1, -3.0), (64, 0.0)]:
+        y = oracle.softmax_fwd(np.full((2, n), c), lib)
+        assert np.all(y == 1.0 / n), f"softmax: constant row of length {n} != 1/{n}"
+
+
+def pin_softmax_two_columns(lib):
+    x = _rng(4).normal(0, 3, size=(20, 2))
+    y = oracle.softmax_fwd(x, lib)
+    want = 1.0 / (1.0 + np.exp(x[:, 1] - x[:, 0]))
+    _close(y[:, 0], want, 1e-14, "softmax: N=2 logistic closed form")
+
+
+def pin_softmax_brute_force(lib):
+    x = _rng(5).normal(0, 2, size=(4, 8))
+    _close(oracle.softmax_fwd(x, lib), brute_softmax(x), 1e-14, "softmax: 4x8 brute force")
+
+
+# --------------------------------------------------------------------------
+# RMSNorm pins
+# --------------------------------------------------------------------------
+def pin_rmsnorm_golden(lib):
+    for c in golden_cases("rmsnorm"):
+        x = np.array([[float(dec(e)) for e in r] for r in c["x"]])
+        w = np.array([float(dec(e)) for e in c["w"]])
+        y, rstd = oracle.rmsnorm_fwd(x, w, float(dec(c["eps"])), lib)
+        want_y = np.array([[float(dec(e)) for e in r] for r in c["y"]])
+        want_r = np.array([float(dec(e)) for e in c["rstd"]])
+        # exact zeros in the expected output must come out as exact zeros
+        assert np.all((want_y == 0) == (y == 0)), f"rmsnorm golden zeros {c['derivation']}"
+        nz = want_y != 0
+        _close(y[nz], want_y[nz], 1e-14, f"rmsnorm golden y {c['derivation']}")
+        _close(rstd, want_r, 1e-14, f"rmsnorm golden rstd {c['derivation']}")
+
+
+def pin_rmsnorm_constant_row(lib):
+    w = _rng(6).uniform(0.5, 1.5, size=12)
+    for c in (2.5, -0.75, 1e-3):
+        y, rstd = oracle.rmsnorm_fwd(np.full((3, 12), c), w, 0.0, lib)
+        _close(y, np.sign(c) * np.broadcast_to(w, y.shape), 1e-15, f"rmsnorm: constant row {c}")
+        _close(rstd, np.full(3, 1.0 / abs(c)), 1e-15, f"rmsnorm: constant row rstd {c}")
+    # with eps > 0 the deviation from sign(c)*w stays within eps / (2 c^2)
+    c, eps = 2.0, 1e-6
+    y, _ = oracle.rmsnorm_fwd(np.full((1, 12), c), w, eps, lib)
+    assert np.max(np.abs(y / w - 1.0)) <= eps / (2 * c * c) * 1.01, "rmsnorm: eps deviation bound"
+
+
+def pin_rmsnorm_zero_row(lib):
+    w = _rng(7).uniform(0.5, 1.5, size=9)
+    eps = 1e-6
+    y, rstd = oracle.rmsnorm_fwd(np.zeros((2, 9)), w, eps, lib)
+    assert np.all(y == 0.0), "rmsnorm: zero row must map to zero"
+    _close(rstd, np.full(2, eps ** -0.5), 1e-15, "rmsnorm: zero row rstd = eps^-1/2")
+
+
+def pin_rmsnorm_scale_invariance(lib):
+    rng = _rng(8)
+    x = rng.normal(size=(5, 33))
+    w = rng.uniform(0.5, 1.5, size=33)
+    y0, r0 = oracle.rmsnorm_fwd(x, w, 0.0, lib)
+    for a in (3.5, 1e-3):
+        y1, r1 = oracle.rmsnorm_fwd(a * x, w, 0.0, lib)
+        _close(y1, y0, 1e-13, f"rmsnorm: scale invariance alpha={a}")
+        _close(r1 * a, r0, 1e-13, f"rmsnorm: rstd scales as 1/alpha, alpha={a}")
+
+
+def pin_rmsnorm_normalised_energy(lib):
+    rng = _rng(9)
+    x = rng.normal(size=(6, 41))
+    w = rng.uniform(0.5, 1.5, size=41)
+    eps = 0.1
+    y, _ = oracle.rmsnorm_fwd(x, w, eps, lib)
+    ms = np.mean(x * x, axis=1)
+    _close(np.mean((y / w) ** 2, axis=1), ms / (ms + eps), 1e-13, "rmsnorm: mean (y/w)^2 = ms/(ms+eps)")
+
+
+def pin_rmsnorm_brute_force(lib):
+    rng = _rng(10)
+    x = rng.normal(size=(4, 8))
+    w = rng.uniform(0.5, 1.5, size=8)
+    y, r = oracle.rmsnorm_fwd(x, w, 1e-6, lib)
+    by, br = brute_rmsnorm(x, w, 1e-6)
+    _close(y, by, 1e-14, "rmsnorm: 4x8 brute force y")
+    _close(r, br, 1e-14, "rmsnorm: 4x8 brute force rstd")
+
+
+# --------------------------------------------------------------------------
+# Cross-entropy pins
+# --------------------------------------------------------------------------
+def pin_xent_golden(lib):
+    for c in golden_cases("xent"):
+        x = np.array([[float(dec(e)) for e in r] for r in c["x"]])
+        loss, lse = oracle.xent_fwd(x, np.array(c["target"], dtype=np.int64), lib)
+        _close(loss, [float(dec(e)) for e in c["loss"]], 1e-14, f"xent golden loss {c['derivation']}")
+        _close(lse, [float(dec(e)) for e in c["lse"]], 1e-14, f"xent golden lse {c['derivation']}")
+
+
+def pin_xent_is_minus_log_softmax(lib):
+    rng = _rng(11)
+    x = rng.normal(0, 2 ** 0.5, size=(12, 50))
+    t = rng.integers(0, 50, size=12)
+    loss, _ = oracle.xent_fwd(x, t, lib)
+    p = oracle.softmax_fwd(x, lib)[np.arange(12), t]
+    _close(loss, -np.log(p), 1e-12, "xent: loss = -log softmax(x)[t]")
+
+
+def pin_xent_constant_row(lib):
+    for n, c in [(7, 0.0), (1000, -4.25)]:
+        loss, lse = oracle.xent_fwd(np.full((2, n), c), np.array([0, n - 1]), lib)
+        _close(loss, np.full(2, math.log(n)), 1e-14, f"xent: constant row loss = ln {n}")
+        _close(lse, np.full(2, c + math.log(n)), 1e-14, f"xent: constant row lse = c + ln {n}")
+
+
+def pin_xent_single_column(lib):
+    x = np.array([[3.5], [-2.0]])
+    loss, lse = oracle.xent_fwd(x, np.array([0, 0]), lib)
+    assert np.all(loss == 0.0), "xent: N=1 loss must be 0"
+    assert np.all(lse == x[:, 0]), "xent: N=1 lse must equal the logit"
+
+
+def pin_xent_bounds(lib):
+    rng = _rng(12)
+    x = rng.normal(0, 3, size=(10, 64))
+    loss, lse = oracle.xent_fwd(x, rng.integers(0, 64, size=10), lib)
+    mx = x.max(axis=1)
+    assert np.all(lse >= mx) and np.all(lse <= mx + math.log(64) + 1e-12), "xent: max <= lse <= max + ln N"
+    assert np.all(loss >= 0), "xent: loss must be non-negative"
+
+
+def pin_xent_out_of_range_target(lib):
+    x = _rng(13).normal(size=(3, 6))
+    loss, lse = oracle.xent_fwd(x, np.array([6, -1, 2]), lib)
+    assert np.isnan(loss[0]) and np.isnan(loss[1]), "xent: out-of-range target must give NaN"
+    assert np.isfinite(loss[2]) and np.all(np.isfinite(lse)), "xent: in-range rows stay finite"
+
+
+def pin_xent_brute_force(lib):
+    rng = _rng(14)
+    x = rng.normal(0, 2 ** 0.5, size=(4, 8))
+    t = rng.integers(0, 8, size=4)
+    loss, lse = oracle.xent_fwd(x, t, lib)
+    bl, bs = brute_xent(x, t)
+    _close(lse, bs, 1e-14, "xent: 4x8 brute force lse")
+    _close(loss, bl, 1e-13, "xent: 4x8 brute force loss")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,57 @@
+"""Plant plausible mistakes in a copy of the oracle and check the pins catch
+every one.  The mutated copies are compiled into a temporary directory and
+loaded beside the real oracle; nothing here touches a GPU or the CUDA path."""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (description, original text, planted mistake); each original must occur in
+# oracle.c exactly once.
+MUTANTS = [
+    ("softmax: sign of the shift", "s += exp(xi[j] - m);\n\n        for (int64_t j = 0; j < N; ++j)\n            yi[j]",
+     "s += exp(xi[j] + m);\n\n        for (int64_t j = 0; j < N; ++j)\n            yi[j]"),
+    ("softmax: shift dropped from the sum", "s += exp(xi[j] - m);\n\n        for (int64_t j = 0; j < N; ++j)\n            yi[j]",
+     "s += exp(xi[j]);\n\n        for (int64_t j = 0; j < N; ++j)\n            yi[j]"),
+    ("softmax: multiply instead of divide", "yi[j] = exp(xi[j] - m) / s;", "yi[j] = exp(xi[j] - m) * s;"),
+    ("softmax: min instead of max", "    double *yi = y + i * N;\n\n        double m = -INFINITY;\n        for (int64_t j = 0; j < N; ++j)\n            if (xi[j] > m)",
+     "    double *yi = y + i * N;\n\n        double m = INFINITY;\n        for (int64_t j = 0; j < N; ++j)\n            if (xi[j] < m)"),
+    ("softmax: transposed row stride", "const double *xi = x + i * N;\n        double *yi = y + i * N;\n\n        double m",
+     "const double *xi = x + i * M;\n        double *yi = y + i * N;\n\n        double m"),
+    ("softmax: no shift at all", "yi[j] = exp(xi[j] - m) / s;", "yi[j] = exp(xi[j]) / s;"),
+    ("rmsnorm: divide by N-1", "sum_sq / (double)N", "sum_sq / (double)(N - 1)"),
+    ("rmsnorm: eps outside the root", "1.0 / sqrt(ms + eps)", "1.0 / (sqrt(ms) + eps)"),
+    ("rmsnorm: square dropped", "sum_sq += xi[j] * xi[j];", "sum_sq += xi[j];"),
+    ("rmsnorm: weight indexed by row", "yi[j] = xi[j] * r * w[j];", "yi[j] = xi[j] * r * w[i];"),
+    ("rmsnorm: weight dropped", "yi[j] = xi[j] * r * w[j];", "yi[j] = xi[j] * r;"),
+    ("rmsnorm: rms instead of its reciprocal", "double r = 1.0 / sqrt(ms + eps);", "double r = sqrt(ms + eps);"),
+    ("rmsnorm: eps times the mean", "1.0 / sqrt(ms + eps)", "1.0 / sqrt(ms * (1.0 + eps))"),
+    ("xent: sign of the loss", "l - xi[t]", "xi[t] - l"),
+    ("xent: max dropped from lse", "double l = m + log(s);", "double l = log(s);"),
+    ("xent: target column off by one", "l - xi[t]", "l - xi[t > 0 ? t - 1 : t]"),
+    ("xent: log2 instead of ln", "double l = m + log(s);", "double l = m + log2(s);"),
+    ("xent: no range check", "(t >= 0 && t < N) ? l - xi[t] : NAN", "(t > -2 && t <= N) ? l - xi[t] : NAN"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(oracle.SOURCE) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("desc,orig,bad", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(desc, orig, bad, source, tmp_path):
+    assert source.count(orig) == 1, f"mutation anchor not unique for {desc!r}"
+    src = tmp_path / "mutant.c"
+    src.write_text(source.replace(orig, bad))
+    lib = oracle.bind(oracle.compile_library(str(src), str(tmp_path / f"mutant_{abs(hash(desc))}.so")))
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except Exception as e:  # an assertion or any breakdown counts as detection
+            caught.append(f"{pin.__name__}: {e}")
+    assert caught, f"no pin detects the planted mistake: {desc}"

@@ -1,0 +1,16 @@
+"""The fp64 oracle against its pins: closed forms, invariants, brute force."""
+import pytest
+
+import oracle
+import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(pin):
+    pin(oracle.library())
+
+
+def test_every_operator_is_pinned():
+    names = [p.__name__ for p in oracle_pins.ALL_PINS]
+    for op in ("softmax", "rmsnorm", "xent"):
+        assert sum(n.startswith(f"pin_{op}_") for n in names) >= 5, op
