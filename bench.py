@@ -1,0 +1,437 @@
+"""Benchmark of the row-reduction kernels: effective HBM TB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one call of the operator over one batch (the full M x N matrix of
+the workload) with its inputs already resident in HBM.  The metric is the
+effective memory throughput: the minimal bytes the operator must move (read
+every input once, write every output once) divided by the device time.
+
+Timing: W warm-up steps, then K steps between CUDA events on the launching
+stream, with a barrier and synchronize on both sides; the max over ranks is
+taken.  Input/output sets rotate over more than 4x the L2 size, so no step
+finds its data in L2.  SM clocks and throttle reasons are sampled with
+nvidia-smi during the timed region.
+
+Multi-GPU (torchrun, one rank per GPU): rows are independent, so each rank
+processes its own batch of the same shape (weak scaling, no collective on the
+data path; one max-reduction of the elapsed time after the timed region).
+
+--impl reference times the fp64 CPU oracle on the host cores instead (rank 0
+only), each step a bounded sample of rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from memory_bound_row_rmsnorm_gb300 import synthetic as syn  # noqa: E402
+
+L2_BYTES = 129 * 10 ** 6
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "effective HBM TB/s and % of GB300 peak per kernel over the M×N sweep"
+ESIZE = {"f32": 4, "bf16": 2}
+DEFAULT_WORKLOAD = "rmsnorm_bf16_16384x4096"
+EPS = 1e-6
+
+
+def min_bytes(op: str, dtype: str, M: int, N: int) -> int:
+    """Algorithmic bytes of one call: every input read once, every output written once."""
+    s = ESIZE[dtype]
+    if op == "softmax":
+        return 2 * M * N * s
+    if op == "rmsnorm":
+        return 2 * M * N * s + N * s + 4 * M
+    return M * N * s + 8 * M + 8 * M  # logits + targets in; loss + lse out
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "memory_bound_row_rmsnorm_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", f"{workload}.traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_set(op, dtype, M, N, sigma, seed, dev):
+    inp = syn.make_inputs(op, dtype, M, N, seed, dev, sigma)
+    out = {}
+    if op in ("softmax", "rmsnorm"):
+        out["y"] = torch.empty_like(inp["x"])
+    if op == "rmsnorm":
+        out["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
+    if op == "xent":
+        out["loss"] = torch.empty(M, dtype=torch.float32, device=dev)
+        out["lse"] = torch.empty(M, dtype=torch.float32, device=dev)
+    return inp, out
+
+
+def launch(qb, op, dtype, inp, out, M, N, stream):
+    code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
+    if op == "softmax":
+        qb.qk_softmax_fwd(inp["x"], out["y"], M, N, code, stream)
+    elif op == "rmsnorm":
+        qb.qk_rmsnorm_fwd(inp["x"], inp["w"], out["y"], out["rstd"], M, N, EPS, code, stream)
+    else:
+        qb.qk_xent_fwd(inp["x"], inp["targets"], out["loss"], out["lse"], M, N, code, stream)
+
+
+def cpu_oracle_rate(op, dtype, M, N, sigma, budget_s: float, seed: int = 4242):
+    """The fp64 oracle, as it stands, over seeded rows of the workload on all
+    host cores (one thread per core, each running the oracle on its own rows).
+    Returns (TB/s, cores, sample description, seconds)."""
+    import concurrent.futures as cf
+
+    import oracle
+
+    cores = os.cpu_count() or 1
+    lib = oracle.library()
+    rows = min(M, max(cores, 64))
+    inp = syn.make_inputs(op, dtype, rows, N, seed, "cpu", sigma)
+    x = inp["x"].to(torch.float64).numpy()
+    w = inp["w"].to(torch.float64).numpy() if op == "rmsnorm" else None
+    t = inp["targets"].numpy() if op == "xent" else None
+    parts = np.array_split(np.arange(rows), cores)
+
+    def work(idx):
+        if idx.size == 0:
+            return
+        sl = slice(int(idx[0]), int(idx[-1]) + 1)
+        if op == "softmax":
+            oracle.softmax_fwd(x[sl], lib)
+        elif op == "rmsnorm":
+            oracle.rmsnorm_fwd(x[sl], w, EPS, lib)
+        else:
+            oracle.xent_fwd(x[sl], t[sl], lib)
+
+    reps = 0
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(work, parts))  # warm
+        t0 = time.perf_counter()
+        while True:
+            list(ex.map(work, parts))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    nbytes = min_bytes(op, dtype, rows, N) * reps
+    sample = (f"{reps} passes over {rows} seeded rows x {N} of the workload "
+              f"({rows * reps} rows, {el:.1f} s), {cores} threads")
+    return nbytes / el / 1e12, cores, sample, el
+
+
+def run_reference(args, op, dtype, M, N, sigma):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle  # noqa: F401  (builds the C oracle on first use)
+
+    K, W = args.steps, args.warmup
+    # calibrate rows per step so the whole run stays within ~2 minutes
+    rate, cores, _, _ = cpu_oracle_rate(op, dtype, M, N, sigma, budget_s=1.0)
+    per_row = min_bytes(op, dtype, 1, N)
+    budget = 120.0 / max(1, K + W)
+    rows = int(max(1, min(M, rate * 1e12 * budget / per_row)))
+    import concurrent.futures as cf
+
+    lib = oracle.library()
+    inp = syn.make_inputs(op, dtype, rows, N, 4343, "cpu", sigma)
+    x = inp["x"].to(torch.float64).numpy()
+    w = inp["w"].to(torch.float64).numpy() if op == "rmsnorm" else None
+    t = inp["targets"].numpy() if op == "xent" else None
+    parts = [p for p in np.array_split(np.arange(rows), cores) if p.size]
+
+    def work(idx):
+        sl = slice(int(idx[0]), int(idx[-1]) + 1)
+        if op == "softmax":
+            oracle.softmax_fwd(x[sl], lib)
+        elif op == "rmsnorm":
+            oracle.rmsnorm_fwd(x[sl], w, EPS, lib)
+        else:
+            oracle.xent_fwd(x[sl], t[sl], lib)
+
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        for _ in range(W):
+            list(ex.map(work, parts))
+        t0 = time.perf_counter()
+        for _ in range(K):
+            list(ex.map(work, parts))
+        el = time.perf_counter() - t0
+    value = min_bytes(op, dtype, rows, N) * K / el / 1e12
+    sample = f"each step: {rows} seeded rows x {N} of the workload on {cores} threads"
+    line = {
+        "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "op": op, "M": M, "N": N, "input_dtype": dtype,
+                   "rows_per_step": rows},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    op, dtype, M, N, sigma = syn.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, op, dtype, M, N, sigma)
+        return
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device(f"cuda:{local}")
+
+    from memory_bound_row_rmsnorm_gb300 import binding as qb
+    from memory_bound_row_rmsnorm_gb300 import build as qk_build
+    if rank == 0 or ws == 1:
+        qk_build.build()
+    if ws > 1:
+        dist.barrier()
+    qb.load_library()
+
+    # rotating input/output sets: > 4x L2 in total
+    set_bytes = min_bytes(op, dtype, M, N)
+    nsets = max(2, math.ceil(4 * L2_BYTES / set_bytes))
+    sets = [make_set(op, dtype, M, N, sigma, 1000 + 17 * rank + i, dev) for i in range(nsets)]
+    stream = torch.cuda.current_stream(dev)
+    code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
+    opcode = {"softmax": qb.QK_OP_SOFTMAX, "rmsnorm": qb.QK_OP_RMSNORM, "xent": qb.QK_OP_XENT}[op]
+    plan = qb.qk_get_plan(opcode, code, M, N)
+
+    for i in range(args.warmup):
+        inp, out = sets[i % nsets]
+        launch(qb, op, dtype, inp, out, M, N, stream)
+    torch.cuda.synchronize(dev)
+    if qb.qk_get_device_status(stream) != qb.QK_OK:
+        raise RuntimeError("device status reports a failure after warm-up")
+
+    K = args.steps
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(K):
+            inp, out = sets[i % nsets]
+            launch(qb, op, dtype, inp, out, M, N, stream)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    if ws > 1:
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    status = qb.qk_get_device_status(stream)
+    if status != qb.QK_OK:
+        raise RuntimeError(f"device status: {qb.qk_status_string(status)}")
+
+    per_launch_s = elapsed_ms / 1e3 / K
+    bytes_per_launch = set_bytes
+    value = bytes_per_launch * ws * K / (elapsed_ms / 1e3) / 1e12
+    peak, peak_src = measured_peak()
+    achieved_gbs = bytes_per_launch / per_launch_s / 1e9
+    traffic = recorded_traffic(args.workload)
+
+    # ---- end to end: pinned host buffers, copies inside the timed region ----
+    inp0, out0 = sets[0]
+    h_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v) for k, v in inp0.items()}
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out0.items()}
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    E = max(3, args.e2e_steps)
+    for i in range(2):
+        for k in inp0:
+            inp0[k].copy_(h_in[k], non_blocking=True)
+        launch(qb, op, dtype, inp0, out0, M, N, stream)
+        for k in out0:
+            h_out[k].copy_(out0[k], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(E):
+        for k in inp0:
+            inp0[k].copy_(h_in[k], non_blocking=True)
+        launch(qb, op, dtype, inp0, out0, M, N, stream)
+        for k in out0:
+            h_out[k].copy_(out0[k], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = set_bytes * ws * E / (e2e_ms / 1e3) / 1e12
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if ws == 1 and args.cpu_seconds > 0:
+        rate, cores, sample, _ = cpu_oracle_rate(op, dtype, M, N, sigma, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "TB/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TB/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if dtype == "f32" else "bf16 in/out, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "op": op, "M": M, "N": N, "input_dtype": dtype,
+                   "rows_per_gpu": M, "l2": f"{nsets} rotating input/output sets "
+                   f"({nsets * set_bytes / 2**20:.0f} MiB) > 4x L2", "plan": plan},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "traffic": traffic, "peak_source": peak_src,
+                     "bytes_per_launch": bytes_per_launch},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": E},
+        "gpu_launches": K,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * qk.h -- C ABI of the GB300 row-reduction library (libqk.so).
+ *
+ * Three forward operators over a row-major M x N matrix, each reading every
+ * input element from HBM once and writing every output element once:
+ *
+ *   qk_softmax_fwd   y[i, :] = softmax(x[i, :])
+ *   qk_rmsnorm_fwd   y[i, :] = x[i, :] * rstd[i] * w[:],
+ *                    rstd[i] = 1 / sqrt(mean_j x[i, j]^2 + eps)
+ *   qk_xent_fwd      lse[i]  = log sum_j exp(x[i, j]),  loss[i] = lse[i] - x[i, t[i]]
+ *
+ * The operators are the three reductions named in the QbitAI article on QuACK
+ * ("无需CUDA代码，给H100加速33%-50%"), section "让内存密集型内核达到“光速”"
+ * (RMSNorm, softmax and cross-entropy loss), benchmarked forward-only in its
+ * section "内存吞吐量" (fp32 and bf16, batch 8k-32k rows, 256-262k columns).
+ * The article gives no formulas; the textbook definitions above are used.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers are DEVICE pointers owned by the caller (for example the
+ *    data_ptr() of CUDA tensors).  The library keeps no reference to them
+ *    after the call is enqueued and allocates no device memory per call.
+ *  - Matrices are dense and row-major with row stride N elements.  x, y and w
+ *    have the element type `dtype`; rstd, loss and lse are float32; targets are
+ *    int64.
+ *  - Every call is asynchronous: it validates its arguments on the host, then
+ *    enqueues kernels on `stream` (a cudaStream_t; NULL means the legacy
+ *    default stream) on the calling thread's current device and returns.
+ *  - Argument errors are returned synchronously and nothing is launched.  A
+ *    launch failure returns QK_ERR_LAUNCH.  Device-side failures (a bounded
+ *    wait inside a kernel that ran out) are recorded in a per-device status
+ *    word that qk_get_device_status() reads and clears.
+ *  - M == 0 is a no-op returning QK_OK.  N <= 0 or M < 0 is QK_ERR_INVALID_ARG.
+ *  - Pointers must be aligned to their element size (QK_ERR_MISALIGNED
+ *    otherwise).  The fast path additionally wants 16-byte aligned x, y, w and
+ *    N * sizeof(dtype) a multiple of 16; other inputs take a slower masked
+ *    path that gives the same results.
+ *  - Accumulation is float32; bf16 outputs are rounded to nearest even once.
+ */
+#ifndef QK_H_
+#define QK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QK_API __attribute__((visibility("default")))
+#else
+#define QK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { QK_F32 = 0, QK_BF16 = 1 } qk_dtype;
+
+typedef enum { QK_OP_SOFTMAX = 0, QK_OP_RMSNORM = 1, QK_OP_XENT = 2 } qk_op;
+
+typedef enum {
+  QK_OK = 0,
+  QK_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad dtype, overlapping buffers */
+  QK_ERR_UNSUPPORTED = 2, /* row longer than the largest plan (see qk_max_row_elements) */
+  QK_ERR_MISALIGNED = 3,  /* a pointer not aligned to its element size */
+  QK_ERR_LAUNCH = 4,      /* the CUDA runtime refused a launch or a query */
+  QK_ERR_TIMEOUT = 5,     /* a bounded wait inside a kernel ran out (device status) */
+  QK_ERR_NO_DEVICE = 6    /* no usable CUDA device, or not an sm_103 device */
+} qk_status;
+
+/*
+ * Softmax forward.  For each row i: m = max_j x[i,j];
+ * y[i,j] = exp(x[i,j] - m) / sum_k exp(x[i,k] - m).
+ * Cited: QbitAI article on QuACK, section "让内存密集型内核达到“光速”" (softmax as
+ * a reduction over the row) and section "内存吞吐量" (three sweeps: maximum, sum
+ * of exponentials, normalisation; here the first two are fused on chip).
+ *
+ *   x      [M, N] dtype, read once.
+ *   y      [M, N] dtype, written once.  y == x (exact aliasing) is allowed;
+ *          any other overlap with x is QK_ERR_INVALID_ARG.
+ *   M, N   rows and columns; N <= qk_max_row_elements(QK_OP_SOFTMAX, dtype).
+ */
+QK_API qk_status qk_softmax_fwd(const void* x, void* y, int64_t M, int64_t N, qk_dtype dtype,
+                         void* stream);
+
+/*
+ * RMSNorm forward.  For each row i: rstd[i] = 1 / sqrt((1/N) sum_j x[i,j]^2 + eps);
+ * y[i,j] = x[i,j] * rstd[i] * w[j]  (eps inside the root, plain weight, no bias).
+ * Cited: QbitAI article on QuACK, section "让内存密集型内核达到“光速”" (RMSNorm as a
+ * reduction over the row).
+ *
+ *   x      [M, N] dtype, read once.
+ *   w      [N] dtype, read once per CTA (cached on chip).
+ *   y      [M, N] dtype, written once; y == x allowed, other overlaps rejected.
+ *   rstd   [M] float32, written once; may be NULL when not wanted.
+ *   eps    added to the mean of squares; must be finite and >= 0.
+ */
+QK_API qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M,
+                         int64_t N, float eps, qk_dtype dtype, void* stream);
+
+/*
+ * Cross-entropy loss forward, one value per row (no reduction over rows, no
+ * ignore index, no label smoothing).  For each row i: lse[i] = log sum_j
+ * exp(x[i,j]); loss[i] = lse[i] - x[i, targets[i]].  A target outside [0, N)
+ * yields loss[i] = NaN (lse[i] is still written); nothing is read out of bounds.
+ * Cited: QbitAI article on QuACK, section "让内存密集型内核达到“光速”" (cross-entropy
+ * loss as the third reduction) and section "内存吞吐量" (an online softmax when
+ * the row does not fit on chip: the row is streamed through shared memory).
+ *
+ *   logits  [M, N] dtype, read once.
+ *   targets [M] int64.
+ *   loss    [M] float32, written once.
+ *   lse     [M] float32, written once; may be NULL when not wanted.
+ *   Any N >= 1 is supported.
+ */
+QK_API qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* loss, float* lse,
+                      int64_t M, int64_t N, qk_dtype dtype, void* stream);
+
+/* Static English description of a status code; never NULL. */
+QK_API const char* qk_status_string(qk_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the calling device's status
+ * word.  Returns QK_OK when no kernel has reported a failure since the last
+ * call, or the first failure recorded (QK_ERR_TIMEOUT).  A CUDA error from the
+ * synchronisation itself is returned as QK_ERR_LAUNCH.
+ */
+QK_API qk_status qk_get_device_status(void* stream);
+
+/* Largest N the operator accepts for `dtype` (rows longer than this return
+ * QK_ERR_UNSUPPORTED); INT64_MAX for qk_xent_fwd, which streams its rows. */
+QK_API int64_t qk_max_row_elements(qk_op op, qk_dtype dtype);
+
+/*
+ * Launch plan: how a call maps onto the GPU.  Reported by qk_get_plan() for
+ * logging and benchmarks; qk_set_plan_override() pins one for tuning sweeps.
+ *
+ *   path            1 = TMA ring (aligned fast path), 2 = masked direct path.
+ *   threads         threads per CTA.
+ *   row_threads     threads that share one row inside a CTA (rows per CTA
+ *                   step = threads / row_threads).
+ *   vec_per_thread  16-byte vectors each thread holds per row (or per chunk
+ *                   for streamed rows); elements per thread on the masked path.
+ *   cluster         CTAs of a thread-block cluster that split one row
+ *                   (1 = no cluster); partial results meet in DSMEM.
+ *   slots           shared-memory ring slots per CTA (TMA loads in flight).
+ *   chunks          ring slots one row slice spans (> 1 only for streamed rows).
+ *   ctas_per_sm     resident CTAs per SM the launch was sized for.
+ *   grid            CTAs launched (persistent: each loops over its share).
+ *   smem_bytes      dynamic shared memory per CTA.
+ */
+typedef struct {
+  int32_t path;
+  int32_t threads;
+  int32_t row_threads;
+  int32_t vec_per_thread;
+  int32_t cluster;
+  int32_t slots;
+  int32_t chunks;
+  int32_t ctas_per_sm;
+  int32_t grid;
+  int32_t smem_bytes;
+} qk_plan;
+
+/*
+ * Fills *plan with what a call with these sizes would launch on the current
+ * device (aligned pointers assumed).  Returns QK_ERR_UNSUPPORTED for rows that
+ * are too long and QK_ERR_INVALID_ARG for bad sizes.
+ */
+QK_API qk_status qk_get_plan(qk_op op, qk_dtype dtype, int64_t M, int64_t N, qk_plan* plan);
+
+/*
+ * Tuning hook: every later aligned-path call of (op, dtype) uses `plan`'s
+ * threads, row_threads, vec_per_thread, cluster, slots and chunks instead of
+ * the built-in table (chunks and ctas_per_sm are recomputed; a zero slots
+ * field keeps the table's rule; a positive grid caps the number of CTAs, which
+ * makes each CTA walk more rows -- a test of the ring's reuse).  plan == NULL removes the override.
+ * Returns QK_ERR_UNSUPPORTED when no compiled kernel matches the triple
+ * (threads, row_threads, vec_per_thread).  Process-wide, not thread-safe
+ * against concurrent calls of the same operator.
+ */
+QK_API qk_status qk_set_plan_override(qk_op op, qk_dtype dtype, const qk_plan* plan);
+
+/*
+ * Test hook for the device-side failure path.  Enqueues one CTA that waits on
+ * a shared-memory barrier nobody completes, bounded by `timeout_ns`; when the
+ * bound runs out the kernel records QK_ERR_TIMEOUT in the device status word
+ * and returns normally (no trap, no fault).  qk_get_device_status() then
+ * reports it.  timeout_ns must be in (0, 10 s].
+ */
+QK_API qk_status qk_test_wait_timeout(uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QK_H_ */

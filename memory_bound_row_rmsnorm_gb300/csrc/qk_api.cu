@@ -1,0 +1,568 @@
+// qk_api.cu -- the C ABI of libqk.so: argument checks, launch plans, launches.
+//
+// Host side only: every element of every row is processed by the kernels in
+// qk_kernels.cuh; nothing here touches row data.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/qk.h"
+#include "qk_device.cuh"
+#include "qk_internal.h"
+
+namespace qk {
+
+// Device status word: the first failure code a kernel reports (0 = none).
+__device__ int g_status_word;
+
+__global__ void wait_timeout_kernel(uint64_t timeout_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_addr(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  // Nobody arrives on `bar`, so phase 0 never completes.
+  if (!mbar_wait<false>(b, 0u, timeout_ns)) report_status(status, QK_ERR_TIMEOUT);
+}
+
+namespace {
+
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s bound on any in-kernel wait
+constexpr int kMaxDevices = 64;
+constexpr int kRingMaxVectorsPerCta = 4096;  // 512 threads x 8 vectors
+constexpr int64_t kMaxRowBytes = int64_t(kMaxCluster) * kRingMaxVectorsPerCta * 16;  // 1 MiB
+
+struct DeviceInfo {
+  bool ready = false;
+  qk_status error = QK_OK;
+  int sms = 0;
+  int smem_optin = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+std::map<std::tuple<int, const void*>, bool> g_attr_done;
+std::map<std::tuple<int, const void*, int, int>, int> g_occ;  // (dev, func, smem, C) -> CTAs/SM or clusters
+
+struct Override {
+  bool on = false;
+  qk_plan plan{};
+};
+Override g_override[3][2];
+
+KernelTable table_for(int op, int dt) {
+  switch (op * 2 + dt) {
+    case 0: return kernels_softmax_f32();
+    case 1: return kernels_softmax_bf16();
+    case 2: return kernels_rmsnorm_f32();
+    case 3: return kernels_rmsnorm_bf16();
+    case 4: return kernels_xent_f32();
+    default: return kernels_xent_bf16();
+  }
+}
+
+const KernelEntry* find_kernel(int op, int dt, int path, int threads, int tpr, int vpt,
+                               bool clustered) {
+  const KernelTable t = table_for(op, dt);
+  for (int i = 0; i < t.count; ++i) {
+    const KernelEntry& e = t.entries[i];
+    if (e.path == path && e.threads == threads && e.row_threads == tpr &&
+        e.vec_per_thread == vpt && e.clustered == clustered)
+      return &e;
+  }
+  return nullptr;
+}
+
+// Per-device facts, read once under the lock.
+qk_status device_info(int* dev_out, DeviceInfo** info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return QK_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    d.ready = true;
+    cudaDeviceProp p;
+    if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) {
+      cudaGetLastError();
+      d.error = QK_ERR_NO_DEVICE;
+    } else if (!(p.major == 10 && p.minor == 3)) {
+      d.error = QK_ERR_NO_DEVICE;  // the kernels are built for sm_103a only
+    } else {
+      d.sms = p.multiProcessorCount;
+      d.smem_optin = int(p.sharedMemPerBlockOptin);
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        d.error = QK_ERR_LAUNCH;
+      } else {
+        d.status = static_cast<int*>(ptr);
+      }
+    }
+  }
+  *dev_out = dev;
+  *info = &d;
+  return d.error;
+}
+
+// Opt a kernel into the device's full shared memory (and non-portable
+// clusters) once per device.
+qk_status prepare_kernel(int dev, const DeviceInfo& d, const KernelEntry& k) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto key = std::make_tuple(dev, k.func);
+  if (g_attr_done.count(key)) return QK_OK;
+  if (k.path == 1 &&
+      cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_LAUNCH;
+  }
+  if (k.clustered &&
+      cudaFuncSetAttribute(k.func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_LAUNCH;
+  }
+  g_attr_done[key] = true;
+  return QK_OK;
+}
+
+// Resident CTAs per SM (cluster == 0) or resident clusters on the device.
+qk_status occupancy(int dev, const KernelEntry& k, int smem, int cluster, int* out) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_occ.find(std::make_tuple(dev, k.func, smem, cluster));
+    if (it != g_occ.end()) {
+      *out = it->second;
+      return QK_OK;
+    }
+  }
+  int n = 0;
+  cudaError_t err;
+  if (cluster == 0) {
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k.func, k.threads, size_t(smem));
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(cluster), 1, 1);
+    cfg.blockDim = dim3(unsigned(k.threads), 1, 1);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaOccupancyMaxActiveClusters(&n, k.func, &cfg);
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_occ[std::make_tuple(dev, k.func, smem, cluster)] = n;
+  *out = n;
+  return QK_OK;
+}
+
+int elem_size(int dt) { return dt == QK_F32 ? 4 : 2; }
+
+int next_pow2(int64_t v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+struct Plan {
+  const KernelEntry* kernel = nullptr;
+  int cluster = 1;
+  int slots = 0;
+  int chunks = 1;
+  int64_t num_items = 0;
+  uint32_t slot_bytes = 0;
+  int smem = 0;
+  int ctas_per_sm = 0;
+  int64_t grid = 0;
+};
+
+// Chooses the ring kernel (fast path) for a row of NV 16-byte vectors.
+qk_status choose_ring(int op, int dt, int64_t NV, int* th, int* tpr, int* vpt, int* cl, int* k) {
+  *cl = 1;
+  *k = 1;
+  if (op == kXent && NV > kRingMaxVectorsPerCta) {  // stream long rows in 32 KB chunks
+    *th = 512, *tpr = 512, *vpt = 4;
+    *k = int((NV + 2047) / 2048);
+    return QK_OK;
+  }
+  if (NV <= 32) *th = 256, *tpr = 32, *vpt = 1;
+  else if (NV <= 64) *th = 256, *tpr = 32, *vpt = 2;
+  else if (NV <= 128) *th = 256, *tpr = 32, *vpt = 4;
+  else if (NV <= 256) *th = 256, *tpr = 64, *vpt = 4;
+  else if (NV <= 512) *th = 256, *tpr = 128, *vpt = 4;
+  else if (NV <= 1024) *th = 256, *tpr = 256, *vpt = 4;
+  else if (NV <= 2048) *th = 512, *tpr = 512, *vpt = 4;
+  else {
+    *th = 512, *tpr = 512, *vpt = 8;
+    const int64_t c = (NV + kRingMaxVectorsPerCta - 1) / kRingMaxVectorsPerCta;
+    if (c > kMaxCluster) return QK_ERR_UNSUPPORTED;
+    *cl = c > 1 ? next_pow2(c) : 1;
+  }
+  (void)dt;
+  return QK_OK;
+}
+
+qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p) {
+  const int E = 16 / elem_size(dt);
+  const int64_t NV = N / E;
+  int th, tpr, vpt, cl, k;
+  int slots = 0;
+  const Override& ov = g_override[op][dt];
+  if (ov.on) {
+    th = ov.plan.threads, tpr = ov.plan.row_threads, vpt = ov.plan.vec_per_thread;
+    cl = std::max(1, int(ov.plan.cluster));
+    slots = ov.plan.slots;
+    const int64_t per_cta = int64_t(tpr) * vpt;
+    const int64_t slice = (NV + cl - 1) / cl;
+    if (cl > kMaxCluster || (cl > 1 && tpr != th)) return QK_ERR_UNSUPPORTED;
+    if (slice <= per_cta) {
+      k = 1;
+    } else if (op == kXent && cl == 1 && tpr == th) {
+      k = int((NV + per_cta - 1) / per_cta);
+    } else {
+      return QK_ERR_UNSUPPORTED;
+    }
+  } else {
+    qk_status st = choose_ring(op, dt, NV, &th, &tpr, &vpt, &cl, &k);
+    if (st != QK_OK) return st;
+  }
+  const KernelEntry* ke = find_kernel(op, dt, 1, th, tpr, vpt, cl > 1);
+  if (ke == nullptr) return QK_ERR_UNSUPPORTED;
+
+  int64_t item_bytes;
+  if (k > 1) {
+    item_bytes = int64_t(tpr) * vpt * 16;
+    p->num_items = M;
+  } else if (cl > 1) {
+    item_bytes = (NV + cl - 1) / cl * 16;
+    p->num_items = M;
+  } else {
+    const int R = th / tpr;
+    item_bytes = int64_t(R) * NV * 16;
+    p->num_items = (M + R - 1) / R;
+  }
+  const uint32_t slot_bytes = uint32_t((item_bytes + 127) / 128 * 128);
+  if (slots <= 0) {
+    const int64_t budget = k > 1 ? 196608 : (cl > 1 ? 196608 : 65536);
+    slots = int(std::min<int64_t>(cl > 1 ? 4 : 8, std::max<int64_t>(2, budget / slot_bytes)));
+  }
+  slots = std::min(slots, kMaxSlots);
+  while (slots > 1 && kSmemHeader + int64_t(slots) * slot_bytes > d.smem_optin) --slots;
+  const int64_t smem = kSmemHeader + int64_t(slots) * slot_bytes;
+  if (smem > d.smem_optin) return QK_ERR_UNSUPPORTED;
+
+  qk_status st = prepare_kernel(dev, d, *ke);
+  if (st != QK_OK) return st;
+  int occ = 0;
+  st = occupancy(dev, *ke, int(smem), cl > 1 ? cl : 0, &occ);
+  if (st != QK_OK) return st;
+  if (occ <= 0) return QK_ERR_UNSUPPORTED;
+
+  p->kernel = ke;
+  p->cluster = cl;
+  p->slots = slots;
+  p->chunks = k;
+  p->slot_bytes = slot_bytes;
+  p->smem = int(smem);
+  // Persistent grid: every resident CTA (or cluster) once, at most one per item.
+  int64_t units = cl > 1 ? int64_t(occ) : int64_t(occ) * d.sms;
+  if (ov.on && ov.plan.grid > 0) units = std::min<int64_t>(units, std::max(1, ov.plan.grid / cl));
+  units = std::min<int64_t>(units, p->num_items);
+  p->ctas_per_sm = cl > 1 ? std::max(1, occ * cl / std::max(1, d.sms)) : occ;
+  p->grid = units * cl;
+  return QK_OK;
+}
+
+// Masked direct path: one row per CTA, or per cluster for long rows.
+qk_status plan_direct(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p) {
+  int th, ept, cl = 1;
+  bool clustered = false;
+  if (N <= 512) th = 128, ept = 4;
+  else if (N <= 4096) th = 256, ept = 16;
+  else if (N <= 16384 || op == kXent) th = 512, ept = 32;
+  else {
+    th = 512, ept = 64;
+    clustered = true;
+    const int64_t c = (N + 32767) / 32768;
+    if (c > kMaxCluster) return QK_ERR_UNSUPPORTED;
+    cl = next_pow2(c);
+  }
+  const KernelEntry* ke = find_kernel(op, dt, 2, th, th, ept, clustered);
+  if (ke == nullptr) return QK_ERR_UNSUPPORTED;
+  if (M * cl > int64_t(INT32_MAX)) return QK_ERR_UNSUPPORTED;
+  qk_status st = prepare_kernel(dev, d, *ke);
+  if (st != QK_OK) return st;
+  p->kernel = ke;
+  p->cluster = cl;
+  p->slots = 0;
+  p->chunks = op == kXent ? int((N + int64_t(th) * ept - 1) / (int64_t(th) * ept)) : 1;
+  p->num_items = M;
+  p->slot_bytes = 0;
+  p->smem = 0;
+  p->ctas_per_sm = 0;
+  p->grid = M * cl;
+  return QK_OK;
+}
+
+int64_t max_row_elements(int op, int dt) {
+  if (op == kXent) return INT64_MAX;
+  return kMaxRowBytes / elem_size(dt);
+}
+
+qk_status launch(const Plan& p, const RowArgs& a, void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(unsigned(p.grid), 1, 1);
+  cfg.blockDim = dim3(unsigned(p.kernel->threads), 1, 1);
+  cfg.dynamicSmemBytes = size_t(p.smem);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  if (p.kernel->clustered) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  RowArgs args = a;
+  void* params[] = {&args};
+  if (cudaLaunchKernelExC(&cfg, p.kernel->func, params) != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_LAUNCH;
+  }
+  return QK_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+bool aligned_to(const void* ptr, size_t n) { return (reinterpret_cast<uintptr_t>(ptr) % n) == 0; }
+
+// [a, a+na) and [b, b+nb) share a byte.
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+  if (a == nullptr || b == nullptr || na <= 0 || nb <= 0) return false;
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + uintptr_t(nb) && pb < pa + uintptr_t(na);
+}
+
+qk_status check_sizes(int op, int dt, int64_t M, int64_t N) {
+  if (dt != QK_F32 && dt != QK_BF16) return QK_ERR_INVALID_ARG;
+  if (M < 0 || N <= 0) return QK_ERR_INVALID_ARG;
+  if (M > 0 && N > INT64_MAX / 16 / M) return QK_ERR_INVALID_ARG;  // byte offsets fit int64
+  if (N > max_row_elements(op, dt)) return QK_ERR_UNSUPPORTED;
+  return QK_OK;
+}
+
+// Shared tail of the three entry points: plan, fill args, launch.
+qk_status run(int op, int dt, RowArgs a, bool fast, void* stream) {
+  int dev;
+  DeviceInfo* d;
+  qk_status st = device_info(&dev, &d);
+  if (st != QK_OK) return st;
+  Plan p;
+  st = fast ? plan_ring(dev, *d, op, dt, a.M, a.N, &p) : plan_direct(dev, *d, op, dt, a.M, a.N, &p);
+  if (st != QK_OK) return st;
+  a.chunks = p.chunks;
+  a.slots = p.slots;
+  a.slot_bytes = p.slot_bytes;
+  a.num_items = p.num_items;
+  a.timeout_ns = kWaitTimeoutNs;
+  a.status = d->status;
+  return launch(p, a, stream);
+}
+
+}  // namespace
+}  // namespace qk
+
+using namespace qk;
+
+extern "C" {
+
+const char* qk_status_string(qk_status s) {
+  switch (s) {
+    case QK_OK: return "ok";
+    case QK_ERR_INVALID_ARG: return "invalid argument";
+    case QK_ERR_UNSUPPORTED: return "unsupported size or plan";
+    case QK_ERR_MISALIGNED: return "pointer not aligned to its element size";
+    case QK_ERR_LAUNCH: return "CUDA launch or query failed";
+    case QK_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case QK_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
+  }
+  return "unknown status";
+}
+
+int64_t qk_max_row_elements(qk_op op, qk_dtype dtype) {
+  if (op < 0 || op > 2 || (dtype != QK_F32 && dtype != QK_BF16)) return 0;
+  return max_row_elements(op, dtype);
+}
+
+qk_status qk_softmax_fwd(const void* x, void* y, int64_t M, int64_t N, qk_dtype dtype,
+                         void* stream) {
+  qk_status st = check_sizes(kSoftmax, dtype, M, N);
+  if (st != QK_OK) return st;
+  if (M == 0) return QK_OK;
+  if (x == nullptr || y == nullptr) return QK_ERR_INVALID_ARG;
+  const size_t es = size_t(elem_size(dtype));
+  if (!aligned_to(x, es) || !aligned_to(y, es)) return QK_ERR_MISALIGNED;
+  const int64_t bytes = M * N * int64_t(es);
+  if (x != y && overlap(x, bytes, y, bytes)) return QK_ERR_INVALID_ARG;
+  RowArgs a = {};
+  a.x = x;
+  a.y = y;
+  a.M = M;
+  a.N = N;
+  const bool fast = aligned16(x) && aligned16(y) && (N * int64_t(es)) % 16 == 0;
+  return run(kSoftmax, dtype, a, fast, stream);
+}
+
+qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M,
+                         int64_t N, float eps, qk_dtype dtype, void* stream) {
+  qk_status st = check_sizes(kRmsNorm, dtype, M, N);
+  if (st != QK_OK) return st;
+  if (!(std::isfinite(eps) && eps >= 0.f)) return QK_ERR_INVALID_ARG;
+  if (M == 0) return QK_OK;
+  if (x == nullptr || w == nullptr || y == nullptr) return QK_ERR_INVALID_ARG;
+  const size_t es = size_t(elem_size(dtype));
+  if (!aligned_to(x, es) || !aligned_to(y, es) || !aligned_to(w, es) || !aligned_to(rstd, 4))
+    return QK_ERR_MISALIGNED;
+  const int64_t bytes = M * N * int64_t(es), wbytes = N * int64_t(es), rbytes = M * 4;
+  if ((x != y && overlap(x, bytes, y, bytes)) || overlap(y, bytes, w, wbytes) ||
+      overlap(rstd, rbytes, x, bytes) || overlap(rstd, rbytes, y, bytes) ||
+      overlap(rstd, rbytes, w, wbytes))
+    return QK_ERR_INVALID_ARG;
+  RowArgs a = {};
+  a.x = x;
+  a.w = w;
+  a.y = y;
+  a.rstd = rstd;
+  a.M = M;
+  a.N = N;
+  a.eps = eps;
+  const bool fast =
+      aligned16(x) && aligned16(y) && aligned16(w) && (N * int64_t(es)) % 16 == 0;
+  return run(kRmsNorm, dtype, a, fast, stream);
+}
+
+qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* loss, float* lse,
+                      int64_t M, int64_t N, qk_dtype dtype, void* stream) {
+  qk_status st = check_sizes(kXent, dtype, M, N);
+  if (st != QK_OK) return st;
+  if (M == 0) return QK_OK;
+  if (logits == nullptr || targets == nullptr || loss == nullptr) return QK_ERR_INVALID_ARG;
+  const size_t es = size_t(elem_size(dtype));
+  if (!aligned_to(logits, es) || !aligned_to(targets, 8) || !aligned_to(loss, 4) ||
+      !aligned_to(lse, 4))
+    return QK_ERR_MISALIGNED;
+  const int64_t bytes = M * N * int64_t(es), tbytes = M * 8, obytes = M * 4;
+  if (overlap(loss, obytes, logits, bytes) || overlap(loss, obytes, targets, tbytes) ||
+      overlap(loss, obytes, lse, obytes) || overlap(lse, obytes, logits, bytes) ||
+      overlap(lse, obytes, targets, tbytes))
+    return QK_ERR_INVALID_ARG;
+  RowArgs a = {};
+  a.x = logits;
+  a.target = targets;
+  a.loss = loss;
+  a.lse = lse;
+  a.M = M;
+  a.N = N;
+  const bool fast = aligned16(logits) && (N * int64_t(es)) % 16 == 0;
+  return run(kXent, dtype, a, fast, stream);
+}
+
+qk_status qk_get_device_status(void* stream) {
+  int dev;
+  DeviceInfo* d;
+  qk_status st = device_info(&dev, &d);
+  if (st != QK_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_LAUNCH;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_LAUNCH;
+  }
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return QK_ERR_LAUNCH;
+    }
+  }
+  return static_cast<qk_status>(v);
+}
+
+qk_status qk_get_plan(qk_op op, qk_dtype dtype, int64_t M, int64_t N, qk_plan* plan) {
+  if (plan == nullptr || op < 0 || op > 2) return QK_ERR_INVALID_ARG;
+  qk_status st = check_sizes(op, dtype, M, N);
+  if (st != QK_OK) return st;
+  int dev;
+  DeviceInfo* d;
+  st = device_info(&dev, &d);
+  if (st != QK_OK) return st;
+  const bool fast = (N * int64_t(elem_size(dtype))) % 16 == 0;
+  Plan p;
+  st = fast ? plan_ring(dev, *d, op, dtype, std::max<int64_t>(M, 1), N, &p)
+            : plan_direct(dev, *d, op, dtype, std::max<int64_t>(M, 1), N, &p);
+  if (st != QK_OK) return st;
+  plan->path = p.kernel->path;
+  plan->threads = p.kernel->threads;
+  plan->row_threads = p.kernel->row_threads;
+  plan->vec_per_thread = p.kernel->vec_per_thread;
+  plan->cluster = p.cluster;
+  plan->slots = p.slots;
+  plan->chunks = p.chunks;
+  plan->ctas_per_sm = p.ctas_per_sm;
+  plan->grid = int32_t(std::min<int64_t>(p.grid, INT32_MAX));
+  plan->smem_bytes = p.smem;
+  return QK_OK;
+}
+
+qk_status qk_set_plan_override(qk_op op, qk_dtype dtype, const qk_plan* plan) {
+  if (op < 0 || op > 2 || (dtype != QK_F32 && dtype != QK_BF16)) return QK_ERR_INVALID_ARG;
+  if (plan == nullptr) {
+    g_override[op][dtype].on = false;
+    return QK_OK;
+  }
+  if (plan->cluster < 0 || plan->cluster > kMaxCluster || plan->slots < 0 ||
+      plan->slots > kMaxSlots)
+    return QK_ERR_INVALID_ARG;
+  const bool clustered = plan->cluster > 1;
+  if (find_kernel(op, dtype, 1, plan->threads, plan->row_threads, plan->vec_per_thread,
+                  clustered) == nullptr)
+    return QK_ERR_UNSUPPORTED;
+  g_override[op][dtype].plan = *plan;
+  g_override[op][dtype].on = true;
+  return QK_OK;
+}
+
+qk_status qk_test_wait_timeout(uint64_t timeout_ns, void* stream) {
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return QK_ERR_INVALID_ARG;
+  int dev;
+  DeviceInfo* d;
+  qk_status st = device_info(&dev, &d);
+  if (st != QK_OK) return st;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns, d->status);
+  if (cudaGetLastError() != cudaSuccess) return QK_ERR_LAUNCH;
+  return QK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,274 @@
+// qk_device.cuh -- device primitives for the sm_103a row-reduction kernels.
+//
+// Hand-written inline PTX (public PTX ISA) for:
+//   * mbarriers with expect-tx byte counting and bounded parity waits,
+//   * bulk (non-tensor) TMA copies global -> shared, completing on an mbarrier,
+//   * thread-block-cluster addressing (mapa) and st.async into a peer CTA's
+//     shared memory that completes on the peer's mbarrier,
+//   * 16-byte vector packing for fp32 / bf16 rows,
+//   * the reduction operators: sum, and the (max, sum-of-exponentials) pair
+//     of an online softmax.
+//
+// The reduction hierarchy (thread -> warp shuffle -> block shared memory ->
+// cluster DSMEM) follows the QbitAI article on QuACK, section
+// "硬件感知的归约策略" (hardware-aware reduction), parts 1-4.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace qk {
+
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x * log2 e)
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// ---------------------------------------------------------------------------
+// Shared-memory addressing and special registers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// Makes initialised barriers visible to the async proxy and to peer CTAs.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Acquire at cluster scope: for data that peer CTAs wrote with st.async.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the phase with the given parity to complete, giving up after
+// timeout_ns nanoseconds of the global timer.  Returns false on time-out; the
+// caller records the failure and leaves its loop, so no wait is unbounded.
+template <bool kClusterScope>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  auto poll = [&]() {
+    return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (poll()) return true;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// First error wins; later ones are dropped.
+__device__ __forceinline__ void report_status(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Bulk TMA copy global -> shared (non-tensor form: contiguous bytes)
+// ---------------------------------------------------------------------------
+// L2 policy for data read exactly once: evict it first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// dst, bar: shared addresses of this CTA; src: global, 16-byte aligned;
+// bytes: a multiple of 16.  Completion adds `bytes` to bar's tx count.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block cluster / DSMEM
+// ---------------------------------------------------------------------------
+// Address of the same shared-memory object in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// 8-byte store into a (possibly remote) CTA's shared memory; completes by
+// adding 8 bytes to the tx count of the mbarrier `rbar` in that same CTA.
+__device__ __forceinline__ void st_async_f2(uint32_t raddr, float a, float b, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+          raddr),
+      "f"(a), "f"(b), "r"(rbar)
+      : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Arithmetic
+// ---------------------------------------------------------------------------
+// 2^x with the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Online-softmax pair: m = running maximum, s = sum of exp(x - m).  Merging
+// two pairs rescales both sums to the larger maximum.  A pair with m = -inf
+// (no elements yet) contributes nothing and never produces inf - inf.
+__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == kNegInf) {
+    s = 0.f;
+    m = mn;
+    return;
+  }
+  // Explicit roundings (no fused multiply-add): merge(a, b) == merge(b, a)
+  // bit for bit, so both lanes of a butterfly step agree exactly.
+  s = __fadd_rn(__fmul_rn(s, exp2_approx((m - mn) * kLog2e)),
+                __fmul_rn(s2, exp2_approx((m2 - mn) * kLog2e)));
+  m = mn;
+}
+
+// Butterfly (xor) reductions: after the loop every lane holds the result.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ void warp_ms(float& m, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    ms_merge(m, s, m2, s2);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of fp32 (4 elements) or bf16 (8 elements)
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Vec16;
+
+template <>
+struct Vec16<float> {
+  static constexpr int kElems = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static void unpack_fresh(const uint4& v, float* f) { unpack(v, f); }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+  __device__ __forceinline__ static float load1(const void* p) {
+    return *static_cast<const float*>(p);
+  }
+  __device__ __forceinline__ static void store1(void* p, float v) { *static_cast<float*>(p) = v; }
+};
+
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  // bf16 -> fp32 is exact: the 16 bits become the high half of the float.
+  __device__ __forceinline__ static void unpack2(uint32_t u, float& lo, float& hi) {
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+  }
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    unpack2(v.x, f[0], f[1]);
+    unpack2(v.y, f[2], f[3]);
+    unpack2(v.z, f[4], f[5]);
+    unpack2(v.w, f[6], f[7]);
+  }
+  // Same as unpack, but opaque to the optimiser: it cannot be hoisted out of
+  // a loop or merged with an earlier unpack, so the packed form (half the
+  // registers) is what stays live between the reduction and the finish.
+  __device__ __forceinline__ static void unpack_fresh(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t lo, hi;
+      asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w[i]));
+      asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(w[i]));
+      f[2 * i] = __uint_as_float(lo);
+      f[2 * i + 1] = __uint_as_float(hi);
+    }
+  }
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+  }
+  __device__ __forceinline__ static float load1(const void* p) {
+    const uint16_t b = *static_cast<const uint16_t*>(p);
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+  __device__ __forceinline__ static void store1(void* p, float v) {
+    *static_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+  }
+};
+
+}  // namespace qk

@@ -1,0 +1,8 @@
+// Kernel instances for rmsnorm forward, f32 rows.
+#define QK_OP 1
+#define QK_T float
+#include "qk_kernel_table.cuh"
+
+namespace qk {
+KernelTable kernels_rmsnorm_f32() { return {kTable, int(sizeof(kTable) / sizeof(kTable[0]))}; }
+}  // namespace qk

@@ -1,0 +1,8 @@
+// Kernel instances for softmax forward, bf16 rows.
+#define QK_OP 0
+#define QK_T __nv_bfloat16
+#include "qk_kernel_table.cuh"
+
+namespace qk {
+KernelTable kernels_softmax_bf16() { return {kTable, int(sizeof(kTable) / sizeof(kTable[0]))}; }
+}  // namespace qk

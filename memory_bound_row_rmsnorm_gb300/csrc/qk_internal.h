@@ -1,0 +1,61 @@
+// qk_internal.h -- types shared by the kernel translation units and the C ABI.
+#pragma once
+
+#include <stdint.h>
+
+namespace qk {
+
+enum Op : int { kSoftmax = 0, kRmsNorm = 1, kXent = 2 };
+enum Dtype : int { kF32 = 0, kBF16 = 1 };
+
+// Everything a row kernel needs, passed by value as its only parameter.
+struct RowArgs {
+  const void* x;          // [M, N] input rows (logits for cross-entropy)
+  void* y;                // [M, N] output rows (softmax, RMSNorm)
+  const void* w;          // [N] RMSNorm weight
+  float* rstd;            // [M] RMSNorm 1/rms, may be null
+  const int64_t* target;  // [M] cross-entropy targets
+  float* loss;            // [M] cross-entropy loss
+  float* lse;             // [M] cross-entropy log-sum-exp, may be null
+  int64_t M;
+  int64_t N;
+  float eps;
+  int32_t chunks;       // ring slots one row slice spans (streamed rows), else 1
+  int32_t slots;        // ring slots per CTA
+  uint32_t slot_bytes;  // bytes per ring slot (multiple of 128)
+  int64_t num_items;    // work items: row blocks of threads/row_threads rows, or rows
+  uint64_t timeout_ns;  // bound on every wait inside the kernel
+  int* status;          // device status word (first failure code)
+};
+
+// Size of the fixed shared-memory header in front of the TMA ring: mbarriers,
+// the block-reduction buffer and the cluster exchange buffer.
+constexpr int kSmemHeader = 1024;
+constexpr int kMaxSlots = 32;
+constexpr int kMaxCluster = 16;
+
+// One compiled kernel.  `path` 1: TMA ring kernel (threads, row_threads,
+// vec_per_thread); path 2: masked direct kernel (threads, elems_per_thread).
+struct KernelEntry {
+  int path;
+  int threads;
+  int row_threads;
+  int vec_per_thread;
+  bool clustered;
+  const void* func;
+};
+
+struct KernelTable {
+  const KernelEntry* entries;
+  int count;
+};
+
+// Defined by the instantiation translation units, one per (op, dtype).
+KernelTable kernels_softmax_f32();
+KernelTable kernels_softmax_bf16();
+KernelTable kernels_rmsnorm_f32();
+KernelTable kernels_rmsnorm_bf16();
+KernelTable kernels_xent_f32();
+KernelTable kernels_xent_bf16();
+
+}  // namespace qk

@@ -1,0 +1,44 @@
+// qk_kernel_table.cuh -- the compiled kernel configurations of one (op, dtype).
+//
+// Include with QK_OP (an Op) and QK_T (float or __nv_bfloat16) defined.
+// Ring kernels: (threads, row_threads, vec_per_thread, clustered); a row of up
+// to row_threads * vec_per_thread 16-byte vectors fits one CTA, and a cluster
+// of up to 16 CTAs multiplies that.  Direct kernels: (threads, elems/thread).
+#pragma once
+
+#include "qk_kernels.cuh"
+
+#define QK_RING(TH, TPR, VPT, CL) \
+  {1, TH, TPR, VPT, CL, reinterpret_cast<const void*>(&row_kernel<QK_OP, QK_T, TH, TPR, VPT, CL>)}
+#define QK_DIRECT(TH, EPT, CL) \
+  {2, TH, TH, EPT, CL, reinterpret_cast<const void*>(&direct_kernel<QK_OP, QK_T, TH, EPT, CL>)}
+
+namespace qk {
+namespace {
+const KernelEntry kTable[] = {
+    QK_RING(256, 32, 1, false),
+    QK_RING(256, 32, 2, false),
+    QK_RING(256, 32, 4, false),
+    QK_RING(256, 64, 4, false),
+    QK_RING(256, 128, 2, false),
+    QK_RING(256, 128, 4, false),
+    QK_RING(128, 128, 4, false),
+    QK_RING(256, 256, 2, false),
+    QK_RING(256, 256, 4, false),
+    QK_RING(256, 256, 8, false),
+    QK_RING(512, 512, 4, false),
+    QK_RING(512, 512, 8, false),
+#if QK_OP != 2  // cross-entropy streams long rows instead of splitting them
+    QK_RING(256, 256, 8, true),
+    QK_RING(512, 512, 4, true),
+    QK_RING(512, 512, 8, true),
+#endif
+    QK_DIRECT(128, 4, false),
+    QK_DIRECT(256, 16, false),
+    QK_DIRECT(512, 32, false),
+#if QK_OP != 2
+    QK_DIRECT(512, 64, true),
+#endif
+};
+}  // namespace
+}  // namespace qk

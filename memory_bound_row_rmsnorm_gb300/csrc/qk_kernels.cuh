@@ -1,0 +1,508 @@
+// qk_kernels.cuh -- the row-reduction kernels for sm_103a (GB300).
+//
+// row_kernel: the fast path (16-byte aligned rows).
+//   * Persistent grid: each CTA (or each cluster of CTAs) walks a strided list
+//     of work items.  An item is a block of `threads / row_threads` consecutive
+//     rows (contiguous in memory), one row slice of a cluster, or one chunk of
+//     a streamed row.
+//   * One thread issues bulk TMA copies (cp.async.bulk) of whole items into a
+//     ring of shared-memory slots; each slot has an mbarrier that completes
+//     when its bytes land.  The ring keeps `slots - 1` items in flight while
+//     one is being reduced, so HBM reads are overlapped with the reduction and
+//     the stores of earlier rows.  Every input byte crosses HBM once.
+//   * Consumers read 16-byte vectors from shared memory (consecutive threads
+//     take consecutive vectors: no bank conflicts) into registers, reduce per
+//     thread, then warp butterfly, then across the warps of a row through a
+//     shared buffer, then -- for rows split over a cluster -- across CTAs by
+//     st.async into every peer's shared memory, counted by an mbarrier.
+//   * The finish works from registers and stores each output vector once with
+//     a 16-byte store.
+//   Cited: QbitAI article on QuACK, section "硬件感知的加载与存储策略" (TV layout,
+//   128-bit coalesced accesses, asynchronous GMEM->SMEM staging, store straight
+//   back to GMEM after the reduction) and section "硬件感知的归约策略" (thread,
+//   warp, block and cluster reduction; the arrival-counting barrier that keeps
+//   a CTA from reading its buffer before every peer has written it).
+//
+// direct_kernel: the masked path for rows whose start or length is not a
+//   multiple of 16 bytes.  Plain element loads into registers, the same
+//   reduction hierarchy, element stores.  Slower but exact on any N.
+#pragma once
+
+#include "qk_device.cuh"
+#include "qk_internal.h"
+
+namespace qk {
+
+constexpr int64_t kCopyBytes = 32768;  // largest single bulk copy issued
+constexpr int kStatusTimeout = 5;      // QK_ERR_TIMEOUT
+
+template <int OP>
+__device__ __forceinline__ void combine(float& m, float& s, float m2, float s2) {
+  if constexpr (OP == kRmsNorm) {
+    s += s2;
+  } else {
+    ms_merge(m, s, m2, s2);
+  }
+}
+
+// Reduces the pair (m, s) (or the sum s for RMSNorm) over the warp.
+template <int OP>
+__device__ __forceinline__ void warp_reduce(float& m, float& s) {
+  if constexpr (OP == kRmsNorm) {
+    s = warp_sum(s);
+  } else {
+    warp_ms(m, s);
+  }
+}
+
+template <int OP, typename T, int THREADS, int TPR, int VPT, bool CLUSTER>
+__global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
+  using V = Vec16<T>;
+  constexpr int E = V::kElems;       // elements per 16-byte vector
+  constexpr int NW = THREADS / 32;   // warps per CTA
+  constexpr int WPG = TPR / 32;      // warps per row group
+  constexpr int R = THREADS / TPR;   // rows per item (unclustered, unchunked)
+  constexpr int64_t CH = int64_t(TPR) * VPT;  // vectors per row-slice chunk
+  static_assert(TPR % 32 == 0 && THREADS % TPR == 0, "row groups are whole warps");
+  static_assert(!CLUSTER || TPR == THREADS, "a clustered row spans the whole CTA");
+  static_assert(NW <= 16, "block-reduction buffer holds 16 warps");
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);                  // [kMaxSlots]
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + 8 * kMaxSlots);  // [2]
+  float2* red = reinterpret_cast<float2*>(smem + 512);                 // [2][16]
+  float2* xbuf = reinterpret_cast<float2*>(smem + 768);                // [2][kMaxCluster]
+  unsigned char* ring = smem + kSmemHeader;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = tid / TPR;  // row group inside an item
+  const int l = tid % TPR;  // thread inside its row group
+  const int64_t M = a.M, N = a.N;
+  const int64_t NV = N / E;  // vectors per row
+  const int S = a.slots;
+  const int64_t K = a.chunks;
+
+  uint32_t C = 1, rank = 0, cid = blockIdx.x, ncl = gridDim.x;
+  if constexpr (CLUSTER) {
+    C = cluster_nctarank();
+    rank = cluster_ctarank();
+    cid = cluster_id_x();
+    ncl = num_clusters_x();
+  }
+  // Column slice of this CTA, in vectors (the whole row unless clustered).
+  const int64_t SV = (NV + C - 1) / C;
+  const int64_t v0 = min(NV, int64_t(rank) * SV);
+  const int64_t nv = min(NV, v0 + SV) - v0;
+
+  // Local steps: item i of this cluster is cid + i * ncl; each item has K chunks.
+  const int64_t n_local = a.num_items > int64_t(cid) ? (a.num_items - 1 - cid) / ncl + 1 : 0;
+  const int64_t q_total = n_local * K;
+
+  const uint32_t full0 = smem_addr(full), xbar0 = smem_addr(xbar), ring0 = smem_addr(ring);
+  const unsigned char* xg = static_cast<const unsigned char*>(a.x);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(full0 + 8 * s, 1);
+    mbar_init(xbar0, 1);
+    mbar_init(xbar0 + 8, 1);
+    fence_mbar_init();
+  }
+  if constexpr (CLUSTER) {
+    cluster_sync_all();  // peers' barriers exist before anyone stores into them
+  } else {
+    __syncthreads();
+  }
+
+  uint64_t policy = 0;
+  // Producer (thread 0): load local step q into ring slot q % S.
+  auto issue = [&](int64_t q) {
+    const int64_t i = q / K, j = q - (q / K) * K;
+    const int64_t item = int64_t(cid) + i * ncl;
+    int64_t off, bytes;
+    if (K > 1) {  // one chunk of a streamed row
+      const int64_t c0 = j * CH;
+      off = (item * NV + c0) * 16;
+      bytes = min(CH, NV - c0) * 16;
+    } else if (CLUSTER) {  // this CTA's slice of one row
+      off = (item * NV + v0) * 16;
+      bytes = nv * 16;
+    } else {  // R consecutive rows
+      const int64_t r0 = item * R;
+      off = r0 * NV * 16;
+      bytes = min(int64_t(R), M - r0) * NV * 16;
+    }
+    const int slot = int(q % S);
+    const uint32_t dst = ring0 + uint32_t(slot) * a.slot_bytes;
+    const uint32_t bar = full0 + 8u * uint32_t(slot);
+    mbar_arrive_expect_tx(bar, uint32_t(bytes));
+    for (int64_t o = 0; o < bytes; o += kCopyBytes)
+      bulk_copy_g2s(dst + uint32_t(o), xg + off + o, uint32_t(min(kCopyBytes, bytes - o)), bar,
+                    policy);
+  };
+  if (tid == 0) {
+    policy = l2_evict_first_policy();
+    const int64_t pre = min(int64_t(S), q_total);
+    for (int64_t q = 0; q < pre; ++q) issue(q);
+  }
+
+  // RMSNorm weight: the columns a thread touches never change, so its share
+  // of w is loaded once into registers.
+  uint4 wv[VPT];
+  if constexpr (OP == kRmsNorm) {
+    const uint4* wg = static_cast<const uint4*>(a.w) + v0;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t lv = l + int64_t(k) * TPR;
+      wv[k] = lv < nv ? __ldg(wg + lv) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  uint4 xr[VPT];        // raw input vectors of the current row (chunk)
+  float ef[VPT * E];    // softmax: exp(x - thread max), kept until the finish
+  float run_m = kNegInf, run_s = 0.f;  // cross-entropy: running pair over chunks
+  float xt = 0.f;                      // cross-entropy: x[target] if this thread holds it
+  bool own_t = false;
+  int64_t trow = -1;
+  bool failed = false;  // a wait of this thread ran out
+  bool abort = false;   // block-uniform: some thread's wait ran out
+  int64_t q = 0;
+
+  for (; q < q_total; ++q) {
+    const int64_t i = q / K, j = q - (q / K) * K;
+    const int64_t item = int64_t(cid) + i * ncl;
+    const int slot = int(q % S);
+    if (!mbar_wait<false>(full0 + 8u * uint32_t(slot), uint32_t((q / S) & 1), a.timeout_ns)) {
+      report_status(a.status, kStatusTimeout);
+      failed = true;
+    }
+
+    const bool single = (K > 1) || CLUSTER;  // one row per item
+    const int64_t row = single ? item : item * R + g;
+    const bool row_ok = row < M;
+    const int64_t cn = (K > 1) ? min(CH, NV - j * CH) : nv;  // vectors of this row in the slot
+    const int64_t cbase = (K > 1) ? j * CH : v0;              // first column vector in the slot
+    const unsigned char* sb =
+        ring + size_t(slot) * a.slot_bytes + (single ? size_t(0) : size_t(g) * size_t(NV) * 16);
+
+    bool valid[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t lv = l + int64_t(k) * TPR;
+      valid[k] = row_ok && lv < cn && !failed;
+      xr[k] = valid[k] ? *reinterpret_cast<const uint4*>(sb + lv * 16) : make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    // ---- thread-level reduction (registers) ----
+    float pm = kNegInf, ps = 0.f;  // partial (max, sum-exp), or (-, sum of squares)
+    float tm = kNegInf;            // softmax: this thread's own maximum
+    if constexpr (OP == kRmsNorm) {
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        float f[E];
+        V::unpack(xr[k], f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc = fmaf(f[e], f[e], acc);  // masked vectors are zero
+      }
+      ps = acc;
+    } else if constexpr (OP == kSoftmax) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        V::unpack(xr[k], &ef[k * E]);
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (valid[k]) tm = fmaxf(tm, ef[k * E + e]);
+      }
+      const float mb = (tm == kNegInf) ? 0.f : tm * kLog2e;
+      float s = 0.f;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float v = valid[k] ? exp2_approx(fmaf(ef[k * E + e], kLog2e, -mb)) : 0.f;
+          ef[k * E + e] = v;
+          s += v;
+        }
+      pm = tm;
+      ps = s;
+    } else {  // cross-entropy: online pair over the chunks of the row
+      if (j == 0) {
+        run_m = kNegInf;
+        run_s = 0.f;
+        own_t = false;
+        trow = row_ok ? a.target[row] : -1;
+      }
+      float f[VPT * E];
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) V::unpack(xr[k], &f[k * E]);
+      if (trow >= 0 && trow < N) {
+        const int64_t tl = trow / E - cbase;  // target vector, relative to the slot
+        if (tl >= 0 && tl < cn && tl % TPR == l) {
+          const int kk = int(tl / TPR), ee = int(trow % E);
+#pragma unroll
+          for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+              if (k == kk && e == ee) xt = f[k * E + e];
+          own_t = true;
+        }
+      }
+      float m = run_m;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (valid[k]) m = fmaxf(m, f[k * E + e]);
+      if (m != kNegInf) {
+        run_s *= exp2_approx((run_m - m) * kLog2e);  // rescale to the new maximum
+        const float mb = m * kLog2e;
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if (valid[k]) s += exp2_approx(fmaf(f[k * E + e], kLog2e, -mb));
+        run_s += s;
+        run_m = m;
+      }
+      pm = run_m;
+      ps = run_s;
+    }
+
+    // ---- warp butterfly; warp partials to the block buffer ----
+    const bool row_end = (j == K - 1);
+    if (row_end) {
+      warp_reduce<OP>(pm, ps);
+      if (WPG > 1 && lane == 0) red[(i & 1) * 16 + warp] = make_float2(pm, ps);
+    }
+    // One barrier per step: the slot is free again (every thread has its data
+    // in registers) and the warp partials are visible.  It also carries a
+    // failed wait to the whole CTA so that everyone leaves together.
+    if (__syncthreads_or(failed)) {
+      abort = true;
+      break;
+    }
+    if (tid == 0 && q + S < q_total) issue(q + S);
+    if (!row_end) continue;
+
+    // ---- block reduction over the warps of this row group ----
+    if constexpr (WPG > 1) {
+      const float2* rg = red + (i & 1) * 16 + g * WPG;
+      float2 p = rg[0];
+      pm = p.x;
+      ps = p.y;
+#pragma unroll
+      for (int w = 1; w < WPG; ++w) {
+        p = rg[w];
+        combine<OP>(pm, ps, p.x, p.y);
+      }
+    }
+
+    // ---- cluster reduction: every CTA's partial into every peer (DSMEM) ----
+    if constexpr (CLUSTER) {
+      const uint32_t b = uint32_t(i & 1);
+      const uint32_t xb = xbar0 + 8u * b;
+      if (tid == 0) {
+        mbar_arrive_expect_tx(xb, C * 8u);
+        const uint32_t mine = smem_addr(xbuf + b * kMaxCluster + rank);
+        for (uint32_t r = 0; r < C; ++r) st_async_f2(map_to_rank(mine, r), pm, ps, map_to_rank(xb, r));
+      }
+      if (!mbar_wait<true>(xb, uint32_t((i >> 1) & 1), a.timeout_ns)) {
+        report_status(a.status, kStatusTimeout);
+        failed = true;
+      }
+      const float2* xs = xbuf + b * kMaxCluster;
+      float2 p = xs[0];
+      pm = p.x;
+      ps = p.y;
+      for (uint32_t r = 1; r < C; ++r) {
+        p = xs[r];
+        combine<OP>(pm, ps, p.x, p.y);
+      }
+    }
+
+    // ---- finish: outputs from registers, each stored once ----
+    if (!row_ok) continue;
+    if constexpr (OP == kSoftmax) {
+      const float scale = (tm == kNegInf) ? 0.f : exp2_approx((tm - pm) * kLog2e) / ps;
+      uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;
+        float o[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = ef[k * E + e] * scale;
+        yg[l + k * TPR] = V::pack(o);
+      }
+    } else if constexpr (OP == kRmsNorm) {
+      const float r = 1.0f / sqrtf(ps / float(N) + a.eps);
+      uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;
+        float f[E], w[E], o[E];
+        V::unpack_fresh(xr[k], f);
+        V::unpack_fresh(wv[k], w);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = __fmul_rn(__fmul_rn(f[e], r), w[e]);
+        yg[l + k * TPR] = V::pack(o);
+      }
+      if (l == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = r;
+    } else {
+      const float lse = pm + logf(ps);
+      if (l == 0 && rank == 0) {
+        if (a.lse != nullptr) a.lse[row] = lse;
+        if (!(trow >= 0 && trow < N)) a.loss[row] = __int_as_float(0x7fc00000);  // NaN
+      }
+      if (own_t) a.loss[row] = lse - xt;
+    }
+  }
+
+  if (abort) {
+    // Leave no bulk copy in flight into this CTA's shared memory.
+    if (tid == 0) {
+      const int64_t end = min(q_total, q + S);
+      for (int64_t qq = q; qq < end; ++qq)
+        mbar_wait<false>(full0 + 8u * uint32_t(qq % S), uint32_t((qq / S) & 1), a.timeout_ns);
+    }
+    __syncthreads();
+  }
+  if constexpr (CLUSTER) cluster_sync_all();  // no CTA leaves while peers may write to it
+}
+
+// ---------------------------------------------------------------------------
+// Masked direct path: any N, any element-aligned pointers.  One row per CTA
+// (or per cluster); cross-entropy streams its row through registers.
+// ---------------------------------------------------------------------------
+template <int OP, typename T, int THREADS, int EPT, bool CLUSTER>
+__global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
+  using V = Vec16<T>;
+  constexpr int NW = THREADS / 32;
+  constexpr int64_t CH = int64_t(THREADS) * EPT;
+  __shared__ float2 red[NW];
+  __shared__ float2 xbuf[kMaxCluster];
+  __shared__ __align__(8) uint64_t xbar;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t C = 1, rank = 0;
+  int64_t row = blockIdx.x;
+  if constexpr (CLUSTER) {
+    C = cluster_nctarank();
+    rank = cluster_ctarank();
+    row = cluster_id_x();
+  }
+  const int64_t N = a.N;
+  const int64_t SE = (N + C - 1) / C;
+  const int64_t e0 = min(N, int64_t(rank) * SE);
+  const int64_t ne = min(N, e0 + SE) - e0;
+  const uint32_t xb = smem_addr(&xbar);
+  if constexpr (CLUSTER) {
+    if (tid == 0) {
+      mbar_init(xb, 1);
+      fence_mbar_init();
+    }
+    cluster_sync_all();
+  }
+
+  const T* xrow = static_cast<const T*>(a.x) + row * N + e0;
+  float f[EPT];
+  float pm = kNegInf, ps = 0.f, tm = kNegInf, xt = 0.f;
+  bool own_t = false;
+  const int64_t trow = (OP == kXent) ? a.target[row] : -1;
+
+  for (int64_t c0 = 0; c0 < ne; c0 += CH) {  // more than one pass only for cross-entropy
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int64_t e = c0 + tid + int64_t(k) * THREADS;
+      f[k] = e < ne ? V::load1(xrow + e) : (OP == kRmsNorm ? 0.f : kNegInf);
+    }
+    if constexpr (OP == kRmsNorm) {
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) ps = fmaf(f[k], f[k], ps);
+    } else {
+      float m = pm;
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) m = fmaxf(m, f[k]);
+      if (m != kNegInf) {
+        ps *= exp2_approx((pm - m) * kLog2e);
+        const float mb = m * kLog2e;
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+          const float v = exp2_approx(fmaf(f[k], kLog2e, -mb));  // masked: exp2(-inf) = 0
+          if constexpr (OP == kSoftmax) f[k] = v;
+          ps += v;
+        }
+        pm = m;
+      }
+      tm = pm;
+      if constexpr (OP == kXent) {
+#pragma unroll
+        for (int k = 0; k < EPT; ++k)
+          if (e0 + c0 + tid + int64_t(k) * THREADS == trow) {
+            xt = f[k];
+            own_t = true;
+          }
+      }
+    }
+  }
+
+  warp_reduce<OP>(pm, ps);
+  if (lane == 0) red[warp] = make_float2(pm, ps);
+  __syncthreads();
+  {
+    float2 p = red[0];
+    pm = p.x;
+    ps = p.y;
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+      p = red[w];
+      combine<OP>(pm, ps, p.x, p.y);
+    }
+  }
+  if constexpr (CLUSTER) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(xb, C * 8u);
+      const uint32_t mine = smem_addr(&xbuf[rank]);
+      for (uint32_t r = 0; r < C; ++r) st_async_f2(map_to_rank(mine, r), pm, ps, map_to_rank(xb, r));
+    }
+    if (!mbar_wait<true>(xb, 0u, a.timeout_ns)) report_status(a.status, kStatusTimeout);
+    float2 p = xbuf[0];
+    pm = p.x;
+    ps = p.y;
+    for (uint32_t r = 1; r < C; ++r) {
+      p = xbuf[r];
+      combine<OP>(pm, ps, p.x, p.y);
+    }
+  }
+
+  if constexpr (OP == kSoftmax) {
+    const float scale = (tm == kNegInf) ? 0.f : exp2_approx((tm - pm) * kLog2e) / ps;
+    T* yrow = static_cast<T*>(a.y) + row * N + e0;
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int64_t e = tid + int64_t(k) * THREADS;
+      if (e < ne) V::store1(yrow + e, f[k] * scale);
+    }
+  } else if constexpr (OP == kRmsNorm) {
+    const float r = 1.0f / sqrtf(ps / float(N) + a.eps);
+    T* yrow = static_cast<T*>(a.y) + row * N + e0;
+    const T* wrow = static_cast<const T*>(a.w) + e0;
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int64_t e = tid + int64_t(k) * THREADS;
+      if (e < ne) V::store1(yrow + e, __fmul_rn(__fmul_rn(f[k], r), V::load1(wrow + e)));
+    }
+    if (tid == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = r;
+  } else {
+    const float lse = pm + logf(ps);
+    if (tid == 0 && rank == 0) {
+      if (a.lse != nullptr) a.lse[row] = lse;
+      if (!(trow >= 0 && trow < N)) a.loss[row] = __int_as_float(0x7fc00000);
+    }
+    if (own_t) a.loss[row] = lse - xt;
+  }
+  if constexpr (CLUSTER) cluster_sync_all();
+}
+
+}  // namespace qk

@@ -1,0 +1,81 @@
+"""Comparison rules between the CUDA path and the fp64 oracle.
+
+Tolerances (fixed before any kernel was run):
+  * fp32 outputs y: relative error <= 1e-5; softmax entries also pass with an
+    absolute error <= 1e-7 (tiny probabilities).
+  * bf16 outputs y: within one bf16 ulp of the fp64 value, where
+    ulp(v) = 2^(floor(log2 |v|) - 7); an exact zero must come out as zero.
+    Softmax entries also pass with an absolute error <= 1e-7, the same floor
+    as fp32 (it only matters where exp underflows in fp32).
+  * rstd, lse: fp32, relative error <= 1e-5.
+  * loss: relative error <= 1e-5 against max(|loss|, 1e-3 |lse|), because
+    loss = lse - x[t] can cancel.
+NaN in the expected value must be NaN in the result and vice versa.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+REL_F32 = 1e-5
+ABS_SOFTMAX = 1e-7
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    """Exact widening of an fp32/bf16 tensor to a float64 numpy array."""
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def bf16_ulp(ref: np.ndarray) -> np.ndarray:
+    a = np.abs(ref)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 7), 0.0)
+
+
+def _nan_agree(got, ref, what):
+    gn, rn = np.isnan(got), np.isnan(ref)
+    assert np.array_equal(gn, rn), f"{what}: NaN pattern differs ({int((gn != rn).sum())} entries)"
+    return ~rn
+
+
+def check_rows(got: np.ndarray, ref: np.ndarray, dtype: str, softmax: bool, what: str) -> None:
+    """Element-wise check of an output matrix against the oracle."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, f"{what}: shape {got.shape} vs {ref.shape}"
+    ok_mask = _nan_agree(got, ref, what)
+    g, r = got[ok_mask], ref[ok_mask]
+    err = np.abs(g - r)
+    if dtype == "f32":
+        good = err <= REL_F32 * np.abs(r)
+    else:
+        ulp = bf16_ulp(r)
+        good = np.where(r == 0, g == 0, err <= ulp)
+    if softmax:
+        good |= err <= ABS_SOFTMAX
+    if not good.all():
+        idx = np.flatnonzero(~good)
+        i = idx[np.argmax(err[idx] / np.maximum(np.abs(r[idx]), 1e-300))]
+        raise AssertionError(
+            f"{what}: {idx.size} of {good.size} outside tolerance; worst got {g[i]!r} "
+            f"want {r[i]!r} (|err| {err[i]:.3e})")
+
+
+def check_scalars(got, ref, what: str, denom=None) -> None:
+    """Per-row fp32 scalars (rstd, lse, loss) against the oracle."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    ok_mask = _nan_agree(got, ref, what)
+    d = np.abs(ref) if denom is None else np.asarray(denom, dtype=np.float64)
+    err = np.abs(got - ref)[ok_mask]
+    bound = REL_F32 * d[ok_mask]
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.flatnonzero(bad)[0]
+        raise AssertionError(f"{what}: {int(bad.sum())} rows outside tolerance; first got "
+                             f"{got[ok_mask][i]!r} want {ref[ok_mask][i]!r}")
+
+
+def loss_denominator(loss_ref, lse_ref):
+    return np.maximum(np.abs(loss_ref), 1e-3 * np.abs(lse_ref))

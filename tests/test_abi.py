@@ -1,0 +1,129 @@
+"""The C ABI without a GPU: libqk.so loads, exports every entry point that
+include/qk.h declares, and rejects bad arguments on the host before touching a
+device.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from memory_bound_row_rmsnorm_gb300 import binding as qb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qk.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"QK_API\s+[\w\s\*]+?\b(qk_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from memory_bound_row_rmsnorm_gb300 import build
+    build.build()
+    return qb.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("qk_softmax_fwd", "qk_rmsnorm_fwd", "qk_xent_fwd", "qk_status_string",
+                     "qk_get_device_status"):
+        assert required in names
+    assert sorted(names) == sorted(qb._EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libqk.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = qb.qk_status_string(code)
+        assert s and s != "unknown status"
+    assert qb.qk_status_string(99) == "unknown status"
+
+
+def test_max_row_elements(lib):
+    assert qb.qk_max_row_elements(qb.QK_OP_SOFTMAX, qb.QK_F32) == 262144
+    assert qb.qk_max_row_elements(qb.QK_OP_RMSNORM, qb.QK_BF16) == 524288
+    assert qb.qk_max_row_elements(qb.QK_OP_XENT, qb.QK_BF16) == 2 ** 63 - 1
+    assert qb.qk_max_row_elements(7, qb.QK_F32) == 0
+
+
+# Fake, never-dereferenced device addresses: every call below must be refused
+# by the host-side checks, which run before any CUDA call.
+A = 1 << 32
+
+
+@pytest.mark.parametrize("M,N,dtype,want", [
+    (-1, 4, qb.QK_F32, qb.QK_ERR_INVALID_ARG),
+    (4, 0, qb.QK_F32, qb.QK_ERR_INVALID_ARG),
+    (4, -3, qb.QK_BF16, qb.QK_ERR_INVALID_ARG),
+    (4, 4, 7, qb.QK_ERR_INVALID_ARG),
+    (4, 262145, qb.QK_F32, qb.QK_ERR_UNSUPPORTED),
+    (4, 524289, qb.QK_BF16, qb.QK_ERR_UNSUPPORTED),
+    (2 ** 40, 2 ** 40, qb.QK_F32, qb.QK_ERR_INVALID_ARG),
+])
+def test_softmax_size_errors(lib, M, N, dtype, want):
+    assert lib.qk_softmax_fwd(A, A + (1 << 30), M, N, dtype, None) == want
+
+
+def test_zero_rows_is_a_no_op(lib):
+    assert lib.qk_softmax_fwd(None, None, 0, 4, qb.QK_F32, None) == qb.QK_OK
+    assert lib.qk_rmsnorm_fwd(None, None, None, None, 0, 4, 1e-6, qb.QK_BF16, None) == qb.QK_OK
+    assert lib.qk_xent_fwd(None, None, None, None, 0, 4, qb.QK_F32, None) == qb.QK_OK
+
+
+def test_null_pointers(lib):
+    assert lib.qk_softmax_fwd(None, A, 4, 4, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_rmsnorm_fwd(A, None, A + 4096, None, 4, 4, 1e-6, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_xent_fwd(A, None, A + 4096, None, 4, 4, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_xent_fwd(A, A + 4096, None, None, 4, 4, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+
+
+def test_misaligned_pointers(lib):
+    assert lib.qk_softmax_fwd(A + 2, A + 4096, 4, 4, qb.QK_F32, None) == qb.QK_ERR_MISALIGNED
+    assert lib.qk_softmax_fwd(A + 1, A + 4096, 4, 4, qb.QK_BF16, None) == qb.QK_ERR_MISALIGNED
+    assert lib.qk_rmsnorm_fwd(A, A + 8192, A + 4096, A + 2 + 16384, 4, 4, 1e-6, qb.QK_F32, None) \
+        == qb.QK_ERR_MISALIGNED
+    assert lib.qk_xent_fwd(A, A + 4 + 4096, A + 8192, None, 4, 4, qb.QK_F32, None) == qb.QK_ERR_MISALIGNED
+
+
+def test_overlapping_buffers(lib):
+    # partial overlap of x and y (exact aliasing would be allowed)
+    assert lib.qk_softmax_fwd(A, A + 16, 4, 4, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    # y overlapping w, rstd overlapping x
+    assert lib.qk_rmsnorm_fwd(A, A + 4096, A + 4096, None, 4, 4, 1e-6, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_rmsnorm_fwd(A, A + 4096, A + 8192, A + 32, 4, 4, 1e-6, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    # loss overlapping the logits, lse overlapping the targets
+    assert lib.qk_xent_fwd(A, A + 4096, A + 8, None, 4, 4, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_xent_fwd(A, A + 4096, A + 8192, A + 4096, 4, 4, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("eps", [-1e-6, float("nan"), float("inf")])
+def test_bad_eps(lib, eps):
+    assert lib.qk_rmsnorm_fwd(A, A + 4096, A + 8192, None, 4, 4, eps, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+
+
+def test_plan_override_validation(lib):
+    bad = qb.qk_plan(threads=256, row_threads=96, vec_per_thread=4, cluster=1)
+    assert lib.qk_set_plan_override(qb.QK_OP_SOFTMAX, qb.QK_F32, ctypes.byref(bad)) == qb.QK_ERR_UNSUPPORTED
+    big = qb.qk_plan(threads=512, row_threads=512, vec_per_thread=8, cluster=32)
+    assert lib.qk_set_plan_override(qb.QK_OP_SOFTMAX, qb.QK_F32, ctypes.byref(big)) == qb.QK_ERR_INVALID_ARG
+    ok = qb.qk_plan(threads=256, row_threads=256, vec_per_thread=4, cluster=1)
+    assert lib.qk_set_plan_override(qb.QK_OP_SOFTMAX, qb.QK_F32, ctypes.byref(ok)) == qb.QK_OK
+    assert lib.qk_set_plan_override(qb.QK_OP_SOFTMAX, qb.QK_F32, None) == qb.QK_OK
+    assert lib.qk_set_plan_override(5, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+
+
+def test_timeout_hook_argument_checks(lib):
+    assert lib.qk_test_wait_timeout(0, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_test_wait_timeout(20_000_000_000, None) == qb.QK_ERR_INVALID_ARG
+
+
+def test_binding_raises_on_error(lib):
+    with pytest.raises(qb.QkError) as e:
+        qb.qk_softmax_fwd(A, A + 16, 4, 4, qb.QK_F32, 0)
+    assert e.value.status == qb.QK_ERR_INVALID_ARG
