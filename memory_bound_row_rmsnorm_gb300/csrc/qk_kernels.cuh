@@ -438,11 +438,13 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
       tm = pm;
       if constexpr (OP == kXent) {
 #pragma unroll
-        for (int k = 0; k < EPT; ++k)
-          if (e0 + c0 + tid + int64_t(k) * THREADS == trow) {
+        for (int k = 0; k < EPT; ++k) {
+          const int64_t e = c0 + tid + int64_t(k) * THREADS;  // padding lanes never match
+          if (e < ne && e0 + e == trow) {
             xt = f[k];
             own_t = true;
           }
+        }
       }
     }
   }
