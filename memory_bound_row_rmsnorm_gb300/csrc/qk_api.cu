@@ -330,18 +330,23 @@ int64_t max_row_elements(int op, int dt) {
 
 qk_status launch(const Plan& p, const RowArgs& a, void* stream) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(unsigned(p.grid), 1, 1);
   cfg.blockDim = dim3(unsigned(p.kernel->threads), 1, 1);
   cfg.dynamicSmemBytes = size_t(p.smem);
   cfg.stream = static_cast<cudaStream_t>(stream);
+  // The kernels wait for the previous grid (griddepcontrol.wait) before their
+  // first global access, so they may be launched before it finishes.
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (p.kernel->clustered) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(p.cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(p.cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   RowArgs args = a;
   void* params[] = {&args};

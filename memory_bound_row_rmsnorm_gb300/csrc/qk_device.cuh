@@ -109,6 +109,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream is still
+// running; grid_dependency_wait() blocks until that kernel has completed and
+// its writes are visible, so it must precede the first global-memory access.
+// allow_dependent_launch() lets the next kernel in the stream start early
+// (it takes effect once every CTA of this grid has issued it or exited).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void report_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
@@ -169,6 +182,42 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (sm_100+ f32x2 forms): two IEEE round-to-nearest
+// results per instruction, bit-identical to the scalar operations.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// Element-wise maximum of two packed bf16 pairs (exact; NaN loses to a number).
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Online-softmax pair: m = running maximum, s = sum of exp(x - m).  Merging
 // two pairs rescales both sums to the larger maximum.  A pair with m = -inf
 // (no elements yet) contributes nothing and never produces inf - inf.
@@ -217,6 +266,13 @@ struct Vec16<float> {
     f[3] = __uint_as_float(v.w);
   }
   __device__ __forceinline__ static void unpack_fresh(const uint4& v, float* f) { unpack(v, f); }
+  // Bit pattern of -inf in every element: the neutral value of a maximum.
+  static constexpr uint32_t kNegInfBits = 0xff800000u;
+  // Running maximum over the four elements of v.
+  __device__ __forceinline__ static float max_into(float m, const uint4& v) {
+    return fmaxf(fmaxf(m, fmaxf(__uint_as_float(v.x), __uint_as_float(v.y))),
+                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
   __device__ __forceinline__ static uint4 pack(const float* f) {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                       __float_as_uint(f[3]));
@@ -240,6 +296,15 @@ struct Vec16<__nv_bfloat16> {
     unpack2(v.y, f[2], f[3]);
     unpack2(v.z, f[4], f[5]);
     unpack2(v.w, f[6], f[7]);
+  }
+  static constexpr uint32_t kNegInfBits = 0xff80ff80u;
+  // Running maximum over the eight elements of v, compared as packed bf16
+  // pairs (exact), widened once at the end.
+  __device__ __forceinline__ static float max_into(float m, const uint4& v) {
+    const uint32_t p = max_bf16x2(max_bf16x2(v.x, v.y), max_bf16x2(v.z, v.w));
+    float lo, hi;
+    unpack2(p, lo, hi);
+    return fmaxf(m, fmaxf(lo, hi));
   }
   // Same as unpack, but opaque to the optimiser: it cannot be hoisted out of
   // a loop or merged with an earlier unpack, so the packed form (half the

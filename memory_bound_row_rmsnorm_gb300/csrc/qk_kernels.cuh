@@ -113,37 +113,47 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   } else {
     __syncthreads();
   }
+  // Everything above touched only shared memory; from here on global memory
+  // is read, which the previous kernel in the stream may still be writing.
+  grid_dependency_wait();
+  allow_dependent_launch();
 
+  // Producer state (thread 0 only): the next step to load, as (item, chunk)
+  // and its ring slot.  Steps are issued in order, so everything advances by
+  // increments -- no 64-bit division in the loop.
   uint64_t policy = 0;
-  // Producer (thread 0): load local step q into ring slot q % S.
-  auto issue = [&](int64_t q) {
-    const int64_t i = q / K, j = q - (q / K) * K;
-    const int64_t item = int64_t(cid) + i * ncl;
+  int64_t p_item = cid, p_left = q_total;
+  int p_chunk = 0, p_slot = 0;
+  auto issue_next = [&]() {
     int64_t off, bytes;
     if (K > 1) {  // one chunk of a streamed row
-      const int64_t c0 = j * CH;
-      off = (item * NV + c0) * 16;
+      const int64_t c0 = int64_t(p_chunk) * CH;
+      off = (p_item * NV + c0) * 16;
       bytes = min(CH, NV - c0) * 16;
     } else if (CLUSTER) {  // this CTA's slice of one row
-      off = (item * NV + v0) * 16;
+      off = (p_item * NV + v0) * 16;
       bytes = nv * 16;
     } else {  // R consecutive rows
-      const int64_t r0 = item * R;
+      const int64_t r0 = p_item * R;
       off = r0 * NV * 16;
       bytes = min(int64_t(R), M - r0) * NV * 16;
     }
-    const int slot = int(q % S);
-    const uint32_t dst = ring0 + uint32_t(slot) * a.slot_bytes;
-    const uint32_t bar = full0 + 8u * uint32_t(slot);
+    const uint32_t dst = ring0 + uint32_t(p_slot) * a.slot_bytes;
+    const uint32_t bar = full0 + 8u * uint32_t(p_slot);
     mbar_arrive_expect_tx(bar, uint32_t(bytes));
     for (int64_t o = 0; o < bytes; o += kCopyBytes)
       bulk_copy_g2s(dst + uint32_t(o), xg + off + o, uint32_t(min(kCopyBytes, bytes - o)), bar,
                     policy);
+    if (++p_slot == S) p_slot = 0;
+    if (++p_chunk == K) {
+      p_chunk = 0;
+      p_item += ncl;
+    }
+    --p_left;
   };
   if (tid == 0) {
     policy = l2_evict_first_policy();
-    const int64_t pre = min(int64_t(S), q_total);
-    for (int64_t q = 0; q < pre; ++q) issue(q);
+    for (int s = 0; s < S && p_left > 0; ++s) issue_next();
   }
 
   // RMSNorm weight: the columns a thread touches never change, so its share
@@ -166,13 +176,14 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   int64_t trow = -1;
   bool failed = false;  // a wait of this thread ran out
   bool abort = false;   // block-uniform: some thread's wait ran out
-  int64_t q = 0;
+  // Consumer position: step q is chunk j of local item i (item = cid + i*ncl),
+  // held in ring slot `slot` whose barrier phase parity is `phase`.
+  int64_t q = 0, item = cid;
+  int j = 0, slot = 0;
+  uint32_t phase = 0, ibit = 0, xphase = 0;  // parities: ring, item (red/xbuf), cluster barrier
 
   for (; q < q_total; ++q) {
-    const int64_t i = q / K, j = q - (q / K) * K;
-    const int64_t item = int64_t(cid) + i * ncl;
-    const int slot = int(q % S);
-    if (!mbar_wait<false>(full0 + 8u * uint32_t(slot), uint32_t((q / S) & 1), a.timeout_ns)) {
+    if (!mbar_wait<false>(full0 + 8u * uint32_t(slot), phase, a.timeout_ns)) {
       report_status(a.status, kStatusTimeout);
       failed = true;
     }
@@ -180,101 +191,103 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     const bool single = (K > 1) || CLUSTER;  // one row per item
     const int64_t row = single ? item : item * R + g;
     const bool row_ok = row < M;
-    const int64_t cn = (K > 1) ? min(CH, NV - j * CH) : nv;  // vectors of this row in the slot
-    const int64_t cbase = (K > 1) ? j * CH : v0;              // first column vector in the slot
+    const int cn = int((K > 1) ? min(CH, NV - int64_t(j) * CH) : nv);  // vectors of this row in the slot
+    const int64_t cbase = (K > 1) ? int64_t(j) * CH : v0;               // first column vector in the slot
     const unsigned char* sb =
         ring + size_t(slot) * a.slot_bytes + (single ? size_t(0) : size_t(g) * size_t(NV) * 16);
 
+    // Padding lanes get the reduction's neutral element (0 for a sum of
+    // squares, -inf for a maximum / sum of exponentials), so the arithmetic
+    // below needs no per-element masking.
+    constexpr uint32_t kFill = (OP == kRmsNorm) ? 0u : V::kNegInfBits;
     bool valid[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      const int64_t lv = l + int64_t(k) * TPR;
+      const int lv = l + k * TPR;
       valid[k] = row_ok && lv < cn && !failed;
-      xr[k] = valid[k] ? *reinterpret_cast<const uint4*>(sb + lv * 16) : make_uint4(0u, 0u, 0u, 0u);
+      xr[k] = valid[k] ? *reinterpret_cast<const uint4*>(sb + lv * 16)
+                       : make_uint4(kFill, kFill, kFill, kFill);
     }
 
     // ---- thread-level reduction (registers) ----
     float pm = kNegInf, ps = 0.f;  // partial (max, sum-exp), or (-, sum of squares)
     float tm = kNegInf;            // softmax: this thread's own maximum
     if constexpr (OP == kRmsNorm) {
-      float acc = 0.f;
+      float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         float f[E];
         V::unpack(xr[k], f);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(f[e], f[e], acc);  // masked vectors are zero
+        for (int e = 0; e < E; e += 2) {
+          const float2 v = make_float2(f[e], f[e + 1]);
+          acc = fma2(v, v, acc);
+        }
       }
-      ps = acc;
-    } else if constexpr (OP == kSoftmax) {
+      ps = acc.x + acc.y;
+    } else {
+      if constexpr (OP == kXent) {
+        if (j == 0) {
+          run_m = kNegInf;
+          run_s = 0.f;
+          own_t = false;
+          trow = row_ok ? a.target[row] : -1;
+        }
+        if (trow >= 0 && trow < N) {  // capture x[target] if it is in this thread's vectors
+          const int64_t tl = trow / E - cbase;  // target vector, relative to the slot
+          if (tl >= 0 && tl < cn && int(tl) % TPR == l) {
+            const int kk = int(tl) / TPR, ee = int(trow % E);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+              if (k != kk) continue;
+              float f[E];
+              V::unpack(xr[k], f);
+#pragma unroll
+              for (int e = 0; e < E; ++e)
+                if (e == ee) xt = f[e];
+            }
+            own_t = true;
+          }
+        }
+      }
+      float m = (OP == kXent) ? run_m : kNegInf;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) m = V::max_into(m, xr[k]);
+      const float mb = (m == kNegInf) ? 0.f : m * kLog2e;
+      const float2 l2e = make_float2(kLog2e, kLog2e), nmb = make_float2(-mb, -mb);
+      float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
-        V::unpack(xr[k], &ef[k * E]);
+        float f[E];
+        V::unpack(xr[k], f);
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-          if (valid[k]) tm = fmaxf(tm, ef[k * E + e]);
-      }
-      const float mb = (tm == kNegInf) ? 0.f : tm * kLog2e;
-      float s = 0.f;
-#pragma unroll
-      for (int k = 0; k < VPT; ++k)
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float v = valid[k] ? exp2_approx(fmaf(ef[k * E + e], kLog2e, -mb)) : 0.f;
-          ef[k * E + e] = v;
-          s += v;
-        }
-      pm = tm;
-      ps = s;
-    } else {  // cross-entropy: online pair over the chunks of the row
-      if (j == 0) {
-        run_m = kNegInf;
-        run_s = 0.f;
-        own_t = false;
-        trow = row_ok ? a.target[row] : -1;
-      }
-      float f[VPT * E];
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) V::unpack(xr[k], &f[k * E]);
-      if (trow >= 0 && trow < N) {
-        const int64_t tl = trow / E - cbase;  // target vector, relative to the slot
-        if (tl >= 0 && tl < cn && tl % TPR == l) {
-          const int kk = int(tl / TPR), ee = int(trow % E);
-#pragma unroll
-          for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-              if (k == kk && e == ee) xt = f[k * E + e];
-          own_t = true;
+        for (int e = 0; e < E; e += 2) {
+          const float2 t = fma2(make_float2(f[e], f[e + 1]), l2e, nmb);
+          const float2 ev = make_float2(exp2_approx(t.x), exp2_approx(t.y));  // padding: 2^-inf = 0
+          if constexpr (OP == kSoftmax) {
+            ef[k * E + e] = ev.x;
+            ef[k * E + e + 1] = ev.y;
+          }
+          acc = add2(acc, ev);
         }
       }
-      float m = run_m;
-#pragma unroll
-      for (int k = 0; k < VPT; ++k)
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          if (valid[k]) m = fmaxf(m, f[k * E + e]);
-      if (m != kNegInf) {
-        run_s *= exp2_approx((run_m - m) * kLog2e);  // rescale to the new maximum
-        const float mb = m * kLog2e;
-        float s = 0.f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-          for (int e = 0; e < E; ++e)
-            if (valid[k]) s += exp2_approx(fmaf(f[k * E + e], kLog2e, -mb));
-        run_s += s;
+      if constexpr (OP == kSoftmax) {
+        tm = m;
+        pm = m;
+        ps = acc.x + acc.y;
+      } else {  // fold the chunk into the running pair of the row
+        if (m != kNegInf) run_s = run_s * exp2_approx((run_m - m) * kLog2e) + (acc.x + acc.y);
         run_m = m;
+        pm = run_m;
+        ps = run_s;
       }
-      pm = run_m;
-      ps = run_s;
     }
 
     // ---- warp butterfly; warp partials to the block buffer ----
     const bool row_end = (j == K - 1);
     if (row_end) {
       warp_reduce<OP>(pm, ps);
-      if (WPG > 1 && lane == 0) red[(i & 1) * 16 + warp] = make_float2(pm, ps);
+      if (WPG > 1 && lane == 0) red[ibit * 16 + warp] = make_float2(pm, ps);
     }
     // One barrier per step: the slot is free again (every thread has its data
     // in registers) and the warp partials are visible.  It also carries a
@@ -283,12 +296,28 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       abort = true;
       break;
     }
-    if (tid == 0 && q + S < q_total) issue(q + S);
-    if (!row_end) continue;
+    if (tid == 0 && p_left > 0) issue_next();
+    // advance the consumer position to step q + 1
+    const int64_t row_item = item;
+    const uint32_t row_ibit = ibit, row_xphase = xphase;
+    if (++slot == S) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    if (row_end) {
+      j = 0;
+      item += ncl;
+      xphase ^= ibit;  // the cluster barrier of buffer b flips every second item
+      ibit ^= 1u;
+    } else {
+      ++j;
+      continue;
+    }
+    (void)row_item;
 
     // ---- block reduction over the warps of this row group ----
     if constexpr (WPG > 1) {
-      const float2* rg = red + (i & 1) * 16 + g * WPG;
+      const float2* rg = red + row_ibit * 16 + g * WPG;
       float2 p = rg[0];
       pm = p.x;
       ps = p.y;
@@ -301,14 +330,14 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
 
     // ---- cluster reduction: every CTA's partial into every peer (DSMEM) ----
     if constexpr (CLUSTER) {
-      const uint32_t b = uint32_t(i & 1);
+      const uint32_t b = row_ibit;
       const uint32_t xb = xbar0 + 8u * b;
       if (tid == 0) {
         mbar_arrive_expect_tx(xb, C * 8u);
         const uint32_t mine = smem_addr(xbuf + b * kMaxCluster + rank);
         for (uint32_t r = 0; r < C; ++r) st_async_f2(map_to_rank(mine, r), pm, ps, map_to_rank(xb, r));
       }
-      if (!mbar_wait<true>(xb, uint32_t((i >> 1) & 1), a.timeout_ns)) {
+      if (!mbar_wait<true>(xb, row_xphase, a.timeout_ns)) {
         report_status(a.status, kStatusTimeout);
         failed = true;
       }
@@ -326,17 +355,23 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     if (!row_ok) continue;
     if constexpr (OP == kSoftmax) {
       const float scale = (tm == kNegInf) ? 0.f : exp2_approx((tm - pm) * kLog2e) / ps;
+      const float2 sc = make_float2(scale, scale);
       uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!valid[k]) continue;
         float o[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = ef[k * E + e] * scale;
+        for (int e = 0; e < E; e += 2) {
+          const float2 v = mul2(make_float2(ef[k * E + e], ef[k * E + e + 1]), sc);
+          o[e] = v.x;
+          o[e + 1] = v.y;
+        }
         yg[l + k * TPR] = V::pack(o);
       }
     } else if constexpr (OP == kRmsNorm) {
       const float r = 1.0f / sqrtf(ps / float(N) + a.eps);
+      const float2 r2 = make_float2(r, r);
       uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -345,7 +380,11 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         V::unpack_fresh(xr[k], f);
         V::unpack_fresh(wv[k], w);
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = __fmul_rn(__fmul_rn(f[e], r), w[e]);
+        for (int e = 0; e < E; e += 2) {  // (x * rstd) * w, each product rounded once
+          const float2 v = mul2(mul2(make_float2(f[e], f[e + 1]), r2), make_float2(w[e], w[e + 1]));
+          o[e] = v.x;
+          o[e + 1] = v.y;
+        }
         yg[l + k * TPR] = V::pack(o);
       }
       if (l == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = r;
@@ -360,11 +399,17 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   }
 
   if (abort) {
-    // Leave no bulk copy in flight into this CTA's shared memory.
+    // Leave no bulk copy in flight into this CTA's shared memory: wait (bounded)
+    // for every step issued but not consumed, from the current ring position on.
     if (tid == 0) {
-      const int64_t end = min(q_total, q + S);
-      for (int64_t qq = q; qq < end; ++qq)
-        mbar_wait<false>(full0 + 8u * uint32_t(qq % S), uint32_t((qq / S) & 1), a.timeout_ns);
+      const int64_t outstanding = (q_total - q) - p_left;
+      for (int64_t n = 0; n < outstanding; ++n) {
+        mbar_wait<false>(full0 + 8u * uint32_t(slot), phase, a.timeout_ns);
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
     }
     __syncthreads();
   }
@@ -404,6 +449,8 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
     }
     cluster_sync_all();
   }
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   const T* xrow = static_cast<const T*>(a.x) + row * N + e0;
   float f[EPT];
