@@ -36,7 +36,7 @@ namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s bound on any in-kernel wait
 constexpr int kMaxDevices = 64;
-constexpr int kRingMaxVectorsPerCta = 4096;  // 512 threads x 8 vectors
+constexpr int kRingMaxVectorsPerCta = 4096;  // 256 threads x 16 vectors, or 512 x 8
 constexpr int64_t kMaxRowBytes = int64_t(kMaxCluster) * kRingMaxVectorsPerCta * 16;  // 1 MiB
 
 struct DeviceInfo {
@@ -195,30 +195,54 @@ struct Plan {
   int64_t grid = 0;
 };
 
+// The fast path's plan table: for rows of at most max_nv 16-byte vectors,
+// (threads, row_threads, vec_per_thread, cluster, slots).  Chosen from sweeps
+// of every compiled configuration on GB300 (M = 16384 rows, N = 256 ... 262144,
+// fp32 and bf16): short rows share a warp (sub-warp row groups), mid rows
+// give each thread 32-64 elements so the per-row reduction is amortised, long
+// rows are split over a thread-block cluster of 256-thread CTAs (small CTAs
+// pack the GPCs better than 512-thread ones).  A one-slot ring is enough when
+// the slice is held in registers: the slot is refilled as soon as it has been
+// read, while the previous row is still being reduced and stored.
+struct Choice {
+  int64_t max_nv;
+  int threads, row_threads, vec_per_thread, cluster, slots;
+};
+constexpr int64_t kStream = INT64_MAX;  // cross-entropy: any longer row is streamed
+const Choice kRmsNormTable[] = {
+    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 2},       {128, 256, 32, 4, 1, 2},
+    {256, 256, 64, 4, 1, 1},     {512, 128, 128, 4, 1, 1},     {1024, 128, 128, 8, 1, 1},
+    {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {16384, 256, 256, 8, 8, 3},  {32768, 256, 256, 8, 16, 2},  {65536, 512, 512, 8, 16, 2},
+};
+const Choice kSoftmaxTable[] = {
+    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 2},       {128, 256, 32, 4, 1, 2},
+    {256, 256, 64, 4, 1, 2},     {512, 256, 128, 4, 1, 1},     {1024, 256, 256, 4, 1, 1},
+    {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {16384, 256, 256, 8, 8, 3},  {32768, 256, 256, 16, 8, 1},  {65536, 256, 256, 16, 16, 1},
+};
+const Choice kXentTable[] = {
+    {32, 256, 8, 4, 1, 1},       {64, 256, 8, 8, 1, 1},        {128, 256, 16, 8, 1, 1},
+    {256, 256, 32, 8, 1, 2},     {512, 256, 64, 8, 1, 2},      {1024, 256, 128, 8, 1, 2},
+    {2048, 256, 256, 8, 1, 2},   {kStream, 256, 256, 4, 1, 2},  // 16 KB chunks
+};
+
 // Chooses the ring kernel (fast path) for a row of NV 16-byte vectors.
-qk_status choose_ring(int op, int dt, int64_t NV, int* th, int* tpr, int* vpt, int* cl, int* k) {
-  *cl = 1;
-  *k = 1;
-  if (op == kXent && NV > kRingMaxVectorsPerCta) {  // stream long rows in 32 KB chunks
-    *th = 512, *tpr = 512, *vpt = 4;
-    *k = int((NV + 2047) / 2048);
+qk_status choose_ring(int op, int64_t NV, int* th, int* tpr, int* vpt, int* cl, int* k,
+                      int* slots) {
+  const Choice* t = op == kRmsNorm ? kRmsNormTable : op == kSoftmax ? kSoftmaxTable : kXentTable;
+  const int n = op == kRmsNorm ? int(sizeof(kRmsNormTable) / sizeof(Choice))
+                : op == kSoftmax ? int(sizeof(kSoftmaxTable) / sizeof(Choice))
+                                 : int(sizeof(kXentTable) / sizeof(Choice));
+  for (int i = 0; i < n; ++i) {
+    if (NV > t[i].max_nv) continue;
+    *th = t[i].threads, *tpr = t[i].row_threads, *vpt = t[i].vec_per_thread;
+    *cl = t[i].cluster, *slots = t[i].slots;
+    const int64_t per_cta = int64_t(*tpr) * *vpt;
+    *k = (t[i].max_nv == kStream) ? int((NV + per_cta - 1) / per_cta) : 1;
     return QK_OK;
   }
-  if (NV <= 32) *th = 256, *tpr = 32, *vpt = 1;
-  else if (NV <= 64) *th = 256, *tpr = 32, *vpt = 2;
-  else if (NV <= 128) *th = 256, *tpr = 32, *vpt = 4;
-  else if (NV <= 256) *th = 256, *tpr = 64, *vpt = 4;
-  else if (NV <= 512) *th = 256, *tpr = 128, *vpt = 4;
-  else if (NV <= 1024) *th = 256, *tpr = 256, *vpt = 4;
-  else if (NV <= 2048) *th = 512, *tpr = 512, *vpt = 4;
-  else {
-    *th = 512, *tpr = 512, *vpt = 8;
-    const int64_t c = (NV + kRingMaxVectorsPerCta - 1) / kRingMaxVectorsPerCta;
-    if (c > kMaxCluster) return QK_ERR_UNSUPPORTED;
-    *cl = c > 1 ? next_pow2(c) : 1;
-  }
-  (void)dt;
-  return QK_OK;
+  return QK_ERR_UNSUPPORTED;
 }
 
 qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p) {
@@ -242,7 +266,7 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
       return QK_ERR_UNSUPPORTED;
     }
   } else {
-    qk_status st = choose_ring(op, dt, NV, &th, &tpr, &vpt, &cl, &k);
+    qk_status st = choose_ring(op, NV, &th, &tpr, &vpt, &cl, &k, &slots);
     if (st != QK_OK) return st;
   }
   const KernelEntry* ke = find_kernel(op, dt, 1, th, tpr, vpt, cl > 1);
@@ -261,10 +285,7 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
     p->num_items = (M + R - 1) / R;
   }
   const uint32_t slot_bytes = uint32_t((item_bytes + 127) / 128 * 128);
-  if (slots <= 0) {
-    const int64_t budget = k > 1 ? 196608 : (cl > 1 ? 196608 : 65536);
-    slots = int(std::min<int64_t>(cl > 1 ? 4 : 8, std::max<int64_t>(2, budget / slot_bytes)));
-  }
+  if (slots <= 0) slots = 2;  // an override without a slot count
   slots = std::min(slots, kMaxSlots);
   while (slots > 1 && kSmemHeader + int64_t(slots) * slot_bytes > d.smem_optin) --slots;
   const int64_t smem = kSmemHeader + int64_t(slots) * slot_bytes;

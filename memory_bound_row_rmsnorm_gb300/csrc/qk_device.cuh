@@ -218,36 +218,31 @@ __device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Online-softmax pair: m = running maximum, s = sum of exp(x - m).  Merging
-// two pairs rescales both sums to the larger maximum.  A pair with m = -inf
-// (no elements yet) contributes nothing and never produces inf - inf.
-__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
-  const float mn = fmaxf(m, m2);
-  if (mn == kNegInf) {
-    s = 0.f;
-    m = mn;
-    return;
-  }
-  // Explicit roundings (no fused multiply-add): merge(a, b) == merge(b, a)
-  // bit for bit, so both lanes of a butterfly step agree exactly.
-  s = __fadd_rn(__fmul_rn(s, exp2_approx((m - mn) * kLog2e)),
-                __fmul_rn(s2, exp2_approx((m2 - mn) * kLog2e)));
-  m = mn;
-}
-
-// Butterfly (xor) reductions: after the loop every lane holds the result.
-__device__ __forceinline__ float warp_sum(float v) {
+// Butterfly (xor) reductions over groups of WIDTH consecutive lanes (WIDTH a
+// power of two <= 32): after the loop every lane holds its group's result.
+// Addition is commutative in IEEE arithmetic, so both lanes of each step
+// compute the same value and all lanes of a group agree bit for bit.
+template <int WIDTH = 32>
+__device__ __forceinline__ float group_sum(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = WIDTH / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-__device__ __forceinline__ void warp_ms(float& m, float& s) {
+template <int WIDTH = 32>
+__device__ __forceinline__ float group_max(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    ms_merge(m, s, m2, s2);
-  }
+  for (int o = WIDTH / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// Reduces online-softmax pairs over the group: the maximum first, then each
+// lane rescales its own sum to it once, then a plain sum.  One SFU op per lane
+// instead of two per butterfly step.
+template <int WIDTH = 32>
+__device__ __forceinline__ void group_ms(float& m, float& s) {
+  const float mg = group_max<WIDTH>(m);
+  const float sl = (m == kNegInf) ? 0.f : s * exp2_approx((m - mg) * kLog2e);
+  s = group_sum<WIDTH>(sl);
+  m = mg;
 }
 
 // ---------------------------------------------------------------------------

@@ -1,6 +1,7 @@
 // Kernel instances for rmsnorm forward, bf16 rows.
 #define QK_OP 1
 #define QK_T __nv_bfloat16
+#define QK_ELEM_BYTES 2
 #include "qk_kernel_table.cuh"
 
 namespace qk {

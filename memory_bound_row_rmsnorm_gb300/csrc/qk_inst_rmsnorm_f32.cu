@@ -1,6 +1,7 @@
 // Kernel instances for rmsnorm forward, f32 rows.
 #define QK_OP 1
 #define QK_T float
+#define QK_ELEM_BYTES 4
 #include "qk_kernel_table.cuh"
 
 namespace qk {

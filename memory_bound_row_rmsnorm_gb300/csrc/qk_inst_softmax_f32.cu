@@ -1,6 +1,7 @@
 // Kernel instances for softmax forward, f32 rows.
 #define QK_OP 0
 #define QK_T float
+#define QK_ELEM_BYTES 4
 #include "qk_kernel_table.cuh"
 
 namespace qk {

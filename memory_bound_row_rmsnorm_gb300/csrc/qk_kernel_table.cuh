@@ -16,22 +16,35 @@
 namespace qk {
 namespace {
 const KernelEntry kTable[] = {
+    QK_RING(256, 8, 4, false),
+    QK_RING(256, 8, 8, false),
+    QK_RING(256, 16, 4, false),
+    QK_RING(256, 16, 8, false),
+    QK_RING(256, 32, 8, false),
+    QK_RING(256, 32, 16, false),
+    QK_RING(256, 64, 8, false),
+    QK_RING(256, 128, 8, false),
     QK_RING(256, 32, 1, false),
     QK_RING(256, 32, 2, false),
     QK_RING(256, 32, 4, false),
+    QK_RING(256, 64, 2, false),
     QK_RING(256, 64, 4, false),
     QK_RING(256, 128, 2, false),
     QK_RING(256, 128, 4, false),
     QK_RING(128, 128, 4, false),
+    QK_RING(128, 128, 8, false),
     QK_RING(256, 256, 2, false),
     QK_RING(256, 256, 4, false),
     QK_RING(256, 256, 8, false),
+    QK_RING(512, 512, 2, false),
     QK_RING(512, 512, 4, false),
     QK_RING(512, 512, 8, false),
 #if QK_OP != 2  // cross-entropy streams long rows instead of splitting them
+    QK_RING(256, 256, 4, true),
     QK_RING(256, 256, 8, true),
     QK_RING(512, 512, 4, true),
     QK_RING(512, 512, 8, true),
+    QK_RING(256, 256, 16, true),
 #endif
     QK_DIRECT(128, 4, false),
     QK_DIRECT(256, 16, false),

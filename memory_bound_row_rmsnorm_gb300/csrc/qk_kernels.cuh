@@ -36,22 +36,34 @@ namespace qk {
 constexpr int64_t kCopyBytes = 32768;  // largest single bulk copy issued
 constexpr int kStatusTimeout = 5;      // QK_ERR_TIMEOUT
 
-template <int OP>
-__device__ __forceinline__ void combine(float& m, float& s, float m2, float s2) {
+// Reduces the pair (m, s) (or the sum s for RMSNorm) over WIDTH lanes.
+template <int OP, int WIDTH = 32>
+__device__ __forceinline__ void warp_reduce(float& m, float& s) {
   if constexpr (OP == kRmsNorm) {
-    s += s2;
+    s = group_sum<WIDTH>(s);
   } else {
-    ms_merge(m, s, m2, s2);
+    group_ms<WIDTH>(m, s);
   }
 }
 
-// Reduces the pair (m, s) (or the sum s for RMSNorm) over the warp.
+// Merges n partial pairs (or sums) p[0..n) in index order: the maximum first,
+// then each partial rescaled to it once.  Every thread that calls this with
+// the same partials gets the same bits.
 template <int OP>
-__device__ __forceinline__ void warp_reduce(float& m, float& s) {
+__device__ __forceinline__ void merge_partials(const float2* p, int n, float& m, float& s) {
   if constexpr (OP == kRmsNorm) {
-    s = warp_sum(s);
+    float acc = p[0].y;
+    for (int w = 1; w < n; ++w) acc += p[w].y;
+    s = acc;
   } else {
-    warp_ms(m, s);
+    float mx = p[0].x;
+    for (int w = 1; w < n; ++w) mx = fmaxf(mx, p[w].x);
+    float acc = 0.f;
+    if (mx != kNegInf)
+      for (int w = 0; w < n; ++w)
+        if (p[w].x != kNegInf) acc += p[w].y * exp2_approx((p[w].x - mx) * kLog2e);
+    m = mx;
+    s = acc;
   }
 }
 
@@ -60,10 +72,12 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   using V = Vec16<T>;
   constexpr int E = V::kElems;       // elements per 16-byte vector
   constexpr int NW = THREADS / 32;   // warps per CTA
-  constexpr int WPG = TPR / 32;      // warps per row group
+  constexpr int WPG = TPR / 32;      // warps per row group (0: a group is part of a warp)
+  constexpr int GW = TPR < 32 ? TPR : 32;  // lanes of a warp that share a row
   constexpr int R = THREADS / TPR;   // rows per item (unclustered, unchunked)
   constexpr int64_t CH = int64_t(TPR) * VPT;  // vectors per row-slice chunk
-  static_assert(TPR % 32 == 0 && THREADS % TPR == 0, "row groups are whole warps");
+  static_assert((TPR % 32 == 0 || 32 % TPR == 0) && THREADS % TPR == 0 && TPR >= 4,
+                "a row group is whole warps or a power-of-two part of one");
   static_assert(!CLUSTER || TPR == THREADS, "a clustered row spans the whole CTA");
   static_assert(NW <= 16, "block-reduction buffer holds 16 warps");
 
@@ -157,10 +171,13 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   }
 
   // RMSNorm weight: the columns a thread touches never change, so its share
-  // of w is loaded once into registers.
-  uint4 wv[VPT];
-  if constexpr (OP == kRmsNorm) {
-    const uint4* wg = static_cast<const uint4*>(a.w) + v0;
+  // of w is loaded once into registers -- unless that would take more than
+  // 8 vectors of registers, in which case the finish re-reads it through L1
+  // (the slice a CTA needs stays cached there; HBM sees w once).
+  constexpr bool kWeightInRegs = VPT <= 8;
+  uint4 wv[kWeightInRegs ? VPT : 1];
+  const uint4* wg = static_cast<const uint4*>(a.w) + v0;
+  if constexpr (OP == kRmsNorm && kWeightInRegs) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int64_t lv = l + int64_t(k) * TPR;
@@ -168,12 +185,23 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     }
   }
 
-  uint4 xr[VPT];        // raw input vectors of the current row (chunk)
-  float ef[VPT * E];    // softmax: exp(x - thread max), kept until the finish
+  // Softmax keeps exp(x - thread max) in registers for the finish, unless
+  // that would take too many registers (bf16 with 16 vectors a thread, or 8 in
+  // a clustered kernel, where occupancy hides the DSMEM exchange): then the finish
+  // recomputes it from the packed input, trading one more SFU op per element
+  // for half the registers (more CTAs per SM).
+  constexpr bool kKeepExp = !(E == 8 && (VPT >= 16 || (CLUSTER && VPT >= 8)));
+  uint4 xr[VPT];                       // raw input vectors of the current row (chunk)
+  float ef[kKeepExp ? VPT * E : 1];    // softmax: exp(x - thread max)
   float run_m = kNegInf, run_s = 0.f;  // cross-entropy: running pair over chunks
   float xt = 0.f;                      // cross-entropy: x[target] if this thread holds it
   bool own_t = false;
   int64_t trow = -1;
+  int64_t t_next = -1;  // cross-entropy: target of the next item's row
+  if constexpr (OP == kXent) {
+    const int64_t row0 = (K > 1 || CLUSTER) ? int64_t(cid) : int64_t(cid) * R + g;
+    if (q_total > 0 && row0 < M) t_next = __ldg(a.target + row0);
+  }
   bool failed = false;  // a wait of this thread ran out
   bool abort = false;   // block-uniform: some thread's wait ran out
   // Consumer position: step q is chunk j of local item i (item = cid + i*ncl),
@@ -231,7 +259,9 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
           run_m = kNegInf;
           run_s = 0.f;
           own_t = false;
-          trow = row_ok ? a.target[row] : -1;
+          trow = t_next;  // loaded one item ahead, so its latency is hidden
+          const int64_t nrow = single ? item + ncl : (item + ncl) * R + g;
+          t_next = nrow < M ? __ldg(a.target + nrow) : -1;
         }
         if (trow >= 0 && trow < N) {  // capture x[target] if it is in this thread's vectors
           const int64_t tl = trow / E - cbase;  // target vector, relative to the slot
@@ -264,7 +294,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         for (int e = 0; e < E; e += 2) {
           const float2 t = fma2(make_float2(f[e], f[e + 1]), l2e, nmb);
           const float2 ev = make_float2(exp2_approx(t.x), exp2_approx(t.y));  // padding: 2^-inf = 0
-          if constexpr (OP == kSoftmax) {
+          if constexpr (OP == kSoftmax && kKeepExp) {
             ef[k * E + e] = ev.x;
             ef[k * E + e + 1] = ev.y;
           }
@@ -286,7 +316,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     // ---- warp butterfly; warp partials to the block buffer ----
     const bool row_end = (j == K - 1);
     if (row_end) {
-      warp_reduce<OP>(pm, ps);
+      warp_reduce<OP, GW>(pm, ps);
       if (WPG > 1 && lane == 0) red[ibit * 16 + warp] = make_float2(pm, ps);
     }
     // One barrier per step: the slot is free again (every thread has its data
@@ -316,17 +346,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     (void)row_item;
 
     // ---- block reduction over the warps of this row group ----
-    if constexpr (WPG > 1) {
-      const float2* rg = red + row_ibit * 16 + g * WPG;
-      float2 p = rg[0];
-      pm = p.x;
-      ps = p.y;
-#pragma unroll
-      for (int w = 1; w < WPG; ++w) {
-        p = rg[w];
-        combine<OP>(pm, ps, p.x, p.y);
-      }
-    }
+    if constexpr (WPG > 1) merge_partials<OP>(red + row_ibit * 16 + g * WPG, WPG, pm, ps);
 
     // ---- cluster reduction: every CTA's partial into every peer (DSMEM) ----
     if constexpr (CLUSTER) {
@@ -341,14 +361,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         report_status(a.status, kStatusTimeout);
         failed = true;
       }
-      const float2* xs = xbuf + b * kMaxCluster;
-      float2 p = xs[0];
-      pm = p.x;
-      ps = p.y;
-      for (uint32_t r = 1; r < C; ++r) {
-        p = xs[r];
-        combine<OP>(pm, ps, p.x, p.y);
-      }
+      merge_partials<OP>(xbuf + b * kMaxCluster, int(C), pm, ps);
     }
 
     // ---- finish: outputs from registers, each stored once ----
@@ -356,14 +369,24 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     if constexpr (OP == kSoftmax) {
       const float scale = (tm == kNegInf) ? 0.f : exp2_approx((tm - pm) * kLog2e) / ps;
       const float2 sc = make_float2(scale, scale);
+      const float mb = (tm == kNegInf) ? 0.f : tm * kLog2e;
       uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!valid[k]) continue;
         float o[E];
+        if constexpr (!kKeepExp) V::unpack_fresh(xr[k], o);
 #pragma unroll
         for (int e = 0; e < E; e += 2) {
-          const float2 v = mul2(make_float2(ef[k * E + e], ef[k * E + e + 1]), sc);
+          float2 ev;
+          if constexpr (kKeepExp) {
+            ev = make_float2(ef[k * E + e], ef[k * E + e + 1]);
+          } else {  // same argument and rounding as in the reduction pass
+            const float2 t = fma2(make_float2(o[e], o[e + 1]), make_float2(kLog2e, kLog2e),
+                                  make_float2(-mb, -mb));
+            ev = make_float2(exp2_approx(t.x), exp2_approx(t.y));
+          }
+          const float2 v = mul2(ev, sc);
           o[e] = v.x;
           o[e + 1] = v.y;
         }
@@ -378,7 +401,11 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         if (!valid[k]) continue;
         float f[E], w[E], o[E];
         V::unpack_fresh(xr[k], f);
-        V::unpack_fresh(wv[k], w);
+        if constexpr (kWeightInRegs) {
+          V::unpack_fresh(wv[k], w);
+        } else {
+          V::unpack(__ldg(wg + l + k * TPR), w);
+        }
 #pragma unroll
         for (int e = 0; e < E; e += 2) {  // (x * rstd) * w, each product rounded once
           const float2 v = mul2(mul2(make_float2(f[e], f[e + 1]), r2), make_float2(w[e], w[e + 1]));
@@ -499,16 +526,7 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
   warp_reduce<OP>(pm, ps);
   if (lane == 0) red[warp] = make_float2(pm, ps);
   __syncthreads();
-  {
-    float2 p = red[0];
-    pm = p.x;
-    ps = p.y;
-#pragma unroll
-    for (int w = 1; w < NW; ++w) {
-      p = red[w];
-      combine<OP>(pm, ps, p.x, p.y);
-    }
-  }
+  merge_partials<OP>(red, NW, pm, ps);
   if constexpr (CLUSTER) {
     if (tid == 0) {
       mbar_arrive_expect_tx(xb, C * 8u);
@@ -516,13 +534,7 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
       for (uint32_t r = 0; r < C; ++r) st_async_f2(map_to_rank(mine, r), pm, ps, map_to_rank(xb, r));
     }
     if (!mbar_wait<true>(xb, 0u, a.timeout_ns)) report_status(a.status, kStatusTimeout);
-    float2 p = xbuf[0];
-    pm = p.x;
-    ps = p.y;
-    for (uint32_t r = 1; r < C; ++r) {
-      p = xbuf[r];
-      combine<OP>(pm, ps, p.x, p.y);
-    }
+    merge_partials<OP>(xbuf, int(C), pm, ps);
   }
 
   if constexpr (OP == kSoftmax) {

@@ -145,6 +145,12 @@ PLANS = [
     dict(threads=512, row_threads=512, vec_per_thread=4, cluster=4, slots=3, grid=8),
     dict(threads=512, row_threads=512, vec_per_thread=8, cluster=8, slots=2, grid=8),
     dict(threads=512, row_threads=512, vec_per_thread=8, cluster=16, slots=2, grid=16),
+    dict(threads=256, row_threads=8, vec_per_thread=4, cluster=1, slots=2, grid=3),
+    dict(threads=256, row_threads=16, vec_per_thread=8, cluster=1, slots=1, grid=2),
+    dict(threads=256, row_threads=32, vec_per_thread=16, cluster=1, slots=2, grid=2),
+    dict(threads=256, row_threads=64, vec_per_thread=8, cluster=1, slots=1, grid=5),
+    dict(threads=256, row_threads=256, vec_per_thread=16, cluster=4, slots=1, grid=8),
+    dict(threads=256, row_threads=256, vec_per_thread=4, cluster=16, slots=3, grid=32),
 ]
 
 
@@ -158,7 +164,9 @@ def test_forced_plans(op, dtype, plan):
     cap = plan["row_threads"] * plan["vec_per_thread"] * E * plan["cluster"]
     # a row that fills most of the plan's capacity and is ragged in vectors
     N = max(E, cap - 3 * E) if cap > 4 * E else cap
-    M = 61 if N <= 8192 else 9
+    rows_per_step = plan["threads"] // plan["row_threads"]
+    # several steps per CTA, and a last step that is only partly filled
+    M = max(61, 3 * rows_per_step * plan["grid"] + 5) if N <= 8192 else 9
     if op == "xent" and plan["row_threads"] == plan["threads"]:
         N = 5 * cap + 7 * E  # streamed through several chunks per row
     qb.qk_set_plan_override(OP_CODE[op], DT_CODE[dtype], plan)
