@@ -181,6 +181,35 @@ def launch(qb, op, dtype, inp, out, M, N, stream):
         qb.qk_xent_fwd(inp["x"], inp["targets"], out["loss"], out["lse"], M, N, code, stream)
 
 
+def timed_launches(qb, op, dtype, sets, M, N, K, stream, graph: bool, dev):
+    """Enqueues K steps (rotating over `sets`) between two CUDA events on
+    `stream` and returns (start, stop).  With graph=True the K calls are first
+    captured into one CUDA graph (the library's launches, recorded once) and
+    the graph is replayed, which removes host launch overhead between steps."""
+    nsets = len(sets)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if not graph:
+        start.record(stream)
+        for i in range(K):
+            inp, out = sets[i % nsets]
+            launch(qb, op, dtype, inp, out, M, N, stream)
+        stop.record(stream)
+        return start, stop
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream(dev)
+        for i in range(K):
+            inp, out = sets[i % nsets]
+            launch(qb, op, dtype, inp, out, M, N, cs)
+    g.replay()  # first replay uploads the graph
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    g.replay()
+    stop.record(stream)
+    timed_launches.keep = g  # the graph must outlive the replay
+    return start, stop
+
+
 def cpu_oracle_rate(op, dtype, M, N, sigma, budget_s: float, seed: int = 4242):
     """The fp64 oracle, as it stands, over seeded rows of the workload on all
     host cores (one thread per core, each running the oracle on its own rows).
@@ -191,7 +220,7 @@ def cpu_oracle_rate(op, dtype, M, N, sigma, budget_s: float, seed: int = 4242):
 
     cores = os.cpu_count() or 1
     lib = oracle.library()
-    rows = min(M, max(cores, 64))
+    rows = min(M, max(cores * 16, 256))
     inp = syn.make_inputs(op, dtype, rows, N, seed, "cpu", sigma)
     x = inp["x"].to(torch.float64).numpy()
     w = inp["w"].to(torch.float64).numpy() if op == "rmsnorm" else None
@@ -278,6 +307,54 @@ def run_reference(args, op, dtype, M, N, sigma):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args, path):
+    """Every point of the M x N sweep grid (3 operators x fp32/bf16 x M x N),
+    timed with the library's default plan, one JSON line per point into
+    `path`; the summary line goes to stdout."""
+    from memory_bound_row_rmsnorm_gb300 import binding as qb
+    from memory_bound_row_rmsnorm_gb300 import build as qk_build
+    qk_build.build()
+    qb.load_library()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_src = measured_peak()
+    points = []
+    with open(path, "w") as fout:
+        for op in ("softmax", "rmsnorm", "xent"):
+            for dtype in ("f32", "bf16"):
+                for M in syn.SWEEP_M:
+                    for N in syn.SWEEP_N:
+                        sb = min_bytes(op, dtype, M, N)
+                        nsets = max(2, math.ceil(4 * L2_BYTES / sb))
+                        sets = [make_set(op, dtype, M, N, 1.0, 77 + i, dev) for i in range(nsets)]
+                        K = int(max(5, min(args.steps, 8e9 / sb)))
+                        for i in range(max(3, min(args.warmup, 20))):
+                            launch(qb, op, dtype, *sets[i % nsets], M, N, stream)
+                        torch.cuda.synchronize(dev)
+                        e0, e1 = timed_launches(qb, op, dtype, sets, M, N, K, stream, args.graph, dev)
+                        torch.cuda.synchronize(dev)
+                        if qb.qk_get_device_status(stream) != qb.QK_OK:
+                            raise RuntimeError("device status reports a failure")
+                        ms = e0.elapsed_time(e1) / K
+                        tbs = sb / (ms * 1e-3) / 1e12
+                        code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
+                        opc = {"softmax": 0, "rmsnorm": 1, "xent": 2}[op]
+                        rec = {"op": op, "dtype": dtype, "M": M, "N": N, "TBps": tbs,
+                               "frac": tbs * 1e3 / peak, "ms": ms, "steps": K,
+                               "launch": "cuda_graph" if args.graph else "stream",
+                               "plan": qb.qk_get_plan(opc, code, M, N)}
+                        fout.write(json.dumps(rec) + "\n")
+                        fout.flush()
+                        points.append(rec)
+                        del sets
+                        torch.cuda.empty_cache()
+    ge = [p for p in points if p["N"] >= 4096]
+    print(json.dumps({"sweep": path, "points": len(points), "peak_gbs": peak, "peak_source": peak_src,
+                      "min_frac_N_ge_4096": min(p["frac"] for p in ge),
+                      "median_frac_N_ge_4096": statistics.median(p["frac"] for p in ge)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -287,8 +364,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", metavar="JSONL", help="time every sweep point instead; write them here")
+    ap.add_argument("--graph", action="store_true",
+                    help="issue the timed steps as one CUDA-graph replay (no host launch overhead)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.sweep:
+        run_sweep(args, args.sweep)
+        return
     op, dtype, M, N, sigma = syn.WORKLOADS[args.workload]
 
     if args.impl == "reference":
@@ -329,16 +412,11 @@ def main():
         raise RuntimeError("device status reports a failure after warm-up")
 
     K = args.steps
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
-        start.record(stream)
-        for i in range(K):
-            inp, out = sets[i % nsets]
-            launch(qb, op, dtype, inp, out, M, N, stream)
-        stop.record(stream)
+        start, stop = timed_launches(qb, op, dtype, sets, M, N, K, stream, args.graph, dev)
         torch.cuda.synchronize(dev)
     if ws > 1:
         dist.barrier()
@@ -416,7 +494,8 @@ def main():
         "dtype": "f32" if dtype == "f32" else "bf16 in/out, f32 accumulate",
         "data": "synthetic",
         "config": {"workload": args.workload, "op": op, "M": M, "N": N, "input_dtype": dtype,
-                   "rows_per_gpu": M, "l2": f"{nsets} rotating input/output sets "
+                   "rows_per_gpu": M, "launch": "cuda_graph" if args.graph else "stream",
+                   "l2": f"{nsets} rotating input/output sets "
                    f"({nsets * set_bytes / 2**20:.0f} MiB) > 4x L2", "plan": plan},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "traffic": traffic, "peak_source": peak_src,

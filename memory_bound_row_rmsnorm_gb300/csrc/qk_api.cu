@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -40,7 +41,7 @@ constexpr int kRingMaxVectorsPerCta = 4096;  // 256 threads x 16 vectors, or 512
 constexpr int64_t kMaxRowBytes = int64_t(kMaxCluster) * kRingMaxVectorsPerCta * 16;  // 1 MiB
 
 struct DeviceInfo {
-  bool ready = false;
+  std::atomic<bool> ready{false};  // set once, after the fields below
   qk_status error = QK_OK;
   int sms = 0;
   int smem_optin = 0;
@@ -57,6 +58,7 @@ struct Override {
   qk_plan plan{};
 };
 Override g_override[3][2];
+std::atomic<uint64_t> g_override_gen{1};  // bumped by every qk_set_plan_override
 
 KernelTable table_for(int op, int dt) {
   switch (op * 2 + dt) {
@@ -88,10 +90,14 @@ qk_status device_info(int* dev_out, DeviceInfo** info) {
     cudaGetLastError();
     return QK_ERR_NO_DEVICE;
   }
-  std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
-    d.ready = true;
+  if (d.ready.load(std::memory_order_acquire)) {  // fast path: no lock after the first call
+    *dev_out = dev;
+    *info = &d;
+    return d.error;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!d.ready.load(std::memory_order_relaxed)) {
     cudaDeviceProp p;
     if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) {
       cudaGetLastError();
@@ -109,6 +115,7 @@ qk_status device_info(int* dev_out, DeviceInfo** info) {
         d.status = static_cast<int*>(ptr);
       }
     }
+    d.ready.store(true, std::memory_order_release);
   }
   *dev_out = dev;
   *info = &d;
@@ -402,14 +409,31 @@ qk_status run(int op, int dt, RowArgs a, bool fast, void* stream) {
   DeviceInfo* d;
   qk_status st = device_info(&dev, &d);
   if (st != QK_OK) return st;
-  Plan p;
-  st = fast ? plan_ring(dev, *d, op, dt, a.M, a.N, &p) : plan_direct(dev, *d, op, dt, a.M, a.N, &p);
-  if (st != QK_OK) return st;
+  // Per-thread cache of the last plan of each (op, dtype, path): repeated
+  // calls with the same shape skip the table walk and the occupancy queries.
+  struct Cached {
+    int dev = -1;
+    int64_t M = -1, N = -1;
+    uint64_t gen = 0;
+    Plan plan;
+  };
+  thread_local Cached cache[3][2][2];
+  Cached& c = cache[op][dt][fast ? 1 : 0];
+  const uint64_t gen = g_override_gen.load(std::memory_order_acquire);
+  if (!(c.dev == dev && c.M == a.M && c.N == a.N && c.gen == gen)) {
+    Plan np;
+    st = fast ? plan_ring(dev, *d, op, dt, a.M, a.N, &np)
+              : plan_direct(dev, *d, op, dt, a.M, a.N, &np);
+    if (st != QK_OK) return st;
+    c.dev = dev, c.M = a.M, c.N = a.N, c.gen = gen, c.plan = np;
+  }
+  const Plan& p = c.plan;
   a.chunks = p.chunks;
   a.slots = p.slots;
   a.slot_bytes = p.slot_bytes;
   a.num_items = p.num_items;
   a.timeout_ns = kWaitTimeoutNs;
+  a.inv_n = float(1.0 / double(a.N));
   a.status = d->status;
   return launch(p, a, stream);
 }
@@ -566,6 +590,7 @@ qk_status qk_set_plan_override(qk_op op, qk_dtype dtype, const qk_plan* plan) {
   if (op < 0 || op > 2 || (dtype != QK_F32 && dtype != QK_BF16)) return QK_ERR_INVALID_ARG;
   if (plan == nullptr) {
     g_override[op][dtype].on = false;
+    g_override_gen.fetch_add(1, std::memory_order_acq_rel);
     return QK_OK;
   }
   if (plan->cluster < 0 || plan->cluster > kMaxCluster || plan->slots < 0 ||
@@ -577,6 +602,7 @@ qk_status qk_set_plan_override(qk_op op, qk_dtype dtype, const qk_plan* plan) {
     return QK_ERR_UNSUPPORTED;
   g_override[op][dtype].plan = *plan;
   g_override[op][dtype].on = true;
+  g_override_gen.fetch_add(1, std::memory_order_acq_rel);
   return QK_OK;
 }
 

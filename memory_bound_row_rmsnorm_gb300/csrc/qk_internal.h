@@ -20,6 +20,7 @@ struct RowArgs {
   int64_t M;
   int64_t N;
   float eps;
+  float inv_n;          // 1 / N, rounded once on the host (RMSNorm mean)
   int32_t chunks;       // ring slots one row slice spans (streamed rows), else 1
   int32_t slots;        // ring slots per CTA
   uint32_t slot_bytes;  // bytes per ring slot (multiple of 128)

@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     // ---- finish: outputs from registers, each stored once ----
     if (!row_ok) continue;
     if constexpr (OP == kSoftmax) {
-      const float scale = (tm == kNegInf) ? 0.f : exp2_approx((tm - pm) * kLog2e) / ps;
+      const float scale = (tm == kNegInf) ? 0.f : __fdividef(exp2_approx((tm - pm) * kLog2e), ps);
       const float2 sc = make_float2(scale, scale);
       const float mb = (tm == kNegInf) ? 0.f : tm * kLog2e;
       uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         yg[l + k * TPR] = V::pack(o);
       }
     } else if constexpr (OP == kRmsNorm) {
-      const float r = 1.0f / sqrtf(ps / float(N) + a.eps);
+      const float r = rsqrtf(fmaf(ps, a.inv_n, a.eps));  // 1/sqrt(mean of squares + eps)
       const float2 r2 = make_float2(r, r);
       uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
 #pragma unroll
@@ -416,12 +416,15 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       }
       if (l == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = r;
     } else {
-      const float lse = pm + logf(ps);
-      if (l == 0 && rank == 0) {
-        if (a.lse != nullptr) a.lse[row] = lse;
-        if (!(trow >= 0 && trow < N)) a.loss[row] = __int_as_float(0x7fc00000);  // NaN
+      const bool leader = (l == 0 && rank == 0);
+      if (leader || own_t) {  // only the threads that write need the logarithm
+        const float lse = pm + logf(ps);
+        if (leader) {
+          if (a.lse != nullptr) a.lse[row] = lse;
+          if (!(trow >= 0 && trow < N)) a.loss[row] = __int_as_float(0x7fc00000);  // NaN
+        }
+        if (own_t) a.loss[row] = lse - xt;
       }
-      if (own_t) a.loss[row] = lse - xt;
     }
   }
 
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
   }
 
   if constexpr (OP == kSoftmax) {
-    const float scale = (tm == kNegInf) ? 0.f : exp2_approx((tm - pm) * kLog2e) / ps;
+    const float scale = (tm == kNegInf) ? 0.f : __fdividef(exp2_approx((tm - pm) * kLog2e), ps);
     T* yrow = static_cast<T*>(a.y) + row * N + e0;
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
@@ -546,7 +549,7 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
       if (e < ne) V::store1(yrow + e, f[k] * scale);
     }
   } else if constexpr (OP == kRmsNorm) {
-    const float r = 1.0f / sqrtf(ps / float(N) + a.eps);
+    const float r = rsqrtf(fmaf(ps, a.inv_n, a.eps));  // 1/sqrt(mean of squares + eps)
     T* yrow = static_cast<T*>(a.y) + row * N + e0;
     const T* wrow = static_cast<const T*>(a.w) + e0;
 #pragma unroll
