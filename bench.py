@@ -59,10 +59,14 @@ def min_bytes(op: str, dtype: str, M: int, N: int) -> int:
     return M * N * s + 8 * M + 8 * M  # logits + targets in; loss + lse out
 
 
+# The device code of the kernels (the launch plan is compared separately).
+KERNEL_SOURCES = ("qk_device.cuh", "qk_kernels.cuh", "qk_kernel_table.cuh", "qk_internal.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "memory_bound_row_rmsnorm_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
@@ -79,9 +83,9 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, plan: dict):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; otherwise None."""
+    the current kernel sources with the same launch plan; otherwise None."""
     p = os.path.join(ROOT, "profiles", f"{workload}.traffic.json")
     try:
         with open(p) as f:
@@ -89,6 +93,9 @@ def recorded_traffic(workload: str):
     except Exception:
         return None
     if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    keys = ("threads", "row_threads", "vec_per_thread", "cluster", "slots", "chunks")
+    if any(rec.get("plan", {}).get(k) != plan.get(k) for k in keys):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -156,6 +163,23 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def rank_seed(rank: int, i: int) -> int:
+    """Seed of input set i on `rank`: every rank draws its own rows."""
+    return 1000 + 17 * rank + i
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of `value` over all ranks (the job ends with its slowest rank)."""
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tbs(bytes_per_rank_step: int, world: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: all ranks' algorithmic bytes over the slowest rank's time."""
+    return bytes_per_rank_step * world * steps / (ms / 1e3) / 1e12
 
 
 def make_set(op, dtype, M, N, sigma, seed, dev):
@@ -262,9 +286,9 @@ def run_reference(args, op, dtype, M, N, sigma):
 
     K, W = args.steps, args.warmup
     # calibrate rows per step so the whole run stays within ~2 minutes
-    rate, cores, _, _ = cpu_oracle_rate(op, dtype, M, N, sigma, budget_s=1.0)
+    rate, cores, _, _ = cpu_oracle_rate(op, dtype, M, N, sigma, budget_s=min(1.0, args.ref_seconds / 4))
     per_row = min_bytes(op, dtype, 1, N)
-    budget = 120.0 / max(1, K + W)
+    budget = args.ref_seconds / max(1, K + W)
     rows = int(max(1, min(M, rate * 1e12 * budget / per_row)))
     import concurrent.futures as cf
 
@@ -365,6 +389,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", metavar="JSONL", help="time every sweep point instead; write them here")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: total CPU time budget of the timed steps")
     ap.add_argument("--graph", action="store_true",
                     help="issue the timed steps as one CUDA-graph replay (no host launch overhead)")
     args = ap.parse_args()
@@ -398,7 +424,7 @@ def main():
     # rotating input/output sets: > 4x L2 in total
     set_bytes = min_bytes(op, dtype, M, N)
     nsets = max(2, math.ceil(4 * L2_BYTES / set_bytes))
-    sets = [make_set(op, dtype, M, N, sigma, 1000 + 17 * rank + i, dev) for i in range(nsets)]
+    sets = [make_set(op, dtype, M, N, sigma, rank_seed(rank, i), dev) for i in range(nsets)]
     stream = torch.cuda.current_stream(dev)
     code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
     opcode = {"softmax": qb.QK_OP_SOFTMAX, "rmsnorm": qb.QK_OP_RMSNORM, "xent": qb.QK_OP_XENT}[op]
@@ -422,19 +448,17 @@ def main():
         dist.barrier()
     elapsed_ms = start.elapsed_time(stop)
     if ws > 1:
-        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     status = qb.qk_get_device_status(stream)
     if status != qb.QK_OK:
         raise RuntimeError(f"device status: {qb.qk_status_string(status)}")
 
     per_launch_s = elapsed_ms / 1e3 / K
     bytes_per_launch = set_bytes
-    value = bytes_per_launch * ws * K / (elapsed_ms / 1e3) / 1e12
+    value = whole_job_tbs(bytes_per_launch, ws, K, elapsed_ms)
     peak, peak_src = measured_peak()
     achieved_gbs = bytes_per_launch / per_launch_s / 1e9
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload, plan)
 
     # ---- end to end: pinned host buffers, copies inside the timed region ----
     inp0, out0 = sets[0]
@@ -464,10 +488,8 @@ def main():
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
     if ws > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = set_bytes * ws * E / (e2e_ms / 1e3) / 1e12
+        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = whole_job_tbs(set_bytes, ws, E, e2e_ms)
 
     if rank != 0:
         if ws > 1:
