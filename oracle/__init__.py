@@ -60,6 +60,12 @@ def bind(path: str):
     lib.oracle_rmsnorm_fwd.restype = None
     lib.oracle_xent_fwd.argtypes = [dp, lp, dp, dp, i64, i64]
     lib.oracle_xent_fwd.restype = None
+    lib.oracle_softmax_bwd.argtypes = [dp, dp, dp, i64, i64]
+    lib.oracle_softmax_bwd.restype = None
+    lib.oracle_rmsnorm_bwd.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64]
+    lib.oracle_rmsnorm_bwd.restype = None
+    lib.oracle_xent_bwd.argtypes = [dp, lp, dp, dp, dp, i64, i64]
+    lib.oracle_xent_bwd.restype = None
     return lib
 
 
@@ -118,3 +124,41 @@ def xent_fwd(x, target, lib=None):
     lse = np.empty(M, dtype=np.float64)
     lib.oracle_xent_fwd(_ptr(x), _ptr(t, ctypes.c_int64), _ptr(loss), _ptr(lse), M, N)
     return loss, lse
+
+
+def softmax_bwd(y, dy, lib=None) -> np.ndarray:
+    """dx of softmax given its output y and the upstream gradient dy (M x N)."""
+    lib = lib or library()
+    y, dy = _f64(y), _f64(dy)
+    M, N = y.shape
+    if dy.shape != (M, N):
+        raise ValueError("y and dy must have the same shape")
+    dx = np.empty_like(y)
+    lib.oracle_softmax_bwd(_ptr(y), _ptr(dy), _ptr(dx), M, N)
+    return dx
+
+
+def rmsnorm_bwd(x, w, rstd, dy, lib=None):
+    """(dx, dw) of RMSNorm given x, w, the forward rstd and the upstream dy."""
+    lib = lib or library()
+    x, w, rstd, dy = _f64(x), _f64(w), _f64(rstd), _f64(dy)
+    M, N = x.shape
+    if w.shape != (N,) or rstd.shape != (M,) or dy.shape != (M, N):
+        raise ValueError("shapes: x [M, N], w [N], rstd [M], dy [M, N]")
+    dx = np.empty_like(x)
+    dw = np.empty(N, dtype=np.float64)
+    lib.oracle_rmsnorm_bwd(_ptr(x), _ptr(w), _ptr(rstd), _ptr(dy), _ptr(dx), _ptr(dw), M, N)
+    return dx, dw
+
+
+def xent_bwd(x, target, lse, dloss, lib=None) -> np.ndarray:
+    """dlogits of the per-row cross-entropy given the forward lse and dloss [M]."""
+    lib = lib or library()
+    x, lse, dloss = _f64(x), _f64(lse), _f64(dloss)
+    M, N = x.shape
+    t = np.ascontiguousarray(target, dtype=np.int64)
+    if t.shape != (M,) or lse.shape != (M,) or dloss.shape != (M,):
+        raise ValueError("shapes: x [M, N], target/lse/dloss [M]")
+    dx = np.empty_like(x)
+    lib.oracle_xent_bwd(_ptr(x), _ptr(t, ctypes.c_int64), _ptr(lse), _ptr(dloss), _ptr(dx), M, N)
+    return dx

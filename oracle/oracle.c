@@ -19,6 +19,9 @@
  *   RMSNorm   rstd = 1 / sqrt((1/N) sum_j x_j^2 + eps),  y_j = x_j * rstd * w_j
  *   x-entropy lse = m + log sum_j exp(x_j - m),  loss = lse - x_t
  *
+ * and, further down, their gradients (softmax dx; RMSNorm dx and dw;
+ * cross-entropy dlogits), the textbook derivatives of the same definitions.
+ *
  * All inputs arrive already widened to double (exact for fp32 and bf16 data);
  * every operation is done in double with libm's exp, log and sqrt.  Each row
  * is handled on its own, one element at a time, in index order.
@@ -106,5 +109,74 @@ void oracle_xent_fwd(const double *x, const int64_t *target, double *loss,
         int64_t t = target[i];
         loss[i] = (t >= 0 && t < N) ? l - xi[t] : NAN;
         if (lse) lse[i] = l;
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * Backward passes (gradients of the three forward operators above).  The
+ * article benchmarks forward passes only; these are the textbook derivatives
+ * of the same definitions, written out the same plain way.
+ * ------------------------------------------------------------------------ */
+
+/* Softmax backward: given y = softmax(x) and dy = dL/dy, per row
+ *   dx_j = y_j * (dy_j - sum_k dy_k * y_k). */
+void oracle_softmax_bwd(const double *y, const double *dy, double *dx, int64_t M, int64_t N)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        const double *yi = y + i * N, *gi = dy + i * N;
+        double *di = dx + i * N;
+
+        double dot = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            dot += gi[j] * yi[j];
+
+        for (int64_t j = 0; j < N; ++j)
+            di[j] = yi[j] * (gi[j] - dot);
+    }
+}
+
+/* RMSNorm backward: given x, w, r = rstd (as returned by the forward pass) and
+ * dy = dL/dy for y_j = x_j * r * w_j, per row
+ *   dx_j = r * dy_j * w_j - x_j * r^3 * (1/N) sum_k dy_k * w_k * x_k,
+ * and over all rows dw_j = sum_i dy_ij * x_ij * r_i.  (d r / d x_j = -r^3 x_j / N.) */
+void oracle_rmsnorm_bwd(const double *x, const double *w, const double *rstd,
+                        const double *dy, double *dx, double *dw, int64_t M, int64_t N)
+{
+    for (int64_t j = 0; j < N; ++j)
+        dw[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        const double *xi = x + i * N, *gi = dy + i * N;
+        double *di = dx + i * N;
+        double r = rstd[i];
+
+        double dot = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            dot += gi[j] * w[j] * xi[j];
+        double c = r * r * r * dot / (double)N;
+
+        for (int64_t j = 0; j < N; ++j) {
+            di[j] = r * gi[j] * w[j] - xi[j] * c;
+            dw[j] += gi[j] * xi[j] * r;
+        }
+    }
+}
+
+/* Cross-entropy backward: given the logits, the targets, lse (as returned by
+ * the forward pass) and dloss_i = dL/dloss_i, per row
+ *   dx_j = dloss_i * (exp(x_j - lse_i) - [j == t_i]);
+ * a row whose target is outside [0, N) gets NaN gradients (its loss is NaN). */
+void oracle_xent_bwd(const double *x, const int64_t *target, const double *lse,
+                     const double *dloss, double *dx, int64_t M, int64_t N)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        const double *xi = x + i * N;
+        double *di = dx + i * N;
+        int64_t t = target[i];
+        int ok = (t >= 0 && t < N);
+
+        for (int64_t j = 0; j < N; ++j) {
+            double p = exp(xi[j] - lse[i]);
+            di[j] = ok ? dloss[i] * (p - (j == t ? 1.0 : 0.0)) : NAN;
+        }
     }
 }

@@ -288,3 +288,156 @@ def pin_xent_brute_force(lib):
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+# --------------------------------------------------------------------------
+# Backward passes: pinned to finite differences of the (independently pinned)
+# forward definitions, to invariants, closed forms and a 50-digit brute force.
+# --------------------------------------------------------------------------
+def _fd_grad(f, x, h=1e-6):
+    """Central-difference gradient of the scalar function f at x."""
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        idx = it.multi_index
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        g[idx] = (f(xp) - f(xm)) / (2 * h)
+    return g
+
+
+def pin_softmax_bwd_finite_differences(lib):
+    rng = _rng(20)
+    x = rng.normal(size=(3, 7))
+    g = rng.normal(size=(3, 7))
+    dx = oracle.softmax_bwd(oracle.softmax_fwd(x, lib), g, lib)
+    fd = _fd_grad(lambda z: float(np.sum(g * oracle.softmax_fwd(z, lib))), x)
+    assert np.max(np.abs(dx - fd)) <= 1e-7, "softmax bwd: not the derivative of softmax fwd"
+
+
+def pin_softmax_bwd_invariants(lib):
+    rng = _rng(21)
+    y = oracle.softmax_fwd(rng.normal(size=(6, 33)), lib)
+    dx = oracle.softmax_bwd(y, rng.normal(size=(6, 33)), lib)
+    assert np.max(np.abs(dx.sum(axis=1))) <= 1e-14, "softmax bwd: rows must sum to 0"
+    dx0 = oracle.softmax_bwd(y, np.full_like(y, 2.5), lib)
+    assert np.max(np.abs(dx0)) <= 1e-15, "softmax bwd: a constant upstream gradient gives 0"
+
+
+def pin_softmax_bwd_two_columns(lib):
+    p = 0.3
+    y = np.array([[p, 1 - p]])
+    dx = oracle.softmax_bwd(y, np.array([[1.0, 0.0]]), lib)
+    _close(dx, [[p * (1 - p), -p * (1 - p)]], 1e-14, "softmax bwd: N=2 closed form")
+
+
+def pin_softmax_bwd_brute_force(lib):
+    rng = _rng(22)
+    x = rng.normal(size=(4, 8))
+    g = rng.normal(size=(4, 8))
+    y = oracle.softmax_fwd(x, lib)
+    want = []
+    for yr, gr in zip(y, g):
+        yd = [Decimal(float(v)) for v in yr]
+        gd = [Decimal(float(v)) for v in gr]
+        dot = sum((a * b for a, b in zip(yd, gd)), Decimal(0))
+        want.append([float(a * (b - dot)) for a, b in zip(yd, gd)])
+    dx = oracle.softmax_bwd(y, g, lib)
+    assert np.max(np.abs(dx - np.array(want))) <= 1e-15, "softmax bwd: 4x8 brute force"
+
+
+def pin_rmsnorm_bwd_finite_differences(lib):
+    rng = _rng(23)
+    x = rng.normal(size=(3, 6))
+    w = rng.uniform(0.5, 1.5, size=6)
+    g = rng.normal(size=(3, 6))
+    eps = 1e-3
+    _, r = oracle.rmsnorm_fwd(x, w, eps, lib)
+    dx, dw = oracle.rmsnorm_bwd(x, w, r, g, lib)
+    fx = _fd_grad(lambda z: float(np.sum(g * oracle.rmsnorm_fwd(z, w, eps, lib)[0])), x)
+    fw = _fd_grad(lambda v: float(np.sum(g * oracle.rmsnorm_fwd(x, v, eps, lib)[0])), w)
+    assert np.max(np.abs(dx - fx)) <= 1e-7, "rmsnorm bwd: dx is not the derivative of the forward"
+    assert np.max(np.abs(dw - fw)) <= 1e-7, "rmsnorm bwd: dw is not the derivative of the forward"
+
+
+def pin_rmsnorm_bwd_invariants(lib):
+    rng = _rng(24)
+    x = rng.normal(size=(5, 40))
+    w = rng.uniform(0.5, 1.5, size=40)
+    g = rng.normal(size=(5, 40))
+    y, r = oracle.rmsnorm_fwd(x, w, 0.0, lib)
+    dx, dw = oracle.rmsnorm_bwd(x, w, r, g, lib)
+    # eps = 0: y(a x) = y(x), so the gradient is orthogonal to x
+    assert np.max(np.abs(np.sum(x * dx, axis=1))) <= 1e-12, "rmsnorm bwd: x . dx must vanish at eps=0"
+    # dw_j = sum_i dy_ij y_ij / w_j
+    _close(dw, np.sum(g * y, axis=0) / w, 1e-12, "rmsnorm bwd: dw = sum dy*y/w")
+    # a single column at eps = 0 is a constant +-w: no gradient to x
+    dx1, _ = oracle.rmsnorm_bwd(np.array([[1.7], [-0.4]]), np.array([0.9]),
+                                np.array([1 / 1.7, 1 / 0.4]), np.array([[2.0], [3.0]]), lib)
+    assert np.max(np.abs(dx1)) <= 1e-15, "rmsnorm bwd: N=1, eps=0 has zero dx"
+
+
+def pin_rmsnorm_bwd_brute_force(lib):
+    rng = _rng(25)
+    x = rng.normal(size=(4, 8))
+    w = rng.uniform(0.5, 1.5, size=8)
+    g = rng.normal(size=(4, 8))
+    _, r = oracle.rmsnorm_fwd(x, w, 1e-6, lib)
+    want_dx, want_dw = [], [Decimal(0)] * 8
+    for xr, gr, ri in zip(x, g, r):
+        xd = [Decimal(float(v)) for v in xr]
+        gd = [Decimal(float(v)) for v in gr]
+        wd = [Decimal(float(v)) for v in w]
+        rd = Decimal(float(ri))
+        dot = sum((a * b * c for a, b, c in zip(gd, wd, xd)), Decimal(0))
+        c = rd * rd * rd * dot / Decimal(8)
+        want_dx.append([float(rd * a * b - xv * c) for a, b, xv in zip(gd, wd, xd)])
+        want_dw = [acc + a * xv * rd for acc, a, xv in zip(want_dw, gd, xd)]
+    dx, dw = oracle.rmsnorm_bwd(x, w, r, g, lib)
+    _close(dx, want_dx, 1e-12, "rmsnorm bwd: 4x8 brute force dx")
+    _close(dw, [float(v) for v in want_dw], 1e-13, "rmsnorm bwd: 4x8 brute force dw")
+
+
+def pin_xent_bwd_finite_differences(lib):
+    rng = _rng(26)
+    x = rng.normal(0, 2 ** 0.5, size=(3, 7))
+    t = np.array([0, 6, 3])
+    g = rng.uniform(0.5, 2.0, size=3)
+    _, lse = oracle.xent_fwd(x, t, lib)
+    dx = oracle.xent_bwd(x, t, lse, g, lib)
+    fd = _fd_grad(lambda z: float(np.sum(g * oracle.xent_fwd(z, t, lib)[0])), x)
+    assert np.max(np.abs(dx - fd)) <= 1e-7, "xent bwd: not the derivative of the forward loss"
+
+
+def pin_xent_bwd_closed_form_and_invariants(lib):
+    x = np.array([[0.0, math.log(3.0)]])
+    _, lse = oracle.xent_fwd(x, np.array([1]), lib)
+    dx = oracle.xent_bwd(x, np.array([1]), lse, np.array([1.0]), lib)
+    _close(dx, [[0.25, -0.25]], 1e-14, "xent bwd: softmax - onehot closed form")
+    rng = _rng(27)
+    x = rng.normal(size=(5, 19))
+    t = rng.integers(0, 19, size=5)
+    _, lse = oracle.xent_fwd(x, t, lib)
+    dx = oracle.xent_bwd(x, t, lse, rng.uniform(0.1, 3, size=5), lib)
+    assert np.max(np.abs(dx.sum(axis=1))) <= 1e-14, "xent bwd: rows must sum to 0"
+    bad = oracle.xent_bwd(x[:2], np.array([19, -1]), lse[:2], np.ones(2), lib)
+    assert np.isnan(bad).all(), "xent bwd: out-of-range target gives NaN gradients"
+
+
+def pin_xent_bwd_brute_force(lib):
+    rng = _rng(28)
+    x = rng.normal(size=(4, 8))
+    t = rng.integers(0, 8, size=4)
+    g = rng.uniform(0.5, 2.0, size=4)
+    _, lse = oracle.xent_fwd(x, t, lib)
+    want = []
+    for xr, ti, gi in zip(x, t, g):
+        s = sum((_CTX.exp(Decimal(float(v))) for v in xr), Decimal(0))
+        want.append([float(Decimal(float(gi)) * (_CTX.exp(Decimal(float(v))) / s - (1 if j == ti else 0)))
+                     for j, v in enumerate(xr)])
+    dx = oracle.xent_bwd(x, t, lse, g, lib)
+    assert np.max(np.abs(dx - np.array(want))) <= 1e-14, "xent bwd: 4x8 brute force"
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

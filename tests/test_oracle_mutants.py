@@ -33,6 +33,17 @@ MUTANTS = [
     ("xent: target column off by one", "l - xi[t]", "l - xi[t > 0 ? t - 1 : t]"),
     ("xent: log2 instead of ln", "double l = m + log(s);", "double l = m + log2(s);"),
     ("xent: no range check", "(t >= 0 && t < N) ? l - xi[t] : NAN", "(t > -2 && t <= N) ? l - xi[t] : NAN"),
+    ("softmax bwd: sign of the dot", "di[j] = yi[j] * (gi[j] - dot);", "di[j] = yi[j] * (gi[j] + dot);"),
+    ("softmax bwd: y dropped from the dot", "dot += gi[j] * yi[j];", "dot += gi[j];"),
+    ("softmax bwd: y factor dropped", "di[j] = yi[j] * (gi[j] - dot);", "di[j] = (gi[j] - dot);"),
+    ("rmsnorm bwd: r squared for r cubed", "double c = r * r * r * dot / (double)N;", "double c = r * r * dot / (double)N;"),
+    ("rmsnorm bwd: mean divisor dropped", "double c = r * r * r * dot / (double)N;", "double c = r * r * r * dot;"),
+    ("rmsnorm bwd: w dropped from the dot", "dot += gi[j] * w[j] * xi[j];", "dot += gi[j] * xi[j];"),
+    ("rmsnorm bwd: dw without rstd", "dw[j] += gi[j] * xi[j] * r;", "dw[j] += gi[j] * xi[j];"),
+    ("rmsnorm bwd: sign of the correction", "di[j] = r * gi[j] * w[j] - xi[j] * c;", "di[j] = r * gi[j] * w[j] + xi[j] * c;"),
+    ("xent bwd: one-hot added", "dloss[i] * (p - (j == t ? 1.0 : 0.0))", "dloss[i] * (p + (j == t ? 1.0 : 0.0))"),
+    ("xent bwd: lse dropped", "double p = exp(xi[j] - lse[i]);", "double p = exp(xi[j]);"),
+    ("xent bwd: upstream gradient dropped", "dloss[i] * (p - (j == t ? 1.0 : 0.0))", "(p - (j == t ? 1.0 : 0.0))"),
 ]
 
 

@@ -13,4 +13,5 @@ def test_oracle_pin(pin):
 def test_every_operator_is_pinned():
     names = [p.__name__ for p in oracle_pins.ALL_PINS]
     for op in ("softmax", "rmsnorm", "xent"):
-        assert sum(n.startswith(f"pin_{op}_") for n in names) >= 5, op
+        assert sum(n.startswith(f"pin_{op}_") and "_bwd_" not in n for n in names) >= 5, op
+        assert sum(n.startswith(f"pin_{op}_bwd_") for n in names) >= 3, op
