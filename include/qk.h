@@ -55,7 +55,16 @@ extern "C" {
 
 typedef enum { QK_F32 = 0, QK_BF16 = 1 } qk_dtype;
 
-typedef enum { QK_OP_SOFTMAX = 0, QK_OP_RMSNORM = 1, QK_OP_XENT = 2 } qk_op;
+/* Operators, as named by qk_get_plan / qk_set_plan_override / qk_max_row_elements:
+ * the three forward passes and their backward passes. */
+typedef enum {
+  QK_OP_SOFTMAX = 0,
+  QK_OP_RMSNORM = 1,
+  QK_OP_XENT = 2,
+  QK_OP_SOFTMAX_BWD = 3,
+  QK_OP_RMSNORM_BWD = 4,
+  QK_OP_XENT_BWD = 5
+} qk_op;
 
 typedef enum {
   QK_OK = 0,
@@ -114,6 +123,58 @@ QK_API qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rs
  */
 QK_API qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* loss, float* lse,
                       int64_t M, int64_t N, qk_dtype dtype, void* stream);
+
+/*
+ * Backward passes.  The article benchmarks the forward passes only; these are
+ * the derivatives of the same definitions, built on the same read-once ring
+ * kernels (each input element read from HBM once, each output written once).
+ * They take the fast path only: x, y, dy, dx, w and the logits must be 16-byte
+ * aligned and N * sizeof(dtype) a multiple of 16 (QK_ERR_UNSUPPORTED
+ * otherwise), and rows may hold up to half of qk_max_row_elements' forward
+ * limit (softmax, RMSNorm; see qk_max_row_elements(QK_OP_*_BWD, dtype)).
+ */
+
+/*
+ * Softmax backward: dx[i,j] = y[i,j] * (dy[i,j] - sum_k dy[i,k] * y[i,k]).
+ *   y    [M, N] dtype, the forward output; dy [M, N] dtype, the upstream gradient.
+ *   dx   [M, N] dtype, written once; may alias y or dy exactly.
+ */
+QK_API qk_status qk_softmax_bwd(const void* y, const void* dy, void* dx, int64_t M, int64_t N,
+                                qk_dtype dtype, void* stream);
+
+/*
+ * Bytes of device workspace qk_rmsnorm_bwd needs for these sizes on the
+ * current device (fp32 partial column sums of dw, one row per CTA).
+ */
+QK_API qk_status qk_rmsnorm_bwd_workspace_size(int64_t M, int64_t N, qk_dtype dtype,
+                                               size_t* bytes);
+
+/*
+ * RMSNorm backward, for y = x * rstd * w with rstd = 1/sqrt(mean(x^2) + eps):
+ *   dx[i,j] = rstd_i dy[i,j] w_j - x[i,j] rstd_i^3 (1/N) sum_k dy[i,k] w_k x[i,k]
+ *   dw[j]   = sum_i dy[i,j] x[i,j] rstd_i          (overwritten, not accumulated)
+ *   x, dy  [M, N] dtype;  w [N] dtype;  rstd [M] float32 from qk_rmsnorm_fwd.
+ *   dx     [M, N] dtype, written once; may alias x or dy exactly.
+ *   dw     [N] float32.
+ *   workspace  caller-owned device memory of at least
+ *              qk_rmsnorm_bwd_workspace_size() bytes, 16-byte aligned; its
+ *              contents are scratch (no need to clear it).  dw is summed from
+ *              the per-CTA partials in a fixed order, so it is reproducible.
+ */
+QK_API qk_status qk_rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy,
+                                void* dx, float* dw, void* workspace, size_t workspace_bytes,
+                                int64_t M, int64_t N, qk_dtype dtype, void* stream);
+
+/*
+ * Cross-entropy backward: dlogits[i,j] = dloss_i * (exp(logits[i,j] - lse_i) - [j == t_i]).
+ *   logits [M, N] dtype; targets [M] int64; lse [M] float32 from qk_xent_fwd;
+ *   dloss  [M] float32 upstream gradient of each row's loss, or NULL for 1.
+ *   dlogits [M, N] dtype, written once; may alias logits exactly.  A row whose
+ *   target is outside [0, N) gets NaN gradients.
+ */
+QK_API qk_status qk_xent_bwd(const void* logits, const int64_t* targets, const float* lse,
+                             const float* dloss, void* dlogits, int64_t M, int64_t N,
+                             qk_dtype dtype, void* stream);
 
 /* Static English description of a status code; never NULL. */
 QK_API const char* qk_status_string(qk_status s);

@@ -20,6 +20,7 @@ LIBRARY = os.path.join(_HERE, "_lib", "libqk.so")
 
 QK_F32, QK_BF16 = 0, 1
 QK_OP_SOFTMAX, QK_OP_RMSNORM, QK_OP_XENT = 0, 1, 2
+QK_OP_SOFTMAX_BWD, QK_OP_RMSNORM_BWD, QK_OP_XENT_BWD = 3, 4, 5
 QK_OK = 0
 QK_ERR_INVALID_ARG = 1
 QK_ERR_UNSUPPORTED = 2
@@ -31,7 +32,8 @@ QK_ERR_NO_DEVICE = 6
 _EXPORTS = (
     "qk_softmax_fwd", "qk_rmsnorm_fwd", "qk_xent_fwd", "qk_status_string",
     "qk_get_device_status", "qk_max_row_elements", "qk_get_plan",
-    "qk_set_plan_override", "qk_test_wait_timeout",
+    "qk_set_plan_override", "qk_test_wait_timeout", "qk_softmax_bwd", "qk_rmsnorm_bwd",
+    "qk_rmsnorm_bwd_workspace_size", "qk_xent_bwd",
 )
 
 
@@ -78,8 +80,14 @@ def load_library(path: str = LIBRARY):
         lib.qk_get_plan.argtypes = [i32, i32, i64, i64, ctypes.POINTER(qk_plan)]
         lib.qk_set_plan_override.argtypes = [i32, i32, ctypes.POINTER(qk_plan)]
         lib.qk_test_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        lib.qk_softmax_bwd.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+        lib.qk_rmsnorm_bwd_workspace_size.argtypes = [i64, i64, i32, ctypes.POINTER(ctypes.c_size_t)]
+        lib.qk_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i64, i64, i32, vp]
+        lib.qk_xent_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, vp]
         for name in ("qk_softmax_fwd", "qk_rmsnorm_fwd", "qk_xent_fwd", "qk_get_device_status",
-                     "qk_get_plan", "qk_set_plan_override", "qk_test_wait_timeout"):
+                     "qk_get_plan", "qk_set_plan_override", "qk_test_wait_timeout",
+                     "qk_softmax_bwd", "qk_rmsnorm_bwd_workspace_size", "qk_rmsnorm_bwd",
+                     "qk_xent_bwd"):
             getattr(lib, name).restype = i32
         del fp
         _lib = lib
@@ -127,6 +135,30 @@ def qk_rmsnorm_fwd(x, w, y, rstd, M: int, N: int, eps: float, dtype: int, stream
 def qk_xent_fwd(logits, targets, loss, lse, M: int, N: int, dtype: int, stream=None) -> None:
     _check(load_library().qk_xent_fwd(_ptr(logits), _ptr(targets), _ptr(loss), _ptr(lse), M, N,
                                       dtype, _stream(stream)), "qk_xent_fwd")
+
+
+def qk_softmax_bwd(y, dy, dx, M: int, N: int, dtype: int, stream=None) -> None:
+    _check(load_library().qk_softmax_bwd(_ptr(y), _ptr(dy), _ptr(dx), M, N, dtype, _stream(stream)),
+           "qk_softmax_bwd")
+
+
+def qk_rmsnorm_bwd_workspace_size(M: int, N: int, dtype: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().qk_rmsnorm_bwd_workspace_size(M, N, dtype, ctypes.byref(n)),
+           "qk_rmsnorm_bwd_workspace_size")
+    return n.value
+
+
+def qk_rmsnorm_bwd(x, w, rstd, dy, dx, dw, workspace, workspace_bytes: int, M: int, N: int,
+                   dtype: int, stream=None) -> None:
+    _check(load_library().qk_rmsnorm_bwd(_ptr(x), _ptr(w), _ptr(rstd), _ptr(dy), _ptr(dx), _ptr(dw),
+                                         _ptr(workspace), int(workspace_bytes), M, N, dtype,
+                                         _stream(stream)), "qk_rmsnorm_bwd")
+
+
+def qk_xent_bwd(logits, targets, lse, dloss, dlogits, M: int, N: int, dtype: int, stream=None) -> None:
+    _check(load_library().qk_xent_bwd(_ptr(logits), _ptr(targets), _ptr(lse), _ptr(dloss),
+                                      _ptr(dlogits), M, N, dtype, _stream(stream)), "qk_xent_bwd")
 
 
 def qk_status_string(status: int) -> str:
@@ -211,3 +243,35 @@ def xent_fwd(logits, targets, want_lse: bool = True, stream=None):
     lse = torch.empty_like(loss) if want_lse else None
     qk_xent_fwd(logits, targets, loss, lse, M, N, _dtype_code(logits), stream)
     return loss, lse
+
+
+def softmax_bwd(y, dy, out=None, stream=None):
+    """Softmax backward over the last dimension: y * (dy - sum(dy * y))."""
+    import torch
+    M, N = _rows(y)
+    dx = torch.empty_like(y) if out is None else out
+    qk_softmax_bwd(y, dy, dx, M, N, _dtype_code(y), stream)
+    return dx
+
+
+def rmsnorm_bwd(x, w, rstd, dy, stream=None):
+    """RMSNorm backward; returns (dx, dw) with dw in float32.  Allocates the
+    workspace with PyTorch (the library itself allocates nothing)."""
+    import torch
+    M, N = _rows(x)
+    code = _dtype_code(x)
+    ws_bytes = qk_rmsnorm_bwd_workspace_size(M, N, code)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    dx = torch.empty_like(x)
+    dw = torch.empty(N, dtype=torch.float32, device=x.device)
+    qk_rmsnorm_bwd(x, w, rstd, dy, dx, dw, ws, ws_bytes, M, N, code, stream)
+    return dx, dw
+
+
+def xent_bwd(logits, targets, lse, dloss=None, stream=None):
+    """Cross-entropy backward: dloss * (softmax(logits) - onehot(targets))."""
+    import torch
+    M, N = _rows(logits)
+    dx = torch.empty_like(logits)
+    qk_xent_bwd(logits, targets, lse, dloss, dx, M, N, _dtype_code(logits), stream)
+    return dx

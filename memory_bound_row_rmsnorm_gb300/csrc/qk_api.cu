@@ -10,11 +10,13 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <map>
 #include <mutex>
 #include <tuple>
 
 #include "../../include/qk.h"
+#include "qk_bwd_kernels.cuh"
 #include "qk_device.cuh"
 #include "qk_internal.h"
 
@@ -57,8 +59,16 @@ struct Override {
   bool on = false;
   qk_plan plan{};
 };
-Override g_override[3][2];
+constexpr int kNumOps = 6;  // forward: softmax, RMSNorm, x-entropy; then their backward passes
+Override g_override[kNumOps][2];
 std::atomic<uint64_t> g_override_gen{1};  // bumped by every qk_set_plan_override
+
+// Backward operator codes of the ABI (qk_op 3, 4, 5).
+constexpr int kOpSoftmaxBwd = 3, kOpRmsNormBwd = 4, kOpXentBwd = 5;
+bool is_bwd(int op) { return op >= kOpSoftmaxBwd; }
+// Input matrices one work item loads (both y/x and dy for two backward passes).
+int inputs_per_item(int op) { return (op == kOpSoftmaxBwd || op == kOpRmsNormBwd) ? 2 : 1; }
+bool streams_rows(int op) { return op == kXent || op == kOpXentBwd; }
 
 KernelTable table_for(int op, int dt) {
   switch (op * 2 + dt) {
@@ -67,7 +77,13 @@ KernelTable table_for(int op, int dt) {
     case 2: return kernels_rmsnorm_f32();
     case 3: return kernels_rmsnorm_bf16();
     case 4: return kernels_xent_f32();
-    default: return kernels_xent_bf16();
+    case 5: return kernels_xent_bf16();
+    case 6: return bwd_kernels_softmax_f32();
+    case 7: return bwd_kernels_softmax_bf16();
+    case 8: return bwd_kernels_rmsnorm_f32();
+    case 9: return bwd_kernels_rmsnorm_bf16();
+    case 10: return bwd_kernels_xent_f32();
+    default: return bwd_kernels_xent_bf16();
   }
 }
 
@@ -128,7 +144,7 @@ qk_status prepare_kernel(int dev, const DeviceInfo& d, const KernelEntry& k) {
   std::lock_guard<std::mutex> lock(g_mu);
   auto key = std::make_tuple(dev, k.func);
   if (g_attr_done.count(key)) return QK_OK;
-  if (k.path == 1 &&
+  if (k.path != 2 &&  // the ring kernels (forward and backward) take dynamic shared memory
       cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin) !=
           cudaSuccess) {
     cudaGetLastError();
@@ -234,13 +250,41 @@ const Choice kXentTable[] = {
     {2048, 256, 256, 8, 1, 2},   {kStream, 256, 256, 4, 1, 2},  // 16 KB chunks
 };
 
+// Backward passes load two matrices per item (softmax, RMSNorm), so they hold
+// at most 4-8 vectors of each per thread; cross-entropy's backward streams.
+const Choice kSoftmaxBwdTable[] = {
+    {32, 256, 8, 4, 1, 2},     {64, 256, 16, 4, 1, 2},    {128, 256, 32, 4, 1, 2},
+    {256, 256, 64, 4, 1, 2},   {512, 256, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 2},
+    {2048, 256, 256, 8, 1, 1}, {4096, 256, 256, 8, 2, 1}, {8192, 256, 256, 8, 4, 1},
+    {16384, 256, 256, 8, 8, 1}, {32768, 256, 256, 8, 16, 1},
+};
+const Choice kRmsNormBwdTable[] = {
+    {32, 256, 8, 4, 1, 2},     {64, 256, 16, 4, 1, 2},    {128, 256, 32, 4, 1, 2},
+    {256, 256, 64, 4, 1, 2},   {512, 256, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 2},
+    {2048, 256, 256, 4, 2, 2}, {4096, 256, 256, 4, 4, 2}, {8192, 256, 256, 4, 8, 2},
+    {16384, 256, 256, 4, 16, 2}, {32768, 512, 512, 4, 16, 1},
+};
+const Choice kXentBwdTable[] = {
+    {32, 256, 8, 4, 1, 2},     {64, 256, 8, 8, 1, 2},     {128, 256, 16, 8, 1, 2},
+    {256, 256, 32, 8, 1, 2},   {512, 256, 64, 8, 1, 2},   {1024, 256, 128, 8, 1, 2},
+    {2048, 256, 256, 8, 1, 2}, {kStream, 256, 256, 4, 1, 2},
+};
+
 // Chooses the ring kernel (fast path) for a row of NV 16-byte vectors.
 qk_status choose_ring(int op, int64_t NV, int* th, int* tpr, int* vpt, int* cl, int* k,
                       int* slots) {
-  const Choice* t = op == kRmsNorm ? kRmsNormTable : op == kSoftmax ? kSoftmaxTable : kXentTable;
-  const int n = op == kRmsNorm ? int(sizeof(kRmsNormTable) / sizeof(Choice))
-                : op == kSoftmax ? int(sizeof(kSoftmaxTable) / sizeof(Choice))
-                                 : int(sizeof(kXentTable) / sizeof(Choice));
+#define QK_TABLE(T) t = T, n = int(sizeof(T) / sizeof(Choice))
+  const Choice* t;
+  int n;
+  switch (op) {
+    case kSoftmax: QK_TABLE(kSoftmaxTable); break;
+    case kRmsNorm: QK_TABLE(kRmsNormTable); break;
+    case kXent: QK_TABLE(kXentTable); break;
+    case kOpSoftmaxBwd: QK_TABLE(kSoftmaxBwdTable); break;
+    case kOpRmsNormBwd: QK_TABLE(kRmsNormBwdTable); break;
+    default: QK_TABLE(kXentBwdTable); break;
+  }
+#undef QK_TABLE
   for (int i = 0; i < n; ++i) {
     if (NV > t[i].max_nv) continue;
     *th = t[i].threads, *tpr = t[i].row_threads, *vpt = t[i].vec_per_thread;
@@ -267,7 +311,7 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
     if (cl > kMaxCluster || (cl > 1 && tpr != th)) return QK_ERR_UNSUPPORTED;
     if (slice <= per_cta) {
       k = 1;
-    } else if (op == kXent && cl == 1 && tpr == th) {
+    } else if (streams_rows(op) && cl == 1 && tpr == th) {
       k = int((NV + per_cta - 1) / per_cta);
     } else {
       return QK_ERR_UNSUPPORTED;
@@ -276,8 +320,9 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
     qk_status st = choose_ring(op, NV, &th, &tpr, &vpt, &cl, &k, &slots);
     if (st != QK_OK) return st;
   }
-  const KernelEntry* ke = find_kernel(op, dt, 1, th, tpr, vpt, cl > 1);
+  const KernelEntry* ke = find_kernel(op, dt, is_bwd(op) ? 3 : 1, th, tpr, vpt, cl > 1);
   if (ke == nullptr) return QK_ERR_UNSUPPORTED;
+  const int nin = inputs_per_item(op);
 
   int64_t item_bytes;
   if (k > 1) {
@@ -294,8 +339,8 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   const uint32_t slot_bytes = uint32_t((item_bytes + 127) / 128 * 128);
   if (slots <= 0) slots = 2;  // an override without a slot count
   slots = std::min(slots, kMaxSlots);
-  while (slots > 1 && kSmemHeader + int64_t(slots) * slot_bytes > d.smem_optin) --slots;
-  const int64_t smem = kSmemHeader + int64_t(slots) * slot_bytes;
+  while (slots > 1 && kSmemHeader + int64_t(slots) * nin * slot_bytes > d.smem_optin) --slots;
+  const int64_t smem = kSmemHeader + int64_t(slots) * nin * slot_bytes;
   if (smem > d.smem_optin) return QK_ERR_UNSUPPORTED;
 
   qk_status st = prepare_kernel(dev, d, *ke);
@@ -352,11 +397,12 @@ qk_status plan_direct(int dev, const DeviceInfo& d, int op, int dt, int64_t M, i
 }
 
 int64_t max_row_elements(int op, int dt) {
-  if (op == kXent) return INT64_MAX;
+  if (streams_rows(op)) return INT64_MAX;
+  if (is_bwd(op)) return kMaxRowBytes / 2 / elem_size(dt);  // 512 KiB rows (two inputs)
   return kMaxRowBytes / elem_size(dt);
 }
 
-qk_status launch(const Plan& p, const RowArgs& a, void* stream) {
+qk_status launch(const Plan& p, void* args, void* stream) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(unsigned(p.grid), 1, 1);
@@ -376,8 +422,7 @@ qk_status launch(const Plan& p, const RowArgs& a, void* stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  RowArgs args = a;
-  void* params[] = {&args};
+  void* params[] = {args};
   if (cudaLaunchKernelExC(&cfg, p.kernel->func, params) != cudaSuccess) {
     cudaGetLastError();
     return QK_ERR_LAUNCH;
@@ -435,7 +480,72 @@ qk_status run(int op, int dt, RowArgs a, bool fast, void* stream) {
   a.timeout_ns = kWaitTimeoutNs;
   a.inv_n = float(1.0 / double(a.N));
   a.status = d->status;
-  return launch(p, a, stream);
+  return launch(p, &a, stream);
+}
+
+// Rows of fp32 dw partials a backward RMSNorm launch writes (one per CTA, or
+// per cluster), hence its workspace: rows * N * 4 bytes.
+int64_t dw_partial_rows(const Plan& p) { return p.grid / std::max(1, p.cluster); }
+
+qk_status plan_bwd_cached(int op, int dt, int64_t M, int64_t N, int* dev, DeviceInfo** d,
+                          const Plan** out) {
+  qk_status st = device_info(dev, d);
+  if (st != QK_OK) return st;
+  struct Cached {
+    int dev = -1;
+    int64_t M = -1, N = -1;
+    uint64_t gen = 0;
+    Plan plan;
+  };
+  thread_local Cached cache[3][2];
+  Cached& c = cache[op - kOpSoftmaxBwd][dt];
+  const uint64_t gen = g_override_gen.load(std::memory_order_acquire);
+  if (!(c.dev == *dev && c.M == M && c.N == N && c.gen == gen)) {
+    Plan np;
+    st = plan_ring(*dev, **d, op, dt, M, N, &np);
+    if (st != QK_OK) return st;
+    c.dev = *dev, c.M = M, c.N = N, c.gen = gen, c.plan = np;
+  }
+  *out = &c.plan;
+  return QK_OK;
+}
+
+// Backward launch: the ring kernel, then (RMSNorm) the fixed-order dw sum.
+qk_status run_bwd(int op, int dt, BwdArgs a, float* dw, size_t workspace_bytes, void* stream) {
+  int dev;
+  DeviceInfo* d;
+  const Plan* pp;
+  qk_status st = plan_bwd_cached(op, dt, a.M, a.N, &dev, &d, &pp);
+  if (st != QK_OK) return st;
+  const Plan& p = *pp;
+  const int64_t rows = dw_partial_rows(p);
+  if (op == kOpRmsNormBwd && workspace_bytes < size_t(rows) * size_t(a.N) * 4)
+    return QK_ERR_INVALID_ARG;
+  a.chunks = p.chunks;
+  a.slots = p.slots;
+  a.slot_bytes = p.slot_bytes;
+  a.num_items = p.num_items;
+  a.timeout_ns = kWaitTimeoutNs;
+  a.inv_n = float(1.0 / double(a.N));
+  a.status = d->status;
+  st = launch(p, &a, stream);
+  if (st != QK_OK || op != kOpRmsNormBwd) return st;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(unsigned((a.N + 31) / 32), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* part = a.dw_partial;
+  int64_t n = a.N;
+  if (cudaLaunchKernelEx(&cfg, dw_reduce_kernel<0>, part, dw, rows, n) != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_LAUNCH;
+  }
+  return QK_OK;
 }
 
 }  // namespace
@@ -459,7 +569,7 @@ const char* qk_status_string(qk_status s) {
 }
 
 int64_t qk_max_row_elements(qk_op op, qk_dtype dtype) {
-  if (op < 0 || op > 2 || (dtype != QK_F32 && dtype != QK_BF16)) return 0;
+  if (op < 0 || op >= kNumOps || (dtype != QK_F32 && dtype != QK_BF16)) return 0;
   return max_row_elements(op, dtype);
 }
 
@@ -536,6 +646,113 @@ qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* loss, f
   return run(kXent, dtype, a, fast, stream);
 }
 
+// Fast-path requirements of the backward passes: 16-byte aligned rows.
+static bool bwd_aligned(int dt, int64_t N, std::initializer_list<const void*> ptrs) {
+  if ((N * int64_t(elem_size(dt))) % 16 != 0) return false;
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return false;
+  return true;
+}
+
+qk_status qk_softmax_bwd(const void* y, const void* dy, void* dx, int64_t M, int64_t N,
+                         qk_dtype dtype, void* stream) {
+  qk_status st = check_sizes(kOpSoftmaxBwd, dtype, M, N);
+  if (st != QK_OK) return st;
+  if (M == 0) return QK_OK;
+  if (y == nullptr || dy == nullptr || dx == nullptr) return QK_ERR_INVALID_ARG;
+  const size_t es = size_t(elem_size(dtype));
+  if (!aligned_to(y, es) || !aligned_to(dy, es) || !aligned_to(dx, es)) return QK_ERR_MISALIGNED;
+  const int64_t bytes = M * N * int64_t(es);
+  if ((dx != y && overlap(dx, bytes, y, bytes)) || (dx != dy && overlap(dx, bytes, dy, bytes)))
+    return QK_ERR_INVALID_ARG;
+  if (!bwd_aligned(dtype, N, {y, dy, dx})) return QK_ERR_UNSUPPORTED;
+  BwdArgs a = {};
+  a.in0 = y;
+  a.in1 = dy;
+  a.out = dx;
+  a.M = M;
+  a.N = N;
+  return run_bwd(kOpSoftmaxBwd, dtype, a, nullptr, 0, stream);
+}
+
+qk_status qk_rmsnorm_bwd_workspace_size(int64_t M, int64_t N, qk_dtype dtype, size_t* bytes) {
+  if (bytes == nullptr) return QK_ERR_INVALID_ARG;
+  *bytes = 0;
+  qk_status st = check_sizes(kOpRmsNormBwd, dtype, M, N);
+  if (st != QK_OK || M == 0) return st;
+  int dev;
+  DeviceInfo* d;
+  const Plan* p;
+  st = plan_bwd_cached(kOpRmsNormBwd, dtype, M, N, &dev, &d, &p);
+  if (st != QK_OK) return st;
+  *bytes = size_t(dw_partial_rows(*p)) * size_t(N) * 4;
+  return QK_OK;
+}
+
+qk_status qk_rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
+                         float* dw, void* workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                         qk_dtype dtype, void* stream) {
+  qk_status st = check_sizes(kOpRmsNormBwd, dtype, M, N);
+  if (st != QK_OK) return st;
+  if (M == 0) return QK_OK;
+  if (x == nullptr || w == nullptr || rstd == nullptr || dy == nullptr || dx == nullptr ||
+      dw == nullptr || workspace == nullptr)
+    return QK_ERR_INVALID_ARG;
+  const size_t es = size_t(elem_size(dtype));
+  if (!aligned_to(x, es) || !aligned_to(w, es) || !aligned_to(dy, es) || !aligned_to(dx, es) ||
+      !aligned_to(rstd, 4) || !aligned_to(dw, 4) || !aligned_to(workspace, 16))
+    return QK_ERR_MISALIGNED;
+  const int64_t bytes = M * N * int64_t(es), wb = N * int64_t(es);
+  const int64_t wsb = int64_t(std::min<size_t>(workspace_bytes, size_t(INT64_MAX)));
+  if ((dx != x && overlap(dx, bytes, x, bytes)) || (dx != dy && overlap(dx, bytes, dy, bytes)) ||
+      overlap(dx, bytes, w, wb) || overlap(dx, bytes, rstd, M * 4) || overlap(dw, N * 4, x, bytes) ||
+      overlap(dw, N * 4, dy, bytes) || overlap(dw, N * 4, dx, bytes) || overlap(dw, N * 4, w, wb) ||
+      overlap(dw, N * 4, rstd, M * 4) || overlap(workspace, wsb, x, bytes) ||
+      overlap(workspace, wsb, dy, bytes) || overlap(workspace, wsb, dx, bytes) ||
+      overlap(workspace, wsb, dw, N * 4))
+    return QK_ERR_INVALID_ARG;
+  if (!bwd_aligned(dtype, N, {x, w, dy, dx})) return QK_ERR_UNSUPPORTED;
+  BwdArgs a = {};
+  a.in0 = x;
+  a.in1 = dy;
+  a.w = w;
+  a.rstd = rstd;
+  a.out = dx;
+  a.dw_partial = static_cast<float*>(workspace);
+  a.M = M;
+  a.N = N;
+  return run_bwd(kOpRmsNormBwd, dtype, a, dw, workspace_bytes, stream);
+}
+
+qk_status qk_xent_bwd(const void* logits, const int64_t* targets, const float* lse,
+                      const float* dloss, void* dlogits, int64_t M, int64_t N, qk_dtype dtype,
+                      void* stream) {
+  qk_status st = check_sizes(kOpXentBwd, dtype, M, N);
+  if (st != QK_OK) return st;
+  if (M == 0) return QK_OK;
+  if (logits == nullptr || targets == nullptr || lse == nullptr || dlogits == nullptr)
+    return QK_ERR_INVALID_ARG;
+  const size_t es = size_t(elem_size(dtype));
+  if (!aligned_to(logits, es) || !aligned_to(dlogits, es) || !aligned_to(targets, 8) ||
+      !aligned_to(lse, 4) || !aligned_to(dloss, 4))
+    return QK_ERR_MISALIGNED;
+  const int64_t bytes = M * N * int64_t(es);
+  if ((dlogits != logits && overlap(dlogits, bytes, logits, bytes)) ||
+      overlap(dlogits, bytes, targets, M * 8) || overlap(dlogits, bytes, lse, M * 4) ||
+      overlap(dlogits, bytes, dloss, M * 4))
+    return QK_ERR_INVALID_ARG;
+  if (!bwd_aligned(dtype, N, {logits, dlogits})) return QK_ERR_UNSUPPORTED;
+  BwdArgs a = {};
+  a.in0 = logits;
+  a.target = targets;
+  a.lse = lse;
+  a.dloss = dloss;
+  a.out = dlogits;
+  a.M = M;
+  a.N = N;
+  return run_bwd(kOpXentBwd, dtype, a, nullptr, 0, stream);
+}
+
 qk_status qk_get_device_status(void* stream) {
   int dev;
   DeviceInfo* d;
@@ -561,14 +778,14 @@ qk_status qk_get_device_status(void* stream) {
 }
 
 qk_status qk_get_plan(qk_op op, qk_dtype dtype, int64_t M, int64_t N, qk_plan* plan) {
-  if (plan == nullptr || op < 0 || op > 2) return QK_ERR_INVALID_ARG;
+  if (plan == nullptr || op < 0 || op >= kNumOps) return QK_ERR_INVALID_ARG;
   qk_status st = check_sizes(op, dtype, M, N);
   if (st != QK_OK) return st;
   int dev;
   DeviceInfo* d;
   st = device_info(&dev, &d);
   if (st != QK_OK) return st;
-  const bool fast = (N * int64_t(elem_size(dtype))) % 16 == 0;
+  const bool fast = (N * int64_t(elem_size(dtype))) % 16 == 0 || is_bwd(op);
   Plan p;
   st = fast ? plan_ring(dev, *d, op, dtype, std::max<int64_t>(M, 1), N, &p)
             : plan_direct(dev, *d, op, dtype, std::max<int64_t>(M, 1), N, &p);
@@ -587,7 +804,7 @@ qk_status qk_get_plan(qk_op op, qk_dtype dtype, int64_t M, int64_t N, qk_plan* p
 }
 
 qk_status qk_set_plan_override(qk_op op, qk_dtype dtype, const qk_plan* plan) {
-  if (op < 0 || op > 2 || (dtype != QK_F32 && dtype != QK_BF16)) return QK_ERR_INVALID_ARG;
+  if (op < 0 || op >= kNumOps || (dtype != QK_F32 && dtype != QK_BF16)) return QK_ERR_INVALID_ARG;
   if (plan == nullptr) {
     g_override[op][dtype].on = false;
     g_override_gen.fetch_add(1, std::memory_order_acq_rel);
@@ -597,8 +814,8 @@ qk_status qk_set_plan_override(qk_op op, qk_dtype dtype, const qk_plan* plan) {
       plan->slots > kMaxSlots)
     return QK_ERR_INVALID_ARG;
   const bool clustered = plan->cluster > 1;
-  if (find_kernel(op, dtype, 1, plan->threads, plan->row_threads, plan->vec_per_thread,
-                  clustered) == nullptr)
+  if (find_kernel(op, dtype, is_bwd(op) ? 3 : 1, plan->threads, plan->row_threads,
+                  plan->vec_per_thread, clustered) == nullptr)
     return QK_ERR_UNSUPPORTED;
   g_override[op][dtype].plan = *plan;
   g_override[op][dtype].on = true;

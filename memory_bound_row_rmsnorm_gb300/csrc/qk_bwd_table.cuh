@@ -1,0 +1,26 @@
+// qk_bwd_table.cuh -- compiled configurations of one backward (op, dtype).
+// Include with QK_BOP (a BwdOp) and QK_T defined.
+#pragma once
+
+#include "qk_bwd_kernels.cuh"
+
+#define QK_BWD(TH, TPR, VPT, CL) \
+  {3, TH, TPR, VPT, CL, reinterpret_cast<const void*>(&bwd_kernel<QK_BOP, QK_T, TH, TPR, VPT, CL>)}
+
+namespace qk {
+namespace {
+const KernelEntry kBwdTable[] = {
+    QK_BWD(256, 8, 4, false),   QK_BWD(256, 16, 4, false),  QK_BWD(256, 32, 4, false),
+    QK_BWD(256, 64, 4, false),  QK_BWD(256, 128, 4, false), QK_BWD(256, 256, 4, false),
+    QK_BWD(128, 128, 4, false),
+#if QK_BOP == 12  // cross-entropy: wider per-thread rows, streamed long rows
+    QK_BWD(256, 8, 8, false),   QK_BWD(256, 16, 8, false),  QK_BWD(256, 32, 8, false),
+    QK_BWD(256, 64, 8, false),  QK_BWD(256, 128, 8, false), QK_BWD(256, 256, 8, false),
+#elif QK_BOP == 10  // softmax: 8 vectors a thread, clusters for long rows
+    QK_BWD(256, 256, 8, false), QK_BWD(256, 256, 8, true),
+#else  // RMSNorm: 4 vectors a thread (x, dy, w and the dw partials live in registers)
+    QK_BWD(256, 256, 4, true),  QK_BWD(512, 512, 4, true),
+#endif
+};
+}  // namespace
+}  // namespace qk

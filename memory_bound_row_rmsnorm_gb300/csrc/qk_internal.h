@@ -36,7 +36,8 @@ constexpr int kMaxSlots = 32;
 constexpr int kMaxCluster = 16;
 
 // One compiled kernel.  `path` 1: TMA ring kernel (threads, row_threads,
-// vec_per_thread); path 2: masked direct kernel (threads, elems_per_thread).
+// vec_per_thread); path 2: masked direct kernel (threads, elems_per_thread);
+// path 3: backward ring kernel (as path 1).
 struct KernelEntry {
   int path;
   int threads;
@@ -58,5 +59,11 @@ KernelTable kernels_rmsnorm_f32();
 KernelTable kernels_rmsnorm_bf16();
 KernelTable kernels_xent_f32();
 KernelTable kernels_xent_bf16();
+KernelTable bwd_kernels_softmax_f32();
+KernelTable bwd_kernels_softmax_bf16();
+KernelTable bwd_kernels_rmsnorm_f32();
+KernelTable bwd_kernels_rmsnorm_bf16();
+KernelTable bwd_kernels_xent_f32();
+KernelTable bwd_kernels_xent_bf16();
 
 }  // namespace qk

@@ -79,3 +79,23 @@ def check_scalars(got, ref, what: str, denom=None) -> None:
 
 def loss_denominator(loss_ref, lse_ref):
     return np.maximum(np.abs(loss_ref), 1e-3 * np.abs(lse_ref))
+
+
+def check_scaled(got, ref, scale, dtype: str, what: str, rel: float = REL_F32) -> None:
+    """Outputs that can cancel (gradients): |got - ref| <= rel * scale, where
+    `scale` is the fp64 magnitude of the terms that form each element (so fp32
+    rounding of the terms is what is bounded), plus one bf16 ulp of the value
+    for bf16 outputs (the final rounding).  NaN must match NaN."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = np.broadcast_to(np.asarray(scale, dtype=np.float64), ref.shape)
+    ok_mask = _nan_agree(got, ref, what)
+    g, r, sc = got[ok_mask], ref[ok_mask], scale[ok_mask]
+    bound = rel * sc + (bf16_ulp(r) if dtype == "bf16" else 0.0)
+    err = np.abs(g - r)
+    good = err <= bound
+    if not good.all():
+        idx = np.flatnonzero(~good)
+        i = idx[np.argmax(err[idx] / np.maximum(bound[idx], 1e-300))]
+        raise AssertionError(f"{what}: {idx.size} of {good.size} outside tolerance; worst got {g[i]!r} "
+                             f"want {r[i]!r} (|err| {err[i]:.3e}, bound {bound[i]:.3e})")

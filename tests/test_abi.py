@@ -50,6 +50,9 @@ def test_max_row_elements(lib):
     assert qb.qk_max_row_elements(qb.QK_OP_RMSNORM, qb.QK_BF16) == 524288
     assert qb.qk_max_row_elements(qb.QK_OP_XENT, qb.QK_BF16) == 2 ** 63 - 1
     assert qb.qk_max_row_elements(7, qb.QK_F32) == 0
+    assert qb.qk_max_row_elements(qb.QK_OP_SOFTMAX_BWD, qb.QK_F32) == 131072
+    assert qb.qk_max_row_elements(qb.QK_OP_RMSNORM_BWD, qb.QK_BF16) == 262144
+    assert qb.qk_max_row_elements(qb.QK_OP_XENT_BWD, qb.QK_F32) == 2 ** 63 - 1
 
 
 # Fake, never-dereferenced device addresses: every call below must be refused
@@ -115,7 +118,7 @@ def test_plan_override_validation(lib):
     ok = qb.qk_plan(threads=256, row_threads=256, vec_per_thread=4, cluster=1)
     assert lib.qk_set_plan_override(qb.QK_OP_SOFTMAX, qb.QK_F32, ctypes.byref(ok)) == qb.QK_OK
     assert lib.qk_set_plan_override(qb.QK_OP_SOFTMAX, qb.QK_F32, None) == qb.QK_OK
-    assert lib.qk_set_plan_override(5, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_set_plan_override(6, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
 
 
 def test_timeout_hook_argument_checks(lib):
@@ -127,3 +130,33 @@ def test_binding_raises_on_error(lib):
     with pytest.raises(qb.QkError) as e:
         qb.qk_softmax_fwd(A, A + 16, 4, 4, qb.QK_F32, 0)
     assert e.value.status == qb.QK_ERR_INVALID_ARG
+
+
+def test_backward_argument_checks(lib):
+    F, B = qb.QK_F32, qb.QK_BF16
+    # softmax backward: nulls, element alignment, partial overlap, 16-byte fast-path requirement
+    assert lib.qk_softmax_bwd(None, A, A + 8192, 4, 4, F, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_softmax_bwd(A + 2, A + 4096, A + 8192, 4, 4, F, None) == qb.QK_ERR_MISALIGNED
+    assert lib.qk_softmax_bwd(A, A + 4096, A + 16, 4, 4, F, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_softmax_bwd(A, A + 4096, A + 8192, 4, 3, F, None) == qb.QK_ERR_UNSUPPORTED
+    assert lib.qk_softmax_bwd(A + 4, A + 4096, A + 8192, 4, 4, F, None) == qb.QK_ERR_UNSUPPORTED
+    assert lib.qk_softmax_bwd(A, A + 4096, A + 8192, 4, 131076, F, None) == qb.QK_ERR_UNSUPPORTED
+    assert lib.qk_softmax_bwd(None, None, None, 0, 4, F, None) == qb.QK_OK
+    # RMSNorm backward: workspace is required; dw must not overlap an input
+    args = [A, A + 4096, A + 8192, A + 12288, A + 16384, A + 20480, A + 24576, 1 << 20]
+    assert lib.qk_rmsnorm_bwd(*args[:6], None, 0, 4, 8, B, None) == qb.QK_ERR_INVALID_ARG
+    bad = list(args)
+    bad[5] = A + 16  # dw inside x
+    assert lib.qk_rmsnorm_bwd(*bad, 4, 8, B, None) == qb.QK_ERR_INVALID_ARG
+    bad = list(args)
+    bad[6] = A + 24576 + 4  # workspace not 16-byte aligned
+    assert lib.qk_rmsnorm_bwd(*bad, 4, 8, B, None) == qb.QK_ERR_MISALIGNED
+    assert lib.qk_rmsnorm_bwd(*args, 4, 7, B, None) == qb.QK_ERR_UNSUPPORTED
+    n = ctypes.c_size_t(123)
+    assert lib.qk_rmsnorm_bwd_workspace_size(-1, 8, B, ctypes.byref(n)) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_rmsnorm_bwd_workspace_size(0, 8, B, ctypes.byref(n)) == qb.QK_OK and n.value == 0
+    assert lib.qk_rmsnorm_bwd_workspace_size(4, 8, B, None) == qb.QK_ERR_INVALID_ARG
+    # cross-entropy backward: lse is required; dlogits must not overlap the targets
+    assert lib.qk_xent_bwd(A, A + 4096, None, None, A + 8192, 4, 8, F, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_xent_bwd(A, A + 4096, A + 4608, None, A + 4096, 4, 8, F, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_xent_bwd(A, A + 4096, A + 4608, None, A + 8192, 4, 6, F, None) == qb.QK_ERR_UNSUPPORTED

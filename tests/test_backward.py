@@ -1,0 +1,197 @@
+"""Backward passes through the C ABI against the fp64 oracle.
+
+Inputs: the forward quantities the backward passes consume (softmax y, RMSNorm
+rstd, cross-entropy lse) come from the oracle's forward pass on seeded inputs,
+rounded to the working dtype; the same bytes go to both sides.  Gradients can
+cancel, so each element is checked against 1e-5 of the magnitude of the terms
+that form it (plus one bf16 ulp for bf16 outputs): see parity.check_scaled."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_row_rmsnorm_gb300 import binding as qb
+from memory_bound_row_rmsnorm_gb300 import synthetic as syn
+from parity import check_scaled, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+DT = {"f32": qb.QK_F32, "bf16": qb.QK_BF16}
+OPC = {"softmax": qb.QK_OP_SOFTMAX_BWD, "rmsnorm": qb.QK_OP_RMSNORM_BWD, "xent": qb.QK_OP_XENT_BWD}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for the gpu tests")
+    from memory_bound_row_rmsnorm_gb300 import build
+    build.build()
+    qb.load_library()
+    torch.cuda.set_device(0)
+    yield
+    for op in OPC.values():
+        for dt in DT.values():
+            qb.qk_set_plan_override(op, dt, None)
+
+
+def to_dtype(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(syn.DTYPES[dtype])
+
+
+def make_case(op, dtype, M, N, seed):
+    """Host tensors of one backward call (already rounded to dtype) and their fp64 copies."""
+    if op == "softmax":
+        x = syn.normal_rows(M, N, dtype, seed, "cpu")
+        y = to_dtype(oracle.softmax_fwd(to_f64(x)), dtype)
+        dy = syn.normal_rows(M, N, dtype, seed + 1, "cpu")
+        return {"y": y, "dy": dy}
+    if op == "rmsnorm":
+        x = syn.normal_rows(M, N, dtype, seed, "cpu")
+        w = syn.uniform_weight(N, dtype, seed + 1, "cpu")
+        _, r = oracle.rmsnorm_fwd(to_f64(x), to_f64(w), 1e-6)
+        dy = syn.normal_rows(M, N, dtype, seed + 2, "cpu")
+        return {"x": x, "w": w, "rstd": torch.from_numpy(r).float(), "dy": dy}
+    x = syn.normal_rows(M, N, dtype, seed, "cpu", sigma=2 ** 0.5)
+    t = syn.uniform_targets(M, N, seed + 1, "cpu")
+    _, lse = oracle.xent_fwd(to_f64(x), t.numpy())
+    g = syn.uniform_weight(M, "f32", seed + 2, "cpu", lo=0.25, hi=2.0)
+    return {"x": x, "targets": t, "lse": torch.from_numpy(lse).float(), "dloss": g}
+
+
+def run_gpu(op, dtype, case, inplace=False):
+    d = {k: v.to(DEV) for k, v in case.items()}
+    M, N = (d["y"] if op == "softmax" else d["x"]).shape
+    code = DT[dtype]
+    if op == "softmax":
+        dx = d["dy"] if inplace else torch.full_like(d["y"], float("nan"))
+        qb.qk_softmax_bwd(d["y"], d["dy"], dx, M, N, code)
+        out = {"dx": dx}
+    elif op == "rmsnorm":
+        dx = d["dy"] if inplace else torch.full_like(d["x"], float("nan"))
+        dw = torch.full((N,), float("nan"), dtype=torch.float32, device=DEV)
+        nbytes = qb.qk_rmsnorm_bwd_workspace_size(M, N, code)
+        ws = torch.full((max(nbytes, 16) // 4,), float("nan"), dtype=torch.float32, device=DEV)
+        qb.qk_rmsnorm_bwd(d["x"], d["w"], d["rstd"], d["dy"], dx, dw, ws, nbytes, M, N, code)
+        out = {"dx": dx, "dw": dw}
+    else:
+        dx = d["x"] if inplace else torch.full_like(d["x"], float("nan"))
+        qb.qk_xent_bwd(d["x"], d["targets"], d["lse"], d["dloss"], dx, M, N, code)
+        out = {"dx": dx}
+    torch.cuda.synchronize()
+    assert qb.qk_get_device_status() == qb.QK_OK
+    return out
+
+
+def check(op, dtype, case, out, what):
+    if op == "softmax":
+        y, dy = to_f64(case["y"]), to_f64(case["dy"])
+        ref = oracle.softmax_bwd(y, dy)
+        scale = y * (np.abs(dy) + np.sum(np.abs(dy * y), axis=1, keepdims=True))
+        check_scaled(to_f64(out["dx"]), ref, scale, dtype, f"softmax bwd {what}")
+    elif op == "rmsnorm":
+        x, w, r, dy = to_f64(case["x"]), to_f64(case["w"]), to_f64(case["rstd"]), to_f64(case["dy"])
+        ref_dx, ref_dw = oracle.rmsnorm_bwd(x, w, r, dy)
+        N = x.shape[1]
+        r2 = r[:, None]
+        scale = r2 * np.abs(dy) * w + np.abs(x) * r2 ** 3 * np.sum(np.abs(dy * w * x), axis=1, keepdims=True) / N
+        check_scaled(to_f64(out["dx"]), ref_dx, scale, dtype, f"rmsnorm bwd dx {what}")
+        check_scaled(to_f64(out["dw"]), ref_dw, np.sum(np.abs(dy * x) * r2, axis=0), "f32",
+                     f"rmsnorm bwd dw {what}")
+    else:
+        x, t = to_f64(case["x"]), case["targets"].numpy()
+        lse, g = to_f64(case["lse"]), to_f64(case["dloss"])
+        ref = oracle.xent_bwd(x, t, lse, g)
+        onehot = np.zeros_like(x)
+        ok = (t >= 0) & (t < x.shape[1])
+        onehot[np.arange(x.shape[0])[ok], t[ok]] = 1.0
+        scale = np.abs(g)[:, None] * (np.exp(x - lse[:, None]) + onehot)
+        check_scaled(to_f64(out["dx"]), ref, scale, dtype, f"xent bwd {what}")
+
+
+def rows_for(N):
+    return max(3, min(37, (1 << 21) // N))
+
+
+@pytest.mark.parametrize("N", [8, 64, 256, 1000, 1024, 4096, 8192, 16384, 65536, 131072])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "xent"])
+def test_backward_shapes(op, dtype, N):
+    M = rows_for(N)
+    case = make_case(op, dtype, M, N, seed=5000 + N)
+    check(op, dtype, case, run_gpu(op, dtype, case), f"{dtype} {M}x{N}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "xent"])
+def test_backward_in_place(op, dtype):
+    case = make_case(op, dtype, 19, 4096, seed=6000)
+    check(op, dtype, case, run_gpu(op, dtype, case, inplace=True), "in place")
+
+
+BWD_PLANS = [
+    dict(threads=256, row_threads=8, vec_per_thread=4, cluster=1, slots=2, grid=3),
+    dict(threads=256, row_threads=32, vec_per_thread=4, cluster=1, slots=1, grid=2),
+    dict(threads=128, row_threads=128, vec_per_thread=4, cluster=1, slots=3, grid=5),
+    dict(threads=256, row_threads=256, vec_per_thread=4, cluster=1, slots=2, grid=4),
+]
+CLUSTER_PLANS = {
+    "softmax": dict(threads=256, row_threads=256, vec_per_thread=8, cluster=4, slots=1, grid=8),
+    "rmsnorm": dict(threads=256, row_threads=256, vec_per_thread=4, cluster=8, slots=2, grid=16),
+}
+
+
+@pytest.mark.parametrize("pi", range(len(BWD_PLANS) + 1))
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "xent"])
+def test_backward_forced_plans(op, dtype, pi):
+    if pi == len(BWD_PLANS):
+        if op not in CLUSTER_PLANS:
+            pytest.skip("cross-entropy backward streams rows instead of splitting them")
+        plan = CLUSTER_PLANS[op]
+    else:
+        plan = BWD_PLANS[pi]
+    E = 4 if dtype == "f32" else 8
+    cap = plan["row_threads"] * plan["vec_per_thread"] * E * plan["cluster"]
+    N = max(E, cap - 3 * E)
+    if op == "xent" and plan["row_threads"] == plan["threads"]:
+        N = 5 * cap + 7 * E  # several chunks per row
+    rows_per_step = plan["threads"] // plan["row_threads"]
+    M = max(61, 3 * rows_per_step * plan["grid"] + 5) if N <= 8192 else 9
+    qb.qk_set_plan_override(OPC[op], DT[dtype], plan)
+    try:
+        got = qb.qk_get_plan(OPC[op], DT[dtype], M, N)
+        assert got["grid"] == plan["grid"] and got["cluster"] == plan["cluster"]
+        case = make_case(op, dtype, M, N, seed=7000 + N)
+        check(op, dtype, case, run_gpu(op, dtype, case), f"plan {plan}")
+    finally:
+        qb.qk_set_plan_override(OPC[op], DT[dtype], None)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_xent_backward_bad_targets_and_default_dloss(dtype):
+    case = make_case("xent", dtype, 6, 1024, seed=8000)
+    case["targets"] = torch.tensor([-1, 1024, 0, 1023, 2 ** 40, 5], dtype=torch.int64)
+    d = {k: v.to(DEV) for k, v in case.items()}
+    dx = torch.empty_like(d["x"])
+    qb.qk_xent_bwd(d["x"], d["targets"], d["lse"], None, dx, 6, 1024, DT[dtype])  # dloss = 1
+    torch.cuda.synchronize()
+    case["dloss"] = torch.ones(6)
+    check("xent", dtype, case, {"dx": dx}, "bad targets, dloss = 1")
+    assert torch.isnan(dx[[0, 1, 4]]).all() and torch.isfinite(dx[[2, 3, 5]]).all()
+
+
+def test_rmsnorm_backward_is_deterministic():
+    case = make_case("rmsnorm", "bf16", 4096, 4096, seed=9000)
+    a = run_gpu("rmsnorm", "bf16", case)
+    b = run_gpu("rmsnorm", "bf16", case)
+    assert torch.equal(a["dw"], b["dw"]) and torch.equal(a["dx"], b["dx"])
+    check("rmsnorm", "bf16", case, a, "4096x4096")
+
+
+@pytest.mark.parametrize("op,dtype,M,N", [("rmsnorm", "bf16", 16384, 4096), ("softmax", "f32", 1024, 4096),
+                                          ("xent", "bf16", 1024, 131072)])
+def test_backward_benchmark_shapes(op, dtype, M, N):
+    """The forward workloads' shapes, checked on every row (oracle in a few seconds)."""
+    case = make_case(op, dtype, M, N, seed=9100)
+    check(op, dtype, case, run_gpu(op, dtype, case), f"{dtype} {M}x{N}")
