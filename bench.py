@@ -47,6 +47,7 @@ METRIC = "effective HBM TB/s and % of GB300 peak per kernel over the M×N sweep"
 ESIZE = {"f32": 4, "bf16": 2}
 DEFAULT_WORKLOAD = "rmsnorm_bf16_16384x4096"
 EPS = 1e-6
+OP_CODES = {"softmax": 0, "rmsnorm": 1, "xent": 2, "softmax_bwd": 3, "rmsnorm_bwd": 4, "xent_bwd": 5}
 
 
 def min_bytes(op: str, dtype: str, M: int, N: int) -> int:
@@ -56,7 +57,15 @@ def min_bytes(op: str, dtype: str, M: int, N: int) -> int:
         return 2 * M * N * s
     if op == "rmsnorm":
         return 2 * M * N * s + N * s + 4 * M
-    return M * N * s + 8 * M + 8 * M  # logits + targets in; loss + lse out
+    if op == "xent":
+        return M * N * s + 8 * M + 8 * M  # logits + targets in; loss + lse out
+    if op == "softmax_bwd":
+        return 3 * M * N * s  # y, dy in; dx out
+    if op == "rmsnorm_bwd":
+        return 3 * M * N * s + N * s + 4 * M + 4 * N  # x, dy, w, rstd in; dx, dw out
+    if op == "xent_bwd":
+        return 2 * M * N * s + 16 * M  # logits, targets, lse, dloss in; dlogits out
+    raise ValueError(op)
 
 
 # The device code of the kernels (the launch plan is compared separately).
@@ -185,6 +194,15 @@ def whole_job_tbs(bytes_per_rank_step: int, world: int, steps: int, ms: float) -
 def make_set(op, dtype, M, N, sigma, seed, dev):
     inp = syn.make_inputs(op, dtype, M, N, seed, dev, sigma)
     out = {}
+    if op.endswith("_bwd"):
+        ref = inp["y"] if op == "softmax_bwd" else inp["x"]
+        out["dx"] = torch.empty_like(ref)
+        if op == "rmsnorm_bwd":
+            from memory_bound_row_rmsnorm_gb300 import binding as qb
+            nbytes = qb.qk_rmsnorm_bwd_workspace_size(M, N, qb.QK_F32 if dtype == "f32" else qb.QK_BF16)
+            out["dw"] = torch.empty(N, dtype=torch.float32, device=dev)
+            out["workspace"] = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        return inp, out
     if op in ("softmax", "rmsnorm"):
         out["y"] = torch.empty_like(inp["x"])
     if op == "rmsnorm":
@@ -197,7 +215,15 @@ def make_set(op, dtype, M, N, sigma, seed, dev):
 
 def launch(qb, op, dtype, inp, out, M, N, stream):
     code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
-    if op == "softmax":
+    if op == "softmax_bwd":
+        qb.qk_softmax_bwd(inp["y"], inp["dy"], out["dx"], M, N, code, stream)
+    elif op == "rmsnorm_bwd":
+        ws = out["workspace"]
+        qb.qk_rmsnorm_bwd(inp["x"], inp["w"], inp["rstd"], inp["dy"], out["dx"], out["dw"], ws,
+                          ws.numel(), M, N, code, stream)
+    elif op == "xent_bwd":
+        qb.qk_xent_bwd(inp["x"], inp["targets"], inp["lse"], inp["dloss"], out["dx"], M, N, code, stream)
+    elif op == "softmax":
         qb.qk_softmax_fwd(inp["x"], out["y"], M, N, code, stream)
     elif op == "rmsnorm":
         qb.qk_rmsnorm_fwd(inp["x"], inp["w"], out["y"], out["rstd"], M, N, EPS, code, stream)
@@ -291,6 +317,28 @@ def e2e_pipelined(qb, op, dtype, dev_sets, M, N, steps, dev):
     return start.elapsed_time(stop), steps, h2d, d2h
 
 
+def oracle_inputs(op, dtype, rows, N, sigma, seed):
+    """Seeded rows of the workload, widened to float64 for the oracle."""
+    inp = syn.make_inputs(op, dtype, rows, N, seed, "cpu", sigma)
+    return {k: (v.numpy() if v.dtype == torch.int64 else v.to(torch.float64).numpy()) for k, v in inp.items()}
+
+
+def oracle_call(oracle, lib, op, d, sl):
+    """The oracle (as it stands) on rows `sl` of the inputs `d`."""
+    if op == "softmax":
+        oracle.softmax_fwd(d["x"][sl], lib)
+    elif op == "rmsnorm":
+        oracle.rmsnorm_fwd(d["x"][sl], d["w"], EPS, lib)
+    elif op == "xent":
+        oracle.xent_fwd(d["x"][sl], d["targets"][sl], lib)
+    elif op == "softmax_bwd":
+        oracle.softmax_bwd(d["y"][sl], d["dy"][sl], lib)
+    elif op == "rmsnorm_bwd":
+        oracle.rmsnorm_bwd(d["x"][sl], d["w"], d["rstd"][sl], d["dy"][sl], lib)
+    else:
+        oracle.xent_bwd(d["x"][sl], d["targets"][sl], d["lse"][sl], d["dloss"][sl], lib)
+
+
 def cpu_oracle_rate(op, dtype, M, N, sigma, budget_s: float, seed: int = 4242):
     """The fp64 oracle, as it stands, over seeded rows of the workload on all
     host cores (one thread per core, each running the oracle on its own rows).
@@ -302,22 +350,11 @@ def cpu_oracle_rate(op, dtype, M, N, sigma, budget_s: float, seed: int = 4242):
     cores = os.cpu_count() or 1
     lib = oracle.library()
     rows = min(M, max(cores * 16, 256))
-    inp = syn.make_inputs(op, dtype, rows, N, seed, "cpu", sigma)
-    x = inp["x"].to(torch.float64).numpy()
-    w = inp["w"].to(torch.float64).numpy() if op == "rmsnorm" else None
-    t = inp["targets"].numpy() if op == "xent" else None
-    parts = np.array_split(np.arange(rows), cores)
+    d = oracle_inputs(op, dtype, rows, N, sigma, seed)
+    parts = [p for p in np.array_split(np.arange(rows), cores) if p.size]
 
     def work(idx):
-        if idx.size == 0:
-            return
-        sl = slice(int(idx[0]), int(idx[-1]) + 1)
-        if op == "softmax":
-            oracle.softmax_fwd(x[sl], lib)
-        elif op == "rmsnorm":
-            oracle.rmsnorm_fwd(x[sl], w, EPS, lib)
-        else:
-            oracle.xent_fwd(x[sl], t[sl], lib)
+        oracle_call(oracle, lib, op, d, slice(int(idx[0]), int(idx[-1]) + 1))
 
     reps = 0
     with cf.ThreadPoolExecutor(max_workers=cores) as ex:
@@ -350,20 +387,11 @@ def run_reference(args, op, dtype, M, N, sigma):
     import concurrent.futures as cf
 
     lib = oracle.library()
-    inp = syn.make_inputs(op, dtype, rows, N, 4343, "cpu", sigma)
-    x = inp["x"].to(torch.float64).numpy()
-    w = inp["w"].to(torch.float64).numpy() if op == "rmsnorm" else None
-    t = inp["targets"].numpy() if op == "xent" else None
+    d = oracle_inputs(op, dtype, rows, N, sigma, 4343)
     parts = [p for p in np.array_split(np.arange(rows), cores) if p.size]
 
     def work(idx):
-        sl = slice(int(idx[0]), int(idx[-1]) + 1)
-        if op == "softmax":
-            oracle.softmax_fwd(x[sl], lib)
-        elif op == "rmsnorm":
-            oracle.rmsnorm_fwd(x[sl], w, EPS, lib)
-        else:
-            oracle.xent_fwd(x[sl], t[sl], lib)
+        oracle_call(oracle, lib, op, d, slice(int(idx[0]), int(idx[-1]) + 1))
 
     with cf.ThreadPoolExecutor(max_workers=cores) as ex:
         for _ in range(W):
@@ -402,10 +430,13 @@ def run_sweep(args, path):
     peak, peak_src = measured_peak()
     points = []
     with open(path, "w") as fout:
-        for op in ("softmax", "rmsnorm", "xent"):
+        for op in args.sweep_ops.split(","):
             for dtype in ("f32", "bf16"):
                 for M in syn.SWEEP_M:
                     for N in syn.SWEEP_N:
+                        code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
+                        if N > qb.qk_max_row_elements(OP_CODES[op], code):
+                            continue  # longer rows than this operator takes
                         sb = min_bytes(op, dtype, M, N)
                         nsets = max(2, math.ceil(4 * L2_BYTES / sb))
                         sets = [make_set(op, dtype, M, N, 1.0, 77 + i, dev) for i in range(nsets)]
@@ -420,7 +451,7 @@ def run_sweep(args, path):
                         ms = e0.elapsed_time(e1) / K
                         tbs = sb / (ms * 1e-3) / 1e12
                         code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
-                        opc = {"softmax": 0, "rmsnorm": 1, "xent": 2}[op]
+                        opc = OP_CODES[op]
                         rec = {"op": op, "dtype": dtype, "M": M, "N": N, "TBps": tbs,
                                "frac": tbs * 1e3 / peak, "ms": ms, "steps": K,
                                "launch": "cuda_graph" if args.graph else "stream",
@@ -441,13 +472,16 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(syn.WORKLOADS) + sorted(syn.BWD_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", metavar="JSONL", help="time every sweep point instead; write them here")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: total CPU time budget of the timed steps")
+    ap.add_argument("--sweep-ops", default="softmax,rmsnorm,xent",
+                    help="operators of --sweep (also softmax_bwd, rmsnorm_bwd, xent_bwd)")
     ap.add_argument("--graph", action="store_true",
                     help="issue the timed steps as one CUDA-graph replay (no host launch overhead)")
     args = ap.parse_args()
@@ -455,7 +489,7 @@ def main():
     if args.sweep:
         run_sweep(args, args.sweep)
         return
-    op, dtype, M, N, sigma = syn.WORKLOADS[args.workload]
+    op, dtype, M, N, sigma = {**syn.WORKLOADS, **syn.BWD_WORKLOADS}[args.workload]
 
     if args.impl == "reference":
         run_reference(args, op, dtype, M, N, sigma)
@@ -484,7 +518,7 @@ def main():
     sets = [make_set(op, dtype, M, N, sigma, rank_seed(rank, i), dev) for i in range(nsets)]
     stream = torch.cuda.current_stream(dev)
     code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
-    opcode = {"softmax": qb.QK_OP_SOFTMAX, "rmsnorm": qb.QK_OP_RMSNORM, "xent": qb.QK_OP_XENT}[op]
+    opcode = OP_CODES[op]
     plan = qb.qk_get_plan(opcode, code, M, N)
 
     for i in range(args.warmup):

@@ -253,21 +253,21 @@ const Choice kXentTable[] = {
 // Backward passes load two matrices per item (softmax, RMSNorm), so they hold
 // at most 4-8 vectors of each per thread; cross-entropy's backward streams.
 const Choice kSoftmaxBwdTable[] = {
-    {32, 256, 8, 4, 1, 2},     {64, 256, 16, 4, 1, 2},    {128, 256, 32, 4, 1, 2},
-    {256, 256, 64, 4, 1, 2},   {512, 256, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 2},
-    {2048, 256, 256, 8, 1, 1}, {4096, 256, 256, 8, 2, 1}, {8192, 256, 256, 8, 4, 1},
+    {32, 256, 8, 4, 1, 2},     {64, 256, 16, 4, 1, 2},    {128, 256, 64, 4, 1, 2},
+    {256, 256, 128, 4, 1, 2},  {512, 128, 128, 4, 1, 1},  {1024, 256, 256, 4, 1, 1},
+    {2048, 256, 256, 8, 1, 2}, {4096, 256, 256, 8, 2, 1}, {8192, 256, 256, 8, 4, 1},
     {16384, 256, 256, 8, 8, 1}, {32768, 256, 256, 8, 16, 1},
 };
 const Choice kRmsNormBwdTable[] = {
-    {32, 256, 8, 4, 1, 2},     {64, 256, 16, 4, 1, 2},    {128, 256, 32, 4, 1, 2},
-    {256, 256, 64, 4, 1, 2},   {512, 256, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 2},
-    {2048, 256, 256, 4, 2, 2}, {4096, 256, 256, 4, 4, 2}, {8192, 256, 256, 4, 8, 2},
-    {16384, 256, 256, 4, 16, 2}, {32768, 512, 512, 4, 16, 1},
+    {32, 256, 32, 2, 1, 2},    {64, 256, 64, 2, 1, 2},    {128, 256, 64, 2, 1, 2},
+    {256, 256, 128, 2, 1, 2},  {512, 128, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 2},
+    {2048, 256, 256, 4, 2, 2}, {4096, 512, 512, 4, 2, 2}, {8192, 512, 512, 4, 4, 2},
+    {16384, 512, 512, 4, 8, 2}, {32768, 512, 512, 4, 16, 2},
 };
 const Choice kXentBwdTable[] = {
-    {32, 256, 8, 4, 1, 2},     {64, 256, 8, 8, 1, 2},     {128, 256, 16, 8, 1, 2},
-    {256, 256, 32, 8, 1, 2},   {512, 256, 64, 8, 1, 2},   {1024, 256, 128, 8, 1, 2},
-    {2048, 256, 256, 8, 1, 2}, {kStream, 256, 256, 4, 1, 2},
+    {32, 256, 8, 4, 1, 1},     {64, 256, 16, 4, 1, 2},    {128, 256, 32, 4, 1, 2},
+    {256, 128, 128, 4, 1, 2},  {512, 128, 128, 4, 1, 1},  {1024, 256, 256, 4, 1, 1},
+    {2048, 256, 256, 8, 1, 1}, {kStream, 256, 256, 8, 1, 1},  // 32 KB chunks
 };
 
 // Chooses the ring kernel (fast path) for a row of NV 16-byte vectors.

@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(THREADS) bwd_kernel(const BwdArgs a) {
         } else {  // sum dy * w * x
           float fw[E];
           if constexpr (kWeightInRegs) {
-            V::unpack(wv[k], fw);
+            V::unpack_fresh(wv[k], fw);  // not hoisted: keep w packed across the loop
           } else {
             V::unpack(valid[k] ? __ldg(wg + l + k * TPR) : make_uint4(0u, 0u, 0u, 0u), fw);
           }

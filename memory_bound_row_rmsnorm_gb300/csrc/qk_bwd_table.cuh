@@ -18,7 +18,10 @@ const KernelEntry kBwdTable[] = {
     QK_BWD(256, 64, 8, false),  QK_BWD(256, 128, 8, false), QK_BWD(256, 256, 8, false),
 #elif QK_BOP == 10  // softmax: 8 vectors a thread, clusters for long rows
     QK_BWD(256, 256, 8, false), QK_BWD(256, 256, 8, true),
-#else  // RMSNorm: 4 vectors a thread (x, dy, w and the dw partials live in registers)
+#else  // RMSNorm: 2-4 vectors a thread (x, dy, w and the dw partials live in registers)
+    QK_BWD(256, 16, 2, false),  QK_BWD(256, 32, 2, false),  QK_BWD(256, 64, 2, false),
+    QK_BWD(256, 128, 2, false), QK_BWD(256, 256, 2, false), QK_BWD(512, 512, 2, false),
+    QK_BWD(256, 256, 2, true),  QK_BWD(512, 512, 2, true),
     QK_BWD(256, 256, 4, true),  QK_BWD(512, 512, 4, true),
 #endif
 };

@@ -19,6 +19,13 @@ WORKLOADS = {
     "xent_bf16_8192x131072": ("xent", "bf16", 8192, 131072, 2.0 ** 0.5),  # N(0, 2): variance 2
     "softmax_f32_16384x131072": ("softmax", "f32", 16384, 131072, 1.0),
 }
+# Backward passes of the same workloads: (op, dtype, M, N, sigma).
+BWD_WORKLOADS = {
+    "softmax_bwd_f32_1024x4096": ("softmax_bwd", "f32", 1024, 4096, 1.0),
+    "rmsnorm_bwd_bf16_16384x4096": ("rmsnorm_bwd", "bf16", 16384, 4096, 1.0),
+    "xent_bwd_bf16_8192x131072": ("xent_bwd", "bf16", 8192, 131072, 2.0 ** 0.5),
+    "softmax_bwd_f32_16384x131072": ("softmax_bwd", "f32", 16384, 131072, 1.0),
+}
 SWEEP_M = (8192, 16384, 32768)
 SWEEP_N = (256, 1024, 4096, 16384, 65536, 262144)
 
@@ -58,8 +65,38 @@ def uniform_targets(M: int, N: int, seed: int, device="cpu") -> torch.Tensor:
     return torch.randint(0, N, (M,), generator=g, dtype=torch.int64, device=device)
 
 
+def uniform_rows(M: int, N: int, dtype, seed: int, device="cpu", lo: float = 0.0, hi: float = 1.0,
+                 row_block: int = 4096) -> torch.Tensor:
+    """Rows ~ U(lo, hi), drawn in fp32 in blocks of rows, rounded to dtype."""
+    dtype = DTYPES.get(dtype, dtype)
+    g = _gen(seed, device)
+    out = torch.empty((M, N), dtype=dtype, device=device)
+    for r0 in range(0, M, row_block):
+        r1 = min(M, r0 + row_block)
+        blk = torch.rand((r1 - r0, N), generator=g, dtype=torch.float32, device=device)
+        out[r0:r1].copy_(blk * (hi - lo) + lo)
+    return out
+
+
 def make_inputs(op: str, dtype, M: int, N: int, seed: int, device="cpu", sigma: float = 1.0) -> dict:
-    """All inputs of one call of `op` ("softmax", "rmsnorm" or "xent")."""
+    """All inputs of one call of `op`: "softmax", "rmsnorm", "xent", or a
+    backward pass ("softmax_bwd", "rmsnorm_bwd", "xent_bwd").  For the backward
+    passes the saved forward quantities are stand-ins of the right range
+    (probabilities in [0, 2/N), rstd in [0.5, 1.5], lse in [10, 14]); the
+    tests build exact ones with the oracle instead."""
+    if op == "softmax_bwd":
+        return {"y": uniform_rows(M, N, dtype, seed, device, 0.0, 2.0 / N),
+                "dy": normal_rows(M, N, dtype, seed + 1, device)}
+    if op == "rmsnorm_bwd":
+        return {"x": normal_rows(M, N, dtype, seed, device, sigma),
+                "w": uniform_weight(N, dtype, seed + 1, device),
+                "rstd": uniform_weight(M, "f32", seed + 2, device),
+                "dy": normal_rows(M, N, dtype, seed + 3, device)}
+    if op == "xent_bwd":
+        return {"x": normal_rows(M, N, dtype, seed, device, sigma),
+                "targets": uniform_targets(M, N, seed + 1, device),
+                "lse": uniform_weight(M, "f32", seed + 2, device, lo=10.0, hi=14.0),
+                "dloss": uniform_weight(M, "f32", seed + 3, device)}
     x = normal_rows(M, N, dtype, seed, device, sigma)
     if op == "softmax":
         return {"x": x}
