@@ -166,6 +166,32 @@ QK_API qk_status qk_rmsnorm_bwd(const void* x, const void* w, const float* rstd,
                                 int64_t M, int64_t N, qk_dtype dtype, void* stream);
 
 /*
+ * RMSNorm backward that allocates nothing.  (No counterpart in the article:
+ * this is an interface variant of qk_rmsnorm_bwd for callers that cannot
+ * allocate device memory -- code running under a device-memory budget that
+ * was reserved up front, hooks that a host framework hands only tensors and a
+ * stream, or code that must avoid the implicit device synchronisation that
+ * cudaMalloc / cudaFree may cause.)
+ *
+ * Same arguments, results and aliasing rules as qk_rmsnorm_bwd, without the
+ * workspace: the dw partial sums go to a fixed 16 MiB array in the library's
+ * own device memory, which every GPU that loads the library's device code
+ * holds until the process exits.  Calls whose workspace need
+ * (qk_rmsnorm_bwd_workspace_size) exceeds 16 MiB return QK_ERR_UNSUPPORTED.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array: calls whose kernels overlap on
+ * the GPU (for example on two streams) race on it and must be serialised by
+ * the caller.  Nothing in it needs clearing between calls: each call writes
+ * every partial it later reads.  No cudaMalloc, cudaFree or other allocating
+ * routine is called.
+ */
+QK_API qk_status qk_rmsnorm_bwd_noalloc(const void* x, const void* w, const float* rstd,
+                                        const void* dy, void* dx, float* dw, int64_t M, int64_t N,
+                                        qk_dtype dtype, void* stream);
+
+/*
  * Cross-entropy backward: dlogits[i,j] = dloss_i * (exp(logits[i,j] - lse_i) - [j == t_i]).
  *   logits [M, N] dtype; targets [M] int64; lse [M] float32 from qk_xent_fwd;
  *   dloss  [M] float32 upstream gradient of each row's loss, or NULL for 1.

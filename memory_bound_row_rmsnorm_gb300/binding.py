@@ -33,7 +33,7 @@ _EXPORTS = (
     "qk_softmax_fwd", "qk_rmsnorm_fwd", "qk_xent_fwd", "qk_status_string",
     "qk_get_device_status", "qk_max_row_elements", "qk_get_plan",
     "qk_set_plan_override", "qk_test_wait_timeout", "qk_softmax_bwd", "qk_rmsnorm_bwd",
-    "qk_rmsnorm_bwd_workspace_size", "qk_xent_bwd",
+    "qk_rmsnorm_bwd_workspace_size", "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc",
 )
 
 
@@ -84,10 +84,11 @@ def load_library(path: str = LIBRARY):
         lib.qk_rmsnorm_bwd_workspace_size.argtypes = [i64, i64, i32, ctypes.POINTER(ctypes.c_size_t)]
         lib.qk_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i64, i64, i32, vp]
         lib.qk_xent_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, vp]
+        lib.qk_rmsnorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
         for name in ("qk_softmax_fwd", "qk_rmsnorm_fwd", "qk_xent_fwd", "qk_get_device_status",
                      "qk_get_plan", "qk_set_plan_override", "qk_test_wait_timeout",
                      "qk_softmax_bwd", "qk_rmsnorm_bwd_workspace_size", "qk_rmsnorm_bwd",
-                     "qk_xent_bwd"):
+                     "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc"):
             getattr(lib, name).restype = i32
         del fp
         _lib = lib
@@ -154,6 +155,14 @@ def qk_rmsnorm_bwd(x, w, rstd, dy, dx, dw, workspace, workspace_bytes: int, M: i
     _check(load_library().qk_rmsnorm_bwd(_ptr(x), _ptr(w), _ptr(rstd), _ptr(dy), _ptr(dx), _ptr(dw),
                                          _ptr(workspace), int(workspace_bytes), M, N, dtype,
                                          _stream(stream)), "qk_rmsnorm_bwd")
+
+
+def qk_rmsnorm_bwd_noalloc(x, w, rstd, dy, dx, dw, M: int, N: int, dtype: int, stream=None) -> None:
+    """qk_rmsnorm_bwd with the workspace taken from the library's fixed device
+    array (for callers that cannot allocate device memory)."""
+    _check(load_library().qk_rmsnorm_bwd_noalloc(_ptr(x), _ptr(w), _ptr(rstd), _ptr(dy), _ptr(dx),
+                                                 _ptr(dw), M, N, dtype, _stream(stream)),
+           "qk_rmsnorm_bwd_noalloc")
 
 
 def qk_xent_bwd(logits, targets, lse, dloss, dlogits, M: int, N: int, dtype: int, stream=None) -> None:
