@@ -180,3 +180,67 @@ void oracle_xent_bwd(const double *x, const int64_t *target, const double *lse,
         }
     }
 }
+
+/* ------------------------------------------------------------------------
+ * Cross-entropy variants (ignore index, z-loss, mean over rows).
+ *   loss_i = lse_i - x_{i,t_i} + z * lse_i^2      for t_i != ignore_index,
+ *   loss_i = 0                                    for t_i == ignore_index,
+ *   mean   = sum of loss_i over the rows not ignored / their number
+ *            (NaN when every row is ignored: 0 / 0);
+ *   dx_ij  = dloss_i * ((1 + 2 z lse_i) exp(x_ij - lse_i) - [j == t_i]),
+ *            0 on ignored rows.  d(z lse^2)/dx_j = 2 z lse softmax_j.
+ * A target that is neither ignored nor inside [0, N) gives NaN, as before.
+ * ------------------------------------------------------------------------ */
+void oracle_xent_fwd_ex(const double *x, const int64_t *target, double *loss, double *lse,
+                        double *mean, int64_t M, int64_t N, int64_t ignore_index, double z)
+{
+    double total = 0.0;
+    int64_t counted = 0;
+    for (int64_t i = 0; i < M; ++i) {
+        const double *xi = x + i * N;
+
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j)
+            if (xi[j] > m) m = xi[j];
+
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            s += exp(xi[j] - m);
+
+        double l = m + log(s);
+        int64_t t = target[i];
+        double li;
+        if (t == ignore_index) {
+            li = 0.0;
+        } else {
+            li = (t >= 0 && t < N) ? l - xi[t] + z * l * l : NAN;
+            total += li;
+            counted += 1;
+        }
+        loss[i] = li;
+        if (lse) lse[i] = l;
+    }
+    if (mean) *mean = total / (double)counted;
+}
+
+void oracle_xent_bwd_ex(const double *x, const int64_t *target, const double *lse,
+                        const double *dloss, double *dx, int64_t M, int64_t N,
+                        int64_t ignore_index, double z)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        const double *xi = x + i * N;
+        double *di = dx + i * N;
+        int64_t t = target[i];
+
+        for (int64_t j = 0; j < N; ++j) {
+            if (t == ignore_index) {
+                di[j] = 0.0;
+            } else if (t >= 0 && t < N) {
+                double p = exp(xi[j] - lse[i]);
+                di[j] = dloss[i] * ((1.0 + 2.0 * z * lse[i]) * p - (j == t ? 1.0 : 0.0));
+            } else {
+                di[j] = NAN;
+            }
+        }
+    }
+}

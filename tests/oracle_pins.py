@@ -287,7 +287,6 @@ def pin_xent_brute_force(lib):
     _close(loss, bl, 1e-13, "xent: 4x8 brute force loss")
 
 
-ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
 # --------------------------------------------------------------------------
@@ -438,6 +437,48 @@ def pin_xent_bwd_brute_force(lib):
                      for j, v in enumerate(xr)])
     dx = oracle.xent_bwd(x, t, lse, g, lib)
     assert np.max(np.abs(dx - np.array(want))) <= 1e-14, "xent bwd: 4x8 brute force"
+
+
+
+
+# --------------------------------------------------------------------------
+# Cross-entropy variants: ignore index, z-loss, mean over rows
+# --------------------------------------------------------------------------
+def pin_xent_ex_closed_form(lib):
+    x = np.array([[0.0, math.log(3.0)], [0.0, math.log(3.0)], [1.0, 2.0]])
+    z = 0.5
+    loss, lse, mean = oracle.xent_fwd_ex(x, np.array([1, -100, 0]), ignore_index=-100, z=z, lib=lib)
+    l4 = math.log(4.0)
+    lse2 = math.log(math.e + math.e ** 2)
+    want = [math.log(4.0 / 3.0) + z * l4 * l4, 0.0, lse2 - 1.0 + z * lse2 * lse2]
+    _close(loss, want, 1e-14, "xent ex: z-loss closed form and ignored row")
+    assert abs(mean - (want[0] + want[2]) / 2) <= 1e-14 * abs(mean), "xent ex: mean excludes ignored rows"
+    _close(lse, [l4, l4, lse2], 1e-14, "xent ex: lse written on every row")
+
+
+def pin_xent_ex_reduces_to_plain(lib):
+    rng = _rng(30)
+    x = rng.normal(size=(6, 17))
+    t = rng.integers(0, 17, size=6)
+    loss0, lse0 = oracle.xent_fwd(x, t, lib)
+    loss, lse, mean = oracle.xent_fwd_ex(x, t, lib=lib)  # no ignore index, z = 0
+    _close(loss, loss0, 1e-15, "xent ex: z=0, no ignore index is the plain loss")
+    assert abs(mean - np.mean(loss0)) <= 1e-14 * abs(mean), "xent ex: mean of every row"
+    all_ignored = oracle.xent_fwd_ex(x, np.full(6, 7), ignore_index=7, lib=lib)[2]
+    assert math.isnan(all_ignored), "xent ex: the mean of no rows is NaN"
+
+
+def pin_xent_ex_bwd_finite_differences(lib):
+    rng = _rng(31)
+    x = rng.normal(0, 1.5, size=(4, 6))
+    t = np.array([2, -1, 5, 0])
+    g = rng.uniform(0.5, 2.0, size=4)
+    z = 0.3
+    _, lse, _ = oracle.xent_fwd_ex(x, t, ignore_index=-1, z=z, lib=lib)
+    dx = oracle.xent_bwd_ex(x, t, lse, g, ignore_index=-1, z=z, lib=lib)
+    fd = _fd_grad(lambda q: float(np.sum(g * oracle.xent_fwd_ex(q, t, -1, z, lib)[0])), x)
+    assert np.max(np.abs(dx - fd)) <= 1e-7, "xent ex bwd: not the derivative of the forward"
+    assert np.all(dx[1] == 0.0), "xent ex bwd: an ignored row has zero gradient"
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

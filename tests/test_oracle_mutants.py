@@ -28,10 +28,12 @@ MUTANTS = [
     ("rmsnorm: weight dropped", "yi[j] = xi[j] * r * w[j];", "yi[j] = xi[j] * r;"),
     ("rmsnorm: rms instead of its reciprocal", "double r = 1.0 / sqrt(ms + eps);", "double r = sqrt(ms + eps);"),
     ("rmsnorm: eps times the mean", "1.0 / sqrt(ms + eps)", "1.0 / sqrt(ms * (1.0 + eps))"),
-    ("xent: sign of the loss", "l - xi[t]", "xi[t] - l"),
-    ("xent: max dropped from lse", "double l = m + log(s);", "double l = log(s);"),
-    ("xent: target column off by one", "l - xi[t]", "l - xi[t > 0 ? t - 1 : t]"),
-    ("xent: log2 instead of ln", "double l = m + log(s);", "double l = m + log2(s);"),
+    ("xent: sign of the loss", "? l - xi[t] : NAN", "? xi[t] - l : NAN"),
+    ("xent: max dropped from lse", "double l = m + log(s);\n        int64_t t = target[i];\n        loss[i]",
+     "double l = log(s);\n        int64_t t = target[i];\n        loss[i]"),
+    ("xent: target column off by one", "? l - xi[t] : NAN", "? l - xi[t > 0 ? t - 1 : t] : NAN"),
+    ("xent: log2 instead of ln", "double l = m + log(s);\n        int64_t t = target[i];\n        loss[i]",
+     "double l = m + log2(s);\n        int64_t t = target[i];\n        loss[i]"),
     ("xent: no range check", "(t >= 0 && t < N) ? l - xi[t] : NAN", "(t > -2 && t <= N) ? l - xi[t] : NAN"),
     ("softmax bwd: sign of the dot", "di[j] = yi[j] * (gi[j] - dot);", "di[j] = yi[j] * (gi[j] + dot);"),
     ("softmax bwd: y dropped from the dot", "dot += gi[j] * yi[j];", "dot += gi[j];"),
@@ -42,8 +44,15 @@ MUTANTS = [
     ("rmsnorm bwd: dw without rstd", "dw[j] += gi[j] * xi[j] * r;", "dw[j] += gi[j] * xi[j];"),
     ("rmsnorm bwd: sign of the correction", "di[j] = r * gi[j] * w[j] - xi[j] * c;", "di[j] = r * gi[j] * w[j] + xi[j] * c;"),
     ("xent bwd: one-hot added", "dloss[i] * (p - (j == t ? 1.0 : 0.0))", "dloss[i] * (p + (j == t ? 1.0 : 0.0))"),
-    ("xent bwd: lse dropped", "double p = exp(xi[j] - lse[i]);", "double p = exp(xi[j]);"),
+    ("xent bwd: lse dropped", "double p = exp(xi[j] - lse[i]);\n            di[j] = ok",
+     "double p = exp(xi[j]);\n            di[j] = ok"),
     ("xent bwd: upstream gradient dropped", "dloss[i] * (p - (j == t ? 1.0 : 0.0))", "(p - (j == t ? 1.0 : 0.0))"),
+    ("xent ex: z-loss uses lse not lse^2", "l - xi[t] + z * l * l", "l - xi[t] + z * l"),
+    ("xent ex: ignored rows counted in the mean", "            total += li;\n            counted += 1;\n        }",
+     "            total += li;\n        }\n        counted += 1;"),
+    ("xent ex bwd: z-loss gradient factor 1 + z lse", "(1.0 + 2.0 * z * lse[i])", "(1.0 + z * lse[i])"),
+    ("xent ex bwd: ignored rows not zeroed", "            if (t == ignore_index) {\n                di[j] = 0.0;",
+     "            if (t == ignore_index) {\n                di[j] = dloss[i];"),
 ]
 
 
