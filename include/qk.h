@@ -202,6 +202,42 @@ QK_API qk_status qk_xent_bwd(const void* logits, const int64_t* targets, const f
                              const float* dloss, void* dlogits, int64_t M, int64_t N,
                              qk_dtype dtype, void* stream);
 
+/*
+ * Cross-entropy variants.  Options of qk_xent_fwd_ex / qk_xent_bwd_ex (NULL
+ * means the plain operator: no ignore index, no z-loss):
+ *   ignore_index  rows whose target equals it get loss 0 and zero gradient and
+ *                 are left out of the mean (QK_NO_IGNORE_INDEX: none);
+ *   z_loss        coefficient z of the term z * lse^2 added to each row's loss
+ *                 (a penalty on the log-partition function; 0: none).
+ * The article names cross-entropy loss only; these are the common training
+ * variants of the same per-row definition, added in its epilogue.
+ */
+#define QK_NO_IGNORE_INDEX INT64_MIN
+typedef struct {
+  int64_t ignore_index;
+  float z_loss;
+} qk_xent_options;
+
+/*
+ * loss[i] = lse[i] - x[i, t_i] + z * lse[i]^2 (0 on ignored rows, NaN for a
+ * target outside [0, N) that is not ignored); lse as in qk_xent_fwd.
+ * mean_loss (may be NULL): one float32, the mean of loss over the rows that
+ * are not ignored, summed in a fixed order (NaN when every row is ignored).
+ * It must not overlap the other buffers.
+ */
+QK_API qk_status qk_xent_fwd_ex(const void* logits, const int64_t* targets, float* loss, float* lse,
+                                float* mean_loss, int64_t M, int64_t N, qk_dtype dtype,
+                                const qk_xent_options* options, void* stream);
+
+/*
+ * dlogits[i,j] = dloss_i * ((1 + 2 z lse_i) * exp(x[i,j] - lse_i) - [j == t_i]),
+ * zero on ignored rows; otherwise as qk_xent_bwd.  For the gradient of the
+ * mean, pass dloss_i = 1 / (number of rows not ignored).
+ */
+QK_API qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float* lse,
+                                const float* dloss, void* dlogits, int64_t M, int64_t N,
+                                qk_dtype dtype, const qk_xent_options* options, void* stream);
+
 /* Static English description of a status code; never NULL. */
 QK_API const char* qk_status_string(qk_status s);
 

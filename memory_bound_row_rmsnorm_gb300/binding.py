@@ -34,13 +34,19 @@ _EXPORTS = (
     "qk_get_device_status", "qk_max_row_elements", "qk_get_plan",
     "qk_set_plan_override", "qk_test_wait_timeout", "qk_softmax_bwd", "qk_rmsnorm_bwd",
     "qk_rmsnorm_bwd_workspace_size", "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc",
+    "qk_xent_fwd_ex", "qk_xent_bwd_ex",
 )
+QK_NO_IGNORE_INDEX = -(2 ** 63)
 
 
 class QkError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: {qk_status_string(status)} (status {status})")
+
+
+class qk_xent_options(ctypes.Structure):
+    _fields_ = [("ignore_index", ctypes.c_int64), ("z_loss", ctypes.c_float)]
 
 
 class qk_plan(ctypes.Structure):
@@ -85,10 +91,13 @@ def load_library(path: str = LIBRARY):
         lib.qk_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i64, i64, i32, vp]
         lib.qk_xent_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, vp]
         lib.qk_rmsnorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
+        op = ctypes.POINTER(qk_xent_options)
+        lib.qk_xent_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, op, vp]
+        lib.qk_xent_bwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, op, vp]
         for name in ("qk_softmax_fwd", "qk_rmsnorm_fwd", "qk_xent_fwd", "qk_get_device_status",
                      "qk_get_plan", "qk_set_plan_override", "qk_test_wait_timeout",
                      "qk_softmax_bwd", "qk_rmsnorm_bwd_workspace_size", "qk_rmsnorm_bwd",
-                     "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc"):
+                     "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc", "qk_xent_fwd_ex", "qk_xent_bwd_ex"):
             getattr(lib, name).restype = i32
         del fp
         _lib = lib
@@ -170,6 +179,27 @@ def qk_xent_bwd(logits, targets, lse, dloss, dlogits, M: int, N: int, dtype: int
                                       _ptr(dlogits), M, N, dtype, _stream(stream)), "qk_xent_bwd")
 
 
+def _options(ignore_index, z_loss):
+    if ignore_index is None and not z_loss:
+        return None
+    return ctypes.byref(qk_xent_options(
+        QK_NO_IGNORE_INDEX if ignore_index is None else int(ignore_index), float(z_loss)))
+
+
+def qk_xent_fwd_ex(logits, targets, loss, lse, mean_loss, M: int, N: int, dtype: int,
+                   ignore_index=None, z_loss: float = 0.0, stream=None) -> None:
+    _check(load_library().qk_xent_fwd_ex(_ptr(logits), _ptr(targets), _ptr(loss), _ptr(lse),
+                                         _ptr(mean_loss), M, N, dtype, _options(ignore_index, z_loss),
+                                         _stream(stream)), "qk_xent_fwd_ex")
+
+
+def qk_xent_bwd_ex(logits, targets, lse, dloss, dlogits, M: int, N: int, dtype: int,
+                   ignore_index=None, z_loss: float = 0.0, stream=None) -> None:
+    _check(load_library().qk_xent_bwd_ex(_ptr(logits), _ptr(targets), _ptr(lse), _ptr(dloss),
+                                         _ptr(dlogits), M, N, dtype, _options(ignore_index, z_loss),
+                                         _stream(stream)), "qk_xent_bwd_ex")
+
+
 def qk_status_string(status: int) -> str:
     return load_library().qk_status_string(status).decode()
 
@@ -242,16 +272,23 @@ def rmsnorm_fwd(x, w, eps: float = 1e-6, out=None, want_rstd: bool = True, strea
     return y, rstd
 
 
-def xent_fwd(logits, targets, want_lse: bool = True, stream=None):
-    """Per-row cross-entropy; returns (loss, lse) (lse is None if not wanted)."""
+def xent_fwd(logits, targets, want_lse: bool = True, ignore_index=None, z_loss: float = 0.0,
+             want_mean: bool = False, stream=None):
+    """Per-row cross-entropy; returns (loss, lse) (lse is None if not wanted),
+    or (loss, lse, mean) with want_mean."""
     import torch
     M, N = _rows(logits)
     if targets.dtype != torch.int64 or targets.numel() != M or not targets.is_contiguous():
         raise ValueError("targets must be a contiguous int64 tensor with one entry per row")
     loss = torch.empty(logits.shape[:-1], dtype=torch.float32, device=logits.device)
     lse = torch.empty_like(loss) if want_lse else None
-    qk_xent_fwd(logits, targets, loss, lse, M, N, _dtype_code(logits), stream)
-    return loss, lse
+    if ignore_index is None and not z_loss and not want_mean:
+        qk_xent_fwd(logits, targets, loss, lse, M, N, _dtype_code(logits), stream)
+        return loss, lse
+    mean = torch.empty((), dtype=torch.float32, device=logits.device) if want_mean else None
+    qk_xent_fwd_ex(logits, targets, loss, lse, mean, M, N, _dtype_code(logits), ignore_index, z_loss,
+                   stream)
+    return (loss, lse, mean) if want_mean else (loss, lse)
 
 
 def softmax_bwd(y, dy, out=None, stream=None):
@@ -277,10 +314,11 @@ def rmsnorm_bwd(x, w, rstd, dy, stream=None):
     return dx, dw
 
 
-def xent_bwd(logits, targets, lse, dloss=None, stream=None):
-    """Cross-entropy backward: dloss * (softmax(logits) - onehot(targets))."""
+def xent_bwd(logits, targets, lse, dloss=None, ignore_index=None, z_loss: float = 0.0, stream=None):
+    """Cross-entropy backward: dloss * ((1 + 2 z lse) softmax(logits) - onehot(targets))."""
     import torch
     M, N = _rows(logits)
     dx = torch.empty_like(logits)
-    qk_xent_bwd(logits, targets, lse, dloss, dx, M, N, _dtype_code(logits), stream)
+    qk_xent_bwd_ex(logits, targets, lse, dloss, dx, M, N, _dtype_code(logits), ignore_index, z_loss,
+                   stream)
     return dx

@@ -620,20 +620,26 @@ qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int
   return run(kRmsNorm, dtype, a, fast, stream);
 }
 
-qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* loss, float* lse,
-                      int64_t M, int64_t N, qk_dtype dtype, void* stream) {
+qk_status qk_xent_fwd_ex(const void* logits, const int64_t* targets, float* loss, float* lse,
+                         float* mean_loss, int64_t M, int64_t N, qk_dtype dtype,
+                         const qk_xent_options* options, void* stream) {
+  const int64_t ignore = options != nullptr ? options->ignore_index : QK_NO_IGNORE_INDEX;
+  const float z = options != nullptr ? options->z_loss : 0.f;
   qk_status st = check_sizes(kXent, dtype, M, N);
   if (st != QK_OK) return st;
+  if (!std::isfinite(z)) return QK_ERR_INVALID_ARG;
   if (M == 0) return QK_OK;
   if (logits == nullptr || targets == nullptr || loss == nullptr) return QK_ERR_INVALID_ARG;
   const size_t es = size_t(elem_size(dtype));
   if (!aligned_to(logits, es) || !aligned_to(targets, 8) || !aligned_to(loss, 4) ||
-      !aligned_to(lse, 4))
+      !aligned_to(lse, 4) || !aligned_to(mean_loss, 4))
     return QK_ERR_MISALIGNED;
   const int64_t bytes = M * N * int64_t(es), tbytes = M * 8, obytes = M * 4;
   if (overlap(loss, obytes, logits, bytes) || overlap(loss, obytes, targets, tbytes) ||
       overlap(loss, obytes, lse, obytes) || overlap(lse, obytes, logits, bytes) ||
-      overlap(lse, obytes, targets, tbytes))
+      overlap(lse, obytes, targets, tbytes) || overlap(mean_loss, 4, logits, bytes) ||
+      overlap(mean_loss, 4, targets, tbytes) || overlap(mean_loss, 4, loss, obytes) ||
+      overlap(mean_loss, 4, lse, obytes))
     return QK_ERR_INVALID_ARG;
   RowArgs a = {};
   a.x = logits;
@@ -642,8 +648,32 @@ qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* loss, f
   a.lse = lse;
   a.M = M;
   a.N = N;
+  a.ignore_index = ignore;
+  a.z_loss = z;
   const bool fast = aligned16(logits) && (N * int64_t(es)) % 16 == 0;
-  return run(kXent, dtype, a, fast, stream);
+  st = run(kXent, dtype, a, fast, stream);
+  if (st != QK_OK || mean_loss == nullptr) return st;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(1024, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* lp = loss;
+  if (cudaLaunchKernelEx(&cfg, xent_mean_kernel<0>, lp, targets, M, ignore, mean_loss) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_LAUNCH;
+  }
+  return QK_OK;
+}
+
+qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* loss, float* lse,
+                      int64_t M, int64_t N, qk_dtype dtype, void* stream) {
+  return qk_xent_fwd_ex(logits, targets, loss, lse, nullptr, M, N, dtype, nullptr, stream);
 }
 
 // Fast-path requirements of the backward passes: 16-byte aligned rows.
@@ -724,11 +754,14 @@ qk_status qk_rmsnorm_bwd(const void* x, const void* w, const float* rstd, const 
   return run_bwd(kOpRmsNormBwd, dtype, a, dw, workspace_bytes, stream);
 }
 
-qk_status qk_xent_bwd(const void* logits, const int64_t* targets, const float* lse,
-                      const float* dloss, void* dlogits, int64_t M, int64_t N, qk_dtype dtype,
-                      void* stream) {
+qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float* lse,
+                         const float* dloss, void* dlogits, int64_t M, int64_t N, qk_dtype dtype,
+                         const qk_xent_options* options, void* stream) {
+  const int64_t ignore = options != nullptr ? options->ignore_index : QK_NO_IGNORE_INDEX;
+  const float z = options != nullptr ? options->z_loss : 0.f;
   qk_status st = check_sizes(kOpXentBwd, dtype, M, N);
   if (st != QK_OK) return st;
+  if (!std::isfinite(z)) return QK_ERR_INVALID_ARG;
   if (M == 0) return QK_OK;
   if (logits == nullptr || targets == nullptr || lse == nullptr || dlogits == nullptr)
     return QK_ERR_INVALID_ARG;
@@ -750,7 +783,15 @@ qk_status qk_xent_bwd(const void* logits, const int64_t* targets, const float* l
   a.out = dlogits;
   a.M = M;
   a.N = N;
+  a.ignore_index = ignore;
+  a.z_loss = z;
   return run_bwd(kOpXentBwd, dtype, a, nullptr, 0, stream);
+}
+
+qk_status qk_xent_bwd(const void* logits, const int64_t* targets, const float* lse,
+                      const float* dloss, void* dlogits, int64_t M, int64_t N, qk_dtype dtype,
+                      void* stream) {
+  return qk_xent_bwd_ex(logits, targets, lse, dloss, dlogits, M, N, dtype, nullptr, stream);
 }
 
 qk_status qk_get_device_status(void* stream) {

@@ -37,6 +37,8 @@ struct BwdArgs {
   int64_t M;
   int64_t N;
   float inv_n;          // 1 / N
+  float z_loss;         // x-entropy: z-loss coefficient (gradient factor 1 + 2 z lse)
+  int64_t ignore_index; // x-entropy: rows with this target get zero gradient
   int32_t chunks;       // ring steps per row (streamed x-entropy rows), else 1
   int32_t slots;        // ring slots per CTA
   uint32_t slot_bytes;  // bytes of ONE input's item in a slot (multiple of 128)
@@ -328,8 +330,12 @@ __global__ void __launch_bounds__(THREADS) bwd_kernel(const BwdArgs a) {
         og[l + k * TPR] = V::pack(o);
       }
     } else {  // cross-entropy: dloss * (exp(x - lse) - onehot)
+      const bool ignored = (trow == a.ignore_index);
       const bool tok = trow >= 0 && trow < N;
-      const float gv = tok ? gs : __int_as_float(0x7fc00000);  // NaN row for a bad target
+      // zero row if ignored, NaN row for a bad target; the z-loss term scales
+      // the softmax part by 1 + 2 z lse
+      const float gv = ignored ? 0.f : (tok ? gs : __int_as_float(0x7fc00000));
+      const float zf = fmaf(2.f * a.z_loss, rs, 1.f);
       const float lb = rs * kLog2e;
       const int64_t tl = tok ? trow / E - cbase : -1;  // target vector, relative to the slot
       const int te = int(trow & (E - 1));
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(THREADS) bwd_kernel(const BwdArgs a) {
         for (int e = 0; e < E; e += 2) {
           const float2 t = fma2(make_float2(f[e], f[e + 1]), make_float2(kLog2e, kLog2e),
                                 make_float2(-lb, -lb));
-          float p0 = exp2_approx(t.x), p1 = exp2_approx(t.y);
+          float p0 = exp2_approx(t.x) * zf, p1 = exp2_approx(t.y) * zf;
           if (tvec && te == e) p0 -= 1.f;
           if (tvec && te == e + 1) p1 -= 1.f;
           const float2 v = mul2(make_float2(p0, p1), make_float2(gv, gv));

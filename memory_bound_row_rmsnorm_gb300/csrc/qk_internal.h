@@ -21,6 +21,8 @@ struct RowArgs {
   int64_t N;
   float eps;
   float inv_n;          // 1 / N, rounded once on the host (RMSNorm mean)
+  float z_loss;         // cross-entropy: coefficient of z * lse^2 added to the loss (0: none)
+  int64_t ignore_index; // cross-entropy: rows with this target give loss 0 (INT64_MIN: none)
   int32_t chunks;       // ring slots one row slice spans (streamed rows), else 1
   int32_t slots;        // ring slots per CTA
   uint32_t slot_bytes;  // bytes per ring slot (multiple of 128)

@@ -417,13 +417,18 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       if (l == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = r;
     } else {
       const bool leader = (l == 0 && rank == 0);
+      const bool ignored = (trow == a.ignore_index);
       if (leader || own_t) {  // only the threads that write need the logarithm
         const float lse = pm + logf(ps);
         if (leader) {
           if (a.lse != nullptr) a.lse[row] = lse;
-          if (!(trow >= 0 && trow < N)) a.loss[row] = __int_as_float(0x7fc00000);  // NaN
+          if (ignored) {
+            a.loss[row] = 0.f;
+          } else if (!(trow >= 0 && trow < N)) {
+            a.loss[row] = __int_as_float(0x7fc00000);  // NaN
+          }
         }
-        if (own_t) a.loss[row] = lse - xt;
+        if (own_t && !ignored) a.loss[row] = fmaf(a.z_loss * lse, lse, lse - xt);  // + z lse^2
       }
     }
   }
@@ -560,13 +565,52 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
     if (tid == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = r;
   } else {
     const float lse = pm + logf(ps);
+    const bool ignored = (trow == a.ignore_index);
     if (tid == 0 && rank == 0) {
       if (a.lse != nullptr) a.lse[row] = lse;
-      if (!(trow >= 0 && trow < N)) a.loss[row] = __int_as_float(0x7fc00000);
+      if (ignored) {
+        a.loss[row] = 0.f;
+      } else if (!(trow >= 0 && trow < N)) {
+        a.loss[row] = __int_as_float(0x7fc00000);
+      }
     }
-    if (own_t) a.loss[row] = lse - xt;
+    if (own_t && !ignored) a.loss[row] = fmaf(a.z_loss * lse, lse, lse - xt);
   }
   if constexpr (CLUSTER) cluster_sync_all();
+}
+
+// Mean of the per-row losses over the rows whose target is not ignore_index
+// (NaN when there are none): one CTA, each thread summing a fixed strided
+// subset in order, then a fixed-shape tree -- deterministic.
+template <int kUnused = 0>
+__global__ void __launch_bounds__(1024) xent_mean_kernel(const float* __restrict__ loss,
+                                                         const int64_t* __restrict__ target,
+                                                         int64_t M, int64_t ignore_index,
+                                                         float* __restrict__ mean) {
+  __shared__ float ssum[1024];
+  __shared__ int64_t scnt[1024];
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int tid = threadIdx.x;
+  float acc = 0.f;
+  int64_t cnt = 0;
+  for (int64_t i = tid; i < M; i += 1024) {
+    if (target[i] != ignore_index) {
+      acc += loss[i];
+      ++cnt;
+    }
+  }
+  ssum[tid] = acc;
+  scnt[tid] = cnt;
+  __syncthreads();
+  for (int s = 512; s > 0; s >>= 1) {
+    if (tid < s) {
+      ssum[tid] += ssum[tid + s];
+      scnt[tid] += scnt[tid + s];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) *mean = ssum[0] / float(scnt[0]);  // 0 / 0 = NaN when every row is ignored
 }
 
 }  // namespace qk
