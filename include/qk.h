@@ -86,7 +86,7 @@ typedef enum {
  *   x      [M, N] dtype, read once.
  *   y      [M, N] dtype, written once.  y == x (exact aliasing) is allowed;
  *          any other overlap with x is QK_ERR_INVALID_ARG.
- *   M, N   rows and columns; N <= qk_max_row_elements(QK_OP_SOFTMAX, dtype).
+ *   M, N   rows and columns (any N on the aligned path; see qk_max_row_elements).
  */
 QK_API qk_status qk_softmax_fwd(const void* x, void* y, int64_t M, int64_t N, qk_dtype dtype,
                          void* stream);
@@ -250,14 +250,20 @@ QK_API const char* qk_status_string(qk_status s);
 QK_API qk_status qk_get_device_status(void* stream);
 
 /* Largest N the operator accepts for `dtype` (rows longer than this return
- * QK_ERR_UNSUPPORTED); INT64_MAX for qk_xent_fwd, which streams its rows. */
+ * QK_ERR_UNSUPPORTED).  The forward operators stream rows of any length on the
+ * aligned path (INT64_MAX): softmax and RMSNorm rows longer than 1 MiB are read
+ * twice (three HBM passes instead of two) -- only on the masked path, for
+ * unaligned rows, are softmax and RMSNorm limited to 524,288 elements.  The
+ * backward passes of softmax and RMSNorm hold rows of up to 512 KiB. */
 QK_API int64_t qk_max_row_elements(qk_op op, qk_dtype dtype);
 
 /*
  * Launch plan: how a call maps onto the GPU.  Reported by qk_get_plan() for
  * logging and benchmarks; qk_set_plan_override() pins one for tuning sweeps.
  *
- *   path            1 = TMA ring (aligned fast path), 2 = masked direct path.
+ *   path            1 = TMA ring (aligned fast path), 2 = masked direct path,
+ *                   3 = backward ring, 4 = two-pass ring (rows beyond 1 MiB;
+ *                   an override with path 4 forces it for any row).
  *   threads         threads per CTA.
  *   row_threads     threads that share one row inside a CTA (rows per CTA
  *                   step = threads / row_threads).

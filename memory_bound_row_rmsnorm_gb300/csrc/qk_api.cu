@@ -296,13 +296,38 @@ qk_status choose_ring(int op, int64_t NV, int* th, int* tpr, int* vpt, int* cl, 
   return QK_ERR_UNSUPPORTED;
 }
 
+// Rows of the forward softmax / RMSNorm longer than the largest cluster plan
+// (64K vectors, 1 MiB) are streamed twice.  A cluster splits each row when
+// there are too few rows to occupy the GPU.
+constexpr int64_t kTwoPassChunkVectors = 256 * 8;  // 32 KB chunks
+bool wants_two_pass(int op, int64_t NV) {
+  return (op == kSoftmax || op == kRmsNorm) && NV > int64_t(kMaxCluster) * kRingMaxVectorsPerCta;
+}
+
 qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p) {
   const int E = 16 / elem_size(dt);
   const int64_t NV = N / E;
   int th, tpr, vpt, cl, k;
   int slots = 0;
+  bool two_pass = false;
   const Override& ov = g_override[op][dt];
-  if (ov.on) {
+  if (ov.on && ov.plan.path == 4) {  // forced two-pass plan (tuning, tests)
+    if (!(op == kSoftmax || op == kRmsNorm)) return QK_ERR_UNSUPPORTED;
+    th = ov.plan.threads, tpr = ov.plan.row_threads, vpt = ov.plan.vec_per_thread;
+    cl = std::max(1, int(ov.plan.cluster));
+    slots = ov.plan.slots;
+    if (cl > kMaxCluster || tpr != th) return QK_ERR_UNSUPPORTED;
+    const int64_t per_cta = int64_t(tpr) * vpt;
+    k = int(((NV + cl - 1) / cl + per_cta - 1) / per_cta);
+    two_pass = true;
+  } else if (!ov.on && wants_two_pass(op, NV)) {
+    th = 256, tpr = 256, vpt = 8, slots = 3;
+    const int64_t want = 2 * int64_t(d.sms);  // row slices in flight
+    cl = 1;
+    while (cl < kMaxCluster && M * cl < want) cl <<= 1;
+    k = int(((NV + cl - 1) / cl + kTwoPassChunkVectors - 1) / kTwoPassChunkVectors);
+    two_pass = true;
+  } else if (ov.on) {
     th = ov.plan.threads, tpr = ov.plan.row_threads, vpt = ov.plan.vec_per_thread;
     cl = std::max(1, int(ov.plan.cluster));
     slots = ov.plan.slots;
@@ -320,12 +345,16 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
     qk_status st = choose_ring(op, NV, &th, &tpr, &vpt, &cl, &k, &slots);
     if (st != QK_OK) return st;
   }
-  const KernelEntry* ke = find_kernel(op, dt, is_bwd(op) ? 3 : 1, th, tpr, vpt, cl > 1);
+  const KernelEntry* ke =
+      find_kernel(op, dt, two_pass ? 4 : (is_bwd(op) ? 3 : 1), th, tpr, vpt, cl > 1);
   if (ke == nullptr) return QK_ERR_UNSUPPORTED;
   const int nin = inputs_per_item(op);
 
   int64_t item_bytes;
-  if (k > 1) {
+  if (two_pass) {
+    item_bytes = int64_t(tpr) * vpt * 16;
+    p->num_items = M;
+  } else if (k > 1) {
     item_bytes = int64_t(tpr) * vpt * 16;
     p->num_items = M;
   } else if (cl > 1) {
@@ -397,7 +426,7 @@ qk_status plan_direct(int dev, const DeviceInfo& d, int op, int dt, int64_t M, i
 }
 
 int64_t max_row_elements(int op, int dt) {
-  if (streams_rows(op)) return INT64_MAX;
+  if (streams_rows(op) || op == kSoftmax || op == kRmsNorm) return INT64_MAX;  // streamed rows
   if (is_bwd(op)) return kMaxRowBytes / 2 / elem_size(dt);  // 512 KiB rows (two inputs)
   return kMaxRowBytes / elem_size(dt);
 }

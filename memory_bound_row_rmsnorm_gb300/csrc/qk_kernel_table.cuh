@@ -10,6 +10,9 @@
 
 #define QK_RING(TH, TPR, VPT, CL) \
   {1, TH, TPR, VPT, CL, reinterpret_cast<const void*>(&row_kernel<QK_OP, QK_T, TH, TPR, VPT, CL>)}
+#define QK_RING2(TH, TPR, VPT, CL)                                                    \
+  {4, TH, TPR, VPT, CL,                                                               \
+   reinterpret_cast<const void*>(&row_kernel<QK_OP, QK_T, TH, TPR, VPT, CL, true>)}
 #define QK_DIRECT(TH, EPT, CL) \
   {2, TH, TH, EPT, CL, reinterpret_cast<const void*>(&direct_kernel<QK_OP, QK_T, TH, EPT, CL>)}
 
@@ -45,6 +48,9 @@ const KernelEntry kTable[] = {
     QK_RING(512, 512, 4, true),
     QK_RING(512, 512, 8, true),
     QK_RING(256, 256, 16, true),
+    // rows longer than a cluster holds: streamed twice in 32 KB chunks
+    QK_RING2(256, 256, 8, false),
+    QK_RING2(256, 256, 8, true),
 #endif
     QK_DIRECT(128, 4, false),
     QK_DIRECT(256, 16, false),

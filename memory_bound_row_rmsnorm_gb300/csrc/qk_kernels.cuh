@@ -67,7 +67,11 @@ __device__ __forceinline__ void merge_partials(const float2* p, int n, float& m,
   }
 }
 
-template <int OP, typename T, int THREADS, int TPR, int VPT, bool CLUSTER>
+// TWO_PASS (softmax, RMSNorm rows longer than a cluster holds): every row
+// slice is streamed through the ring twice in chunks -- the first pass
+// accumulates the reduction, the second re-reads each chunk and writes its
+// outputs with the row's totals (three HBM passes instead of two).
+template <int OP, typename T, int THREADS, int TPR, int VPT, bool CLUSTER, bool TWO_PASS = false>
 __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   using V = Vec16<T>;
   constexpr int E = V::kElems;       // elements per 16-byte vector
@@ -80,6 +84,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
                 "a row group is whole warps or a power-of-two part of one");
   static_assert(!CLUSTER || TPR == THREADS, "a clustered row spans the whole CTA");
   static_assert(NW <= 16, "block-reduction buffer holds 16 warps");
+  static_assert(!TWO_PASS || (TPR == THREADS && OP != kXent), "two passes: one row per CTA");
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);                  // [kMaxSlots]
@@ -95,7 +100,9 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   const int64_t M = a.M, N = a.N;
   const int64_t NV = N / E;  // vectors per row
   const int S = a.slots;
-  const int64_t K = a.chunks;
+  const int64_t K = a.chunks;              // chunks per row slice
+  const int64_t KK = TWO_PASS ? 2 * K : K;  // ring steps per work item
+  constexpr bool kChunked = TWO_PASS;        // slices stream in chunks (also when K > 1)
 
   uint32_t C = 1, rank = 0, cid = blockIdx.x, ncl = gridDim.x;
   if constexpr (CLUSTER) {
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
 
   // Local steps: item i of this cluster is cid + i * ncl; each item has K chunks.
   const int64_t n_local = a.num_items > int64_t(cid) ? (a.num_items - 1 - cid) / ncl + 1 : 0;
-  const int64_t q_total = n_local * K;
+  const int64_t q_total = n_local * KK;
 
   const uint32_t full0 = smem_addr(full), xbar0 = smem_addr(xbar), ring0 = smem_addr(ring);
   const unsigned char* xg = static_cast<const unsigned char*>(a.x);
@@ -140,10 +147,12 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   int p_chunk = 0, p_slot = 0;
   auto issue_next = [&]() {
     int64_t off, bytes;
-    if (K > 1) {  // one chunk of a streamed row
-      const int64_t c0 = int64_t(p_chunk) * CH;
-      off = (p_item * NV + c0) * 16;
-      bytes = min(CH, NV - c0) * 16;
+    if (K > 1 || kChunked) {  // one chunk of this CTA's slice of a streamed row
+      const int64_t c0 = int64_t(p_chunk >= K ? p_chunk - K : p_chunk) * CH;  // 2nd pass: same chunks
+      off = (p_item * NV + v0 + c0) * 16;
+      // K is sized for the longest slice; the last CTA's slice may be shorter,
+      // so its last chunks can be empty (then the barrier just completes).
+      bytes = max(int64_t(0), min(CH, nv - c0)) * 16;
     } else if (CLUSTER) {  // this CTA's slice of one row
       off = (p_item * NV + v0) * 16;
       bytes = nv * 16;
@@ -159,7 +168,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       bulk_copy_g2s(dst + uint32_t(o), xg + off + o, uint32_t(min(kCopyBytes, bytes - o)), bar,
                     policy);
     if (++p_slot == S) p_slot = 0;
-    if (++p_chunk == K) {
+    if (++p_chunk == KK) {
       p_chunk = 0;
       p_item += ncl;
     }
@@ -174,7 +183,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   // of w is loaded once into registers -- unless that would take more than
   // 8 vectors of registers, in which case the finish re-reads it through L1
   // (the slice a CTA needs stays cached there; HBM sees w once).
-  constexpr bool kWeightInRegs = VPT <= 8;
+  constexpr bool kWeightInRegs = VPT <= 8 && !TWO_PASS;  // two passes: columns change per chunk
   uint4 wv[kWeightInRegs ? VPT : 1];
   const uint4* wg = static_cast<const uint4*>(a.w) + v0;
   if constexpr (OP == kRmsNorm && kWeightInRegs) {
@@ -193,7 +202,9 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   constexpr bool kKeepExp = !(E == 8 && (VPT >= 16 || (CLUSTER && VPT >= 8)));
   uint4 xr[VPT];                       // raw input vectors of the current row (chunk)
   float ef[kKeepExp ? VPT * E : 1];    // softmax: exp(x - thread max)
-  float run_m = kNegInf, run_s = 0.f;  // cross-entropy: running pair over chunks
+  float run_m = kNegInf, run_s = 0.f;  // cross-entropy, two-pass softmax: running pair
+  float run_ss = 0.f;                  // two-pass RMSNorm: running sum of squares
+  float tot_a = 0.f, tot_b = 0.f;      // two-pass: the row's totals for the second pass
   float xt = 0.f;                      // cross-entropy: x[target] if this thread holds it
   bool own_t = false;
   int64_t trow = -1;
@@ -216,11 +227,15 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       failed = true;
     }
 
-    const bool single = (K > 1) || CLUSTER;  // one row per item
+    const bool single = (K > 1) || CLUSTER || kChunked;  // one row per item
     const int64_t row = single ? item : item * R + g;
     const bool row_ok = row < M;
-    const int cn = int((K > 1) ? min(CH, NV - int64_t(j) * CH) : nv);  // vectors of this row in the slot
-    const int64_t cbase = (K > 1) ? int64_t(j) * CH : v0;               // first column vector in the slot
+    const bool second = TWO_PASS && j >= K;  // second pass over the row: write outputs
+    const int64_t chunk = second ? j - K : j;
+    const bool chunked = (K > 1) || kChunked;
+    // vectors of this row in the slot (0 for an empty trailing chunk of a short slice)
+    const int cn = int(chunked ? max(int64_t(0), min(CH, nv - chunk * CH)) : nv);
+    const int64_t cbase = chunked ? v0 + chunk * CH : v0;  // first column vector in the slot
     const unsigned char* sb =
         ring + size_t(slot) * a.slot_bytes + (single ? size_t(0) : size_t(g) * size_t(NV) * 16);
 
@@ -240,7 +255,23 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     // ---- thread-level reduction (registers) ----
     float pm = kNegInf, ps = 0.f;  // partial (max, sum-exp), or (-, sum of squares)
     float tm = kNegInf;            // softmax: this thread's own maximum
-    if constexpr (OP == kRmsNorm) {
+    if (second) {
+      // two-pass, second pass: nothing to reduce
+    } else if constexpr (OP == kRmsNorm && TWO_PASS) {
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        float f[E];
+        V::unpack(xr[k], f);
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          const float2 v = make_float2(f[e], f[e + 1]);
+          acc = fma2(v, v, acc);
+        }
+      }
+      run_ss = (j == 0 ? 0.f : run_ss) + (acc.x + acc.y);
+      ps = run_ss;
+    } else if constexpr (OP == kRmsNorm) {
       float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -254,6 +285,12 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       }
       ps = acc.x + acc.y;
     } else {
+      if constexpr (TWO_PASS) {
+        if (j == 0) {
+          run_m = kNegInf;
+          run_s = 0.f;
+        }
+      }
       if constexpr (OP == kXent) {
         if (j == 0) {
           run_m = kNegInf;
@@ -280,7 +317,9 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
           }
         }
       }
-      float m = (OP == kXent) ? run_m : kNegInf;
+      // Streamed pairs start from the running maximum, so a chunk with no
+      // elements for this thread leaves the pair unchanged.
+      float m = (OP == kXent || TWO_PASS) ? run_m : kNegInf;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) m = V::max_into(m, xr[k]);
       const float mb = (m == kNegInf) ? 0.f : m * kLog2e;
@@ -294,14 +333,14 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         for (int e = 0; e < E; e += 2) {
           const float2 t = fma2(make_float2(f[e], f[e + 1]), l2e, nmb);
           const float2 ev = make_float2(exp2_approx(t.x), exp2_approx(t.y));  // padding: 2^-inf = 0
-          if constexpr (OP == kSoftmax && kKeepExp) {
+          if constexpr (OP == kSoftmax && kKeepExp && !TWO_PASS) {
             ef[k * E + e] = ev.x;
             ef[k * E + e + 1] = ev.y;
           }
           acc = add2(acc, ev);
         }
       }
-      if constexpr (OP == kSoftmax) {
+      if constexpr (OP == kSoftmax && !TWO_PASS) {
         tm = m;
         pm = m;
         ps = acc.x + acc.y;
@@ -314,7 +353,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     }
 
     // ---- warp butterfly; warp partials to the block buffer ----
-    const bool row_end = (j == K - 1);
+    const bool row_end = (j == K - 1);  // the row's reduction is complete (first pass)
     if (row_end) {
       warp_reduce<OP, GW>(pm, ps);
       if (WPG > 1 && lane == 0) red[ibit * 16 + warp] = make_float2(pm, ps);
@@ -328,22 +367,58 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     }
     if (tid == 0 && p_left > 0) issue_next();
     // advance the consumer position to step q + 1
-    const int64_t row_item = item;
     const uint32_t row_ibit = ibit, row_xphase = xphase;
     if (++slot == S) {
       slot = 0;
       phase ^= 1u;
     }
     if (row_end) {
-      j = 0;
-      item += ncl;
       xphase ^= ibit;  // the cluster barrier of buffer b flips every second item
       ibit ^= 1u;
+    }
+    if (j == KK - 1) {
+      j = 0;
+      item += ncl;
     } else {
       ++j;
+    }
+    if (!row_end) {
+      if constexpr (TWO_PASS) {
+        if (second && row_ok) {  // write this chunk's outputs with the row's totals
+          uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
+          const uint4* wg2 = static_cast<const uint4*>(a.w) + cbase;
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            if (!valid[k]) continue;
+            float f[E], o[E];
+            V::unpack_fresh(xr[k], f);
+            if constexpr (OP == kSoftmax) {  // exp(x - M) / S
+#pragma unroll
+              for (int e = 0; e < E; e += 2) {
+                const float2 t = fma2(make_float2(f[e], f[e + 1]), make_float2(kLog2e, kLog2e),
+                                      make_float2(-tot_a, -tot_a));
+                const float2 v = mul2(make_float2(exp2_approx(t.x), exp2_approx(t.y)),
+                                      make_float2(tot_b, tot_b));
+                o[e] = v.x;
+                o[e + 1] = v.y;
+              }
+            } else {  // (x * rstd) * w
+              float w[E];
+              V::unpack(__ldg(wg2 + l + k * TPR), w);
+#pragma unroll
+              for (int e = 0; e < E; e += 2) {
+                const float2 v = mul2(mul2(make_float2(f[e], f[e + 1]), make_float2(tot_a, tot_a)),
+                                      make_float2(w[e], w[e + 1]));
+                o[e] = v.x;
+                o[e + 1] = v.y;
+              }
+            }
+            yg[l + k * TPR] = V::pack(o);
+          }
+        }
+      }
       continue;
     }
-    (void)row_item;
 
     // ---- block reduction over the warps of this row group ----
     if constexpr (WPG > 1) merge_partials<OP>(red + row_ibit * 16 + g * WPG, WPG, pm, ps);
@@ -362,6 +437,17 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         failed = true;
       }
       merge_partials<OP>(xbuf + b * kMaxCluster, int(C), pm, ps);
+    }
+
+    if constexpr (TWO_PASS) {  // keep the totals for the second pass
+      if constexpr (OP == kSoftmax) {
+        tot_a = (pm == kNegInf) ? 0.f : pm * kLog2e;  // M log2 e
+        tot_b = __fdividef(1.f, ps);                  // 1 / S
+      } else {
+        tot_a = rsqrtf(fmaf(ps, a.inv_n, a.eps));     // rstd
+        if (l == 0 && rank == 0 && row_ok && a.rstd != nullptr) a.rstd[row] = tot_a;
+      }
+      continue;
     }
 
     // ---- finish: outputs from registers, each stored once ----

@@ -111,25 +111,69 @@ def test_shapes(op, dtype, N):
     full_check(op, dtype, _rows_for(N), N, seed=100 + N)
 
 
-@pytest.mark.parametrize("N", [65536, 131072, 262144, 524288, 262148, 300001])
+@pytest.mark.parametrize("N", [65536, 131072, 262144, 524288, 262148, 300001, 1048576])
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("op", OPS)
 def test_long_rows(op, dtype, N):
-    if op != "xent" and N > qb.qk_max_row_elements(OP_CODE[op], DT_CODE[dtype]):
-        pytest.skip("longer than the operator supports for this dtype")
+    """Clustered rows up to 1 MiB, streamed-twice rows beyond it, masked long rows."""
     full_check(op, dtype, 3, N, seed=200 + N)
 
 
+@pytest.mark.parametrize("M", [1, 5, 400])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm"])
+def test_rows_beyond_a_cluster(op, M):
+    """Rows beyond 1 MiB take two passes: split over a cluster when there are
+    few rows, one CTA per row when there are many."""
+    N = 3 * 2 ** 19 if M <= 5 else 2 ** 18 + 4096
+    got = qb.qk_get_plan(OP_CODE[op], qb.QK_F32, M, N)
+    assert got["path"] == 4
+    inp = syn.make_inputs(op, "f32", M, N, 250 + M, "cpu")
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    out = run_gpu(op, dev, "f32")
+    rows = None if M <= 5 else torch.tensor([0, 1, 199, 398, 399])
+    check_against_oracle(op, "f32", inp, out, rows=rows, what=f"two-pass {M}x{N}")
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("op", OPS)
-def test_rows_beyond_limit_are_refused(op, dtype):
-    if op == "xent":
-        pytest.skip("cross-entropy streams rows of any length")
-    N = qb.qk_max_row_elements(OP_CODE[op], DT_CODE[dtype]) + 8
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm"])
+def test_unaligned_rows_beyond_limit_are_refused(op, dtype):
+    """The masked path (unaligned rows) holds rows of up to 524,288 elements."""
+    N = 524288 + 3
     x = torch.empty((1, N), dtype=syn.DTYPES[dtype], device=DEV)
     with pytest.raises(qb.QkError) as e:
-        qb.qk_softmax_fwd(x, x, 1, N, DT_CODE[dtype])
+        if op == "softmax":
+            qb.qk_softmax_fwd(x, x, 1, N, DT_CODE[dtype])
+        else:
+            w = torch.empty(N, dtype=syn.DTYPES[dtype], device=DEV)
+            qb.qk_rmsnorm_fwd(x, w, x, None, 1, N, 1e-6, DT_CODE[dtype])
     assert e.value.status == qb.QK_ERR_UNSUPPORTED
+
+
+# Forced two-pass plans on moderate rows: several chunks per slice, ring reuse,
+# clusters splitting the row, ragged last chunk and a short last slice.
+TWO_PASS_PLANS = [
+    dict(path=4, threads=256, row_threads=256, vec_per_thread=8, cluster=1, slots=2, grid=3),
+    dict(path=4, threads=256, row_threads=256, vec_per_thread=8, cluster=1, slots=3, grid=16),
+    dict(path=4, threads=256, row_threads=256, vec_per_thread=8, cluster=4, slots=2, grid=8),
+    dict(path=4, threads=256, row_threads=256, vec_per_thread=8, cluster=16, slots=3, grid=16),
+]
+
+
+@pytest.mark.parametrize("pi", range(len(TWO_PASS_PLANS)))
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm"])
+def test_forced_two_pass(op, dtype, pi):
+    plan = TWO_PASS_PLANS[pi]
+    E = 4 if dtype == "f32" else 8
+    N = (5 * 2048 * plan["cluster"] + 37) * E  # about 5 chunks per slice, ragged
+    M = 7
+    qb.qk_set_plan_override(OP_CODE[op], DT_CODE[dtype], plan)
+    try:
+        got = qb.qk_get_plan(OP_CODE[op], DT_CODE[dtype], M, N)
+        assert got["path"] == 4 and got["cluster"] == plan["cluster"] and got["chunks"] >= 5
+        full_check(op, dtype, M, N, seed=260 + pi, what=f"two-pass plan {plan}")
+    finally:
+        qb.qk_set_plan_override(OP_CODE[op], DT_CODE[dtype], None)
 
 
 # Forced plans: tiny grids make every CTA walk many items, so each ring slot is
