@@ -428,12 +428,14 @@ def run_sweep(args, path):
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream(dev)
     peak, peak_src = measured_peak()
+    sweep_m = [int(v) for v in args.sweep_m.split(",")] if args.sweep_m else list(syn.SWEEP_M)
+    sweep_n = [int(v) for v in args.sweep_n.split(",")] if args.sweep_n else list(syn.SWEEP_N)
     points = []
     with open(path, "w") as fout:
         for op in args.sweep_ops.split(","):
             for dtype in ("f32", "bf16"):
-                for M in syn.SWEEP_M:
-                    for N in syn.SWEEP_N:
+                for M in sweep_m:
+                    for N in sweep_n:
                         code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
                         if N > qb.qk_max_row_elements(OP_CODES[op], code):
                             continue  # longer rows than this operator takes
@@ -461,7 +463,7 @@ def run_sweep(args, path):
                         points.append(rec)
                         del sets
                         torch.cuda.empty_cache()
-    ge = [p for p in points if p["N"] >= 4096]
+    ge = [p for p in points if p["N"] >= 4096] or points
     print(json.dumps({"sweep": path, "points": len(points), "peak_gbs": peak, "peak_source": peak_src,
                       "min_frac_N_ge_4096": min(p["frac"] for p in ge),
                       "median_frac_N_ge_4096": statistics.median(p["frac"] for p in ge)}))
@@ -482,6 +484,8 @@ def main():
                     help="--impl reference: total CPU time budget of the timed steps")
     ap.add_argument("--sweep-ops", default="softmax,rmsnorm,xent",
                     help="operators of --sweep (also softmax_bwd, rmsnorm_bwd, xent_bwd)")
+    ap.add_argument("--sweep-m", help="comma-separated row counts of --sweep (default: the sweep grid)")
+    ap.add_argument("--sweep-n", help="comma-separated row lengths of --sweep (default: the sweep grid)")
     ap.add_argument("--graph", action="store_true",
                     help="issue the timed steps as one CUDA-graph replay (no host launch overhead)")
     args = ap.parse_args()
