@@ -70,6 +70,8 @@ def bind(path: str):
     lib.oracle_xent_fwd_ex.restype = None
     lib.oracle_xent_bwd_ex.argtypes = [dp, lp, dp, dp, dp, i64, i64, i64, ctypes.c_double]
     lib.oracle_xent_bwd_ex.restype = None
+    lib.oracle_layernorm_fwd.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64, ctypes.c_double]
+    lib.oracle_layernorm_fwd.restype = None
     return lib
 
 
@@ -196,3 +198,20 @@ def xent_bwd_ex(x, target, lse, dloss, ignore_index: int = NO_IGNORE, z: float =
     lib.oracle_xent_bwd_ex(_ptr(x), _ptr(t, ctypes.c_int64), _ptr(lse), _ptr(dloss), _ptr(dx), M, N,
                            int(ignore_index), float(z))
     return dx
+
+
+def layernorm_fwd(x, w, b, eps: float, lib=None):
+    """Row-wise LayerNorm (population variance, eps inside the root); b may be
+    None.  Returns (y, mean, rstd)."""
+    lib = lib or library()
+    x, w = _f64(x), _f64(w)
+    M, N = x.shape
+    bb = None if b is None else _f64(b)
+    if w.shape != (N,) or (bb is not None and bb.shape != (N,)):
+        raise ValueError("w and b must have shape (N,)")
+    y = np.empty_like(x)
+    mean = np.empty(M, dtype=np.float64)
+    rstd = np.empty(M, dtype=np.float64)
+    lib.oracle_layernorm_fwd(_ptr(x), _ptr(w), None if bb is None else _ptr(bb), _ptr(y), _ptr(mean),
+                             _ptr(rstd), M, N, float(eps))
+    return y, mean, rstd

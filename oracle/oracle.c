@@ -244,3 +244,36 @@ void oracle_xent_bwd_ex(const double *x, const int64_t *target, const double *ls
         }
     }
 }
+
+/* ------------------------------------------------------------------------
+ * LayerNorm forward (the article's claim that the same row-reduction template
+ * carries over to other normalisations; LayerNorm itself is not named there).
+ * Per row, with the population variance (divide by N) and eps inside the root:
+ *   mean = (1/N) sum_j x_j,  var = (1/N) sum_j (x_j - mean)^2,
+ *   rstd = 1 / sqrt(var + eps),  y_j = (x_j - mean) * rstd * w_j + b_j
+ * b may be NULL (no bias).  mean and rstd may be NULL.
+ * ------------------------------------------------------------------------ */
+void oracle_layernorm_fwd(const double *x, const double *w, const double *b, double *y,
+                          double *mean, double *rstd, int64_t M, int64_t N, double eps)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        const double *xi = x + i * N;
+        double *yi = y + i * N;
+
+        double sum = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            sum += xi[j];
+        double mu = sum / (double)N;
+
+        double sq = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            sq += (xi[j] - mu) * (xi[j] - mu);
+        double var = sq / (double)N;
+        double r = 1.0 / sqrt(var + eps);
+
+        for (int64_t j = 0; j < N; ++j)
+            yi[j] = (xi[j] - mu) * r * w[j] + (b ? b[j] : 0.0);
+        if (mean) mean[i] = mu;
+        if (rstd) rstd[i] = r;
+    }
+}

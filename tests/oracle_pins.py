@@ -481,4 +481,65 @@ def pin_xent_ex_bwd_finite_differences(lib):
     assert np.all(dx[1] == 0.0), "xent ex bwd: an ignored row has zero gradient"
 
 
+# --------------------------------------------------------------------------
+# LayerNorm
+# --------------------------------------------------------------------------
+def pin_layernorm_closed_form(lib):
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    w = np.array([1.0, 2.0, 0.5, -1.0])
+    b = np.array([0.0, 1.0, -1.0, 0.25])
+    y, mean, rstd = oracle.layernorm_fwd(x, w, b, 0.0, lib)
+    r = 1.0 / math.sqrt(1.25)  # mean 2.5, population variance 1.25
+    want = (np.array([-1.5, -0.5, 0.5, 1.5]) * r) * w + b
+    _close(y, [want], 1e-14, "layernorm: (1,2,3,4) closed form")
+    _close(mean, [2.5], 1e-15, "layernorm: mean")
+    _close(rstd, [r], 1e-14, "layernorm: rstd with the population variance")
+
+
+def pin_layernorm_constant_row_and_no_bias(lib):
+    w = _rng(40).uniform(0.5, 1.5, size=9)
+    b = _rng(41).normal(size=9)
+    y, mean, rstd = oracle.layernorm_fwd(np.full((2, 9), -3.5), w, b, 1e-5, lib)
+    assert np.all(y == b), "layernorm: a constant row maps to the bias"
+    _close(rstd, [1e-5 ** -0.5] * 2, 1e-14, "layernorm: constant row rstd = eps^-1/2")
+    y0, _, _ = oracle.layernorm_fwd(np.full((1, 9), 2.0), w, None, 1e-5, lib)
+    assert np.all(y0 == 0.0), "layernorm: no bias means zero output on a constant row"
+
+
+def pin_layernorm_invariances(lib):
+    rng = _rng(42)
+    x = rng.normal(size=(5, 31))
+    w = rng.uniform(0.5, 1.5, size=31)
+    b = rng.normal(size=31)
+    y0, m0, r0 = oracle.layernorm_fwd(x, w, b, 0.0, lib)
+    y1, m1, r1 = oracle.layernorm_fwd(3.0 * x + 7.25, w, b, 0.0, lib)
+    _close(y1, y0, 1e-12, "layernorm: y(a x + c) = y(x) at eps=0")
+    _close(m1, 3.0 * m0 + 7.25, 1e-13, "layernorm: mean is affine")
+    _close(r1 * 3.0, r0, 1e-13, "layernorm: rstd scales as 1/a")
+    z = (y0 - b) / w
+    assert np.max(np.abs(z.mean(axis=1))) <= 1e-13, "layernorm: normalised rows have zero mean"
+    _close(np.mean(z * z, axis=1), np.ones(5), 1e-13, "layernorm: normalised rows have unit variance")
+
+
+def pin_layernorm_brute_force(lib):
+    rng = _rng(43)
+    x = rng.normal(2.0, 3.0, size=(4, 8))
+    w = rng.uniform(0.5, 1.5, size=8)
+    b = rng.normal(size=8)
+    eps = 1e-3
+    y, mean, rstd = oracle.layernorm_fwd(x, w, b, eps, lib)
+    ys, ms, rs = [], [], []
+    for row in x:
+        d = [Decimal(float(v)) for v in row]
+        mu = sum(d, Decimal(0)) / Decimal(8)
+        var = sum(((v - mu) * (v - mu) for v in d), Decimal(0)) / Decimal(8)
+        r = _CTX.divide(Decimal(1), _CTX.sqrt(var + Decimal(eps)))
+        ys.append([float((v - mu) * r * Decimal(float(wj)) + Decimal(float(bj))) for v, wj, bj in zip(d, w, b)])
+        ms.append(float(mu))
+        rs.append(float(r))
+    _close(y, ys, 1e-13, "layernorm: 4x8 brute force y")
+    _close(mean, ms, 1e-14, "layernorm: 4x8 brute force mean")
+    _close(rstd, rs, 1e-14, "layernorm: 4x8 brute force rstd")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -53,6 +53,11 @@ MUTANTS = [
     ("xent ex bwd: z-loss gradient factor 1 + z lse", "(1.0 + 2.0 * z * lse[i])", "(1.0 + z * lse[i])"),
     ("xent ex bwd: ignored rows not zeroed", "            if (t == ignore_index) {\n                di[j] = 0.0;",
      "            if (t == ignore_index) {\n                di[j] = dloss[i];"),
+    ("layernorm: sample variance", "double var = sq / (double)N;", "double var = sq / (double)(N - 1);"),
+    ("layernorm: mean not subtracted in the variance", "sq += (xi[j] - mu) * (xi[j] - mu);", "sq += xi[j] * xi[j];"),
+    ("layernorm: eps outside the root", "double r = 1.0 / sqrt(var + eps);", "double r = 1.0 / (sqrt(var) + eps);"),
+    ("layernorm: bias dropped", "* w[j] + (b ? b[j] : 0.0);", "* w[j];"),
+    ("layernorm: mean not subtracted in y", "yi[j] = (xi[j] - mu) * r * w[j]", "yi[j] = xi[j] * r * w[j]"),
 ]
 
 
