@@ -47,7 +47,8 @@ METRIC = "effective HBM TB/s and % of GB300 peak per kernel over the M×N sweep"
 ESIZE = {"f32": 4, "bf16": 2}
 DEFAULT_WORKLOAD = "rmsnorm_bf16_16384x4096"
 EPS = 1e-6
-OP_CODES = {"softmax": 0, "rmsnorm": 1, "xent": 2, "softmax_bwd": 3, "rmsnorm_bwd": 4, "xent_bwd": 5}
+OP_CODES = {"softmax": 0, "rmsnorm": 1, "xent": 2, "softmax_bwd": 3, "rmsnorm_bwd": 4, "xent_bwd": 5,
+            "layernorm": 6}
 
 
 def min_bytes(op: str, dtype: str, M: int, N: int) -> int:
@@ -65,6 +66,8 @@ def min_bytes(op: str, dtype: str, M: int, N: int) -> int:
         return 3 * M * N * s + N * s + 4 * M + 4 * N  # x, dy, w, rstd in; dx, dw out
     if op == "xent_bwd":
         return 2 * M * N * s + 16 * M  # logits, targets, lse, dloss in; dlogits out
+    if op == "layernorm":
+        return 2 * M * N * s + 2 * N * s + 8 * M  # x, w, b in; y, mean, rstd out
     raise ValueError(op)
 
 
@@ -203,10 +206,12 @@ def make_set(op, dtype, M, N, sigma, seed, dev):
             out["dw"] = torch.empty(N, dtype=torch.float32, device=dev)
             out["workspace"] = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
         return inp, out
-    if op in ("softmax", "rmsnorm"):
+    if op in ("softmax", "rmsnorm", "layernorm"):
         out["y"] = torch.empty_like(inp["x"])
-    if op == "rmsnorm":
+    if op in ("rmsnorm", "layernorm"):
         out["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
+    if op == "layernorm":
+        out["mean"] = torch.empty(M, dtype=torch.float32, device=dev)
     if op == "xent":
         out["loss"] = torch.empty(M, dtype=torch.float32, device=dev)
         out["lse"] = torch.empty(M, dtype=torch.float32, device=dev)
@@ -227,6 +232,9 @@ def launch(qb, op, dtype, inp, out, M, N, stream):
         qb.qk_softmax_fwd(inp["x"], out["y"], M, N, code, stream)
     elif op == "rmsnorm":
         qb.qk_rmsnorm_fwd(inp["x"], inp["w"], out["y"], out["rstd"], M, N, EPS, code, stream)
+    elif op == "layernorm":
+        qb.qk_layernorm_fwd(inp["x"], inp["w"], inp["b"], out["y"], out["mean"], out["rstd"], M, N,
+                            EPS, code, stream)
     else:
         qb.qk_xent_fwd(inp["x"], inp["targets"], out["loss"], out["lse"], M, N, code, stream)
 
@@ -335,6 +343,8 @@ def oracle_call(oracle, lib, op, d, sl):
         oracle.softmax_bwd(d["y"][sl], d["dy"][sl], lib)
     elif op == "rmsnorm_bwd":
         oracle.rmsnorm_bwd(d["x"][sl], d["w"], d["rstd"][sl], d["dy"][sl], lib)
+    elif op == "layernorm":
+        oracle.layernorm_fwd(d["x"][sl], d["w"], d["b"], EPS, lib)
     else:
         oracle.xent_bwd(d["x"][sl], d["targets"][sl], d["lse"][sl], d["dloss"][sl], lib)
 
@@ -475,7 +485,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(syn.WORKLOADS) + sorted(syn.BWD_WORKLOADS))
+                    choices=sorted(syn.WORKLOADS) + sorted(syn.BWD_WORKLOADS) + sorted(syn.NEXT_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -483,7 +493,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: total CPU time budget of the timed steps")
     ap.add_argument("--sweep-ops", default="softmax,rmsnorm,xent",
-                    help="operators of --sweep (also softmax_bwd, rmsnorm_bwd, xent_bwd)")
+                    help="operators of --sweep (also softmax_bwd, rmsnorm_bwd, xent_bwd, layernorm)")
     ap.add_argument("--sweep-m", help="comma-separated row counts of --sweep (default: the sweep grid)")
     ap.add_argument("--sweep-n", help="comma-separated row lengths of --sweep (default: the sweep grid)")
     ap.add_argument("--graph", action="store_true",
@@ -493,7 +503,7 @@ def main():
     if args.sweep:
         run_sweep(args, args.sweep)
         return
-    op, dtype, M, N, sigma = {**syn.WORKLOADS, **syn.BWD_WORKLOADS}[args.workload]
+    op, dtype, M, N, sigma = {**syn.WORKLOADS, **syn.BWD_WORKLOADS, **syn.NEXT_WORKLOADS}[args.workload]
 
     if args.impl == "reference":
         run_reference(args, op, dtype, M, N, sigma)

@@ -56,14 +56,15 @@ extern "C" {
 typedef enum { QK_F32 = 0, QK_BF16 = 1 } qk_dtype;
 
 /* Operators, as named by qk_get_plan / qk_set_plan_override / qk_max_row_elements:
- * the three forward passes and their backward passes. */
+ * the three forward passes, their backward passes, and LayerNorm forward. */
 typedef enum {
   QK_OP_SOFTMAX = 0,
   QK_OP_RMSNORM = 1,
   QK_OP_XENT = 2,
   QK_OP_SOFTMAX_BWD = 3,
   QK_OP_RMSNORM_BWD = 4,
-  QK_OP_XENT_BWD = 5
+  QK_OP_XENT_BWD = 5,
+  QK_OP_LAYERNORM = 6
 } qk_op;
 
 typedef enum {
@@ -105,6 +106,29 @@ QK_API qk_status qk_softmax_fwd(const void* x, void* y, int64_t M, int64_t N, qk
  */
 QK_API qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M,
                          int64_t N, float eps, qk_dtype dtype, void* stream);
+
+/*
+ * LayerNorm forward.  For each row i, with the population variance:
+ *   mean[i] = (1/N) sum_j x[i,j],  var[i] = (1/N) sum_j (x[i,j] - mean[i])^2,
+ *   rstd[i] = 1 / sqrt(var[i] + eps),  y[i,j] = (x[i,j] - mean[i]) * rstd[i] * w[j] + b[j].
+ * The article names RMSNorm, softmax and cross-entropy only; its section "总结"
+ * says the RMSNorm kernel's layout, copy strategy and reduction helpers carry
+ * over to other row reductions, and LayerNorm is that carry-over with a
+ * (mean, M2) pair reduced instead of a sum of squares.  The pair is merged
+ * with the pairwise form of Welford's update (Chan et al.), so the variance
+ * is not formed as a difference of two large sums.  Each element of x is read
+ * from HBM once.
+ *
+ *   x      [M, N] dtype, read once.
+ *   w      [N] dtype; b [N] dtype or NULL (no bias); both cached on chip.
+ *   y      [M, N] dtype, written once; y == x allowed, other overlaps rejected.
+ *   mean   [M] float32, may be NULL; rstd [M] float32, may be NULL.
+ *   eps    added to the variance; must be finite and >= 0.
+ *   Rows up to qk_max_row_elements(QK_OP_LAYERNORM, dtype) elements (1 MiB).
+ */
+QK_API qk_status qk_layernorm_fwd(const void* x, const void* w, const void* b, void* y,
+                                  float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                                  qk_dtype dtype, void* stream);
 
 /*
  * Cross-entropy loss forward, one value per row (no reduction over rows, no

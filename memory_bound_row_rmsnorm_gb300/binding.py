@@ -5,7 +5,7 @@ converted and passed through; the operators themselves run in the CUDA
 kernels of libqk.so.  A non-OK status raises QkError.  There is no fallback:
 if the library is missing every call raises.
 
-The ``softmax_fwd`` / ``rmsnorm_fwd`` / ``xent_fwd`` helpers at the bottom take
+The ``softmax_fwd`` / ``rmsnorm_fwd`` / ``layernorm_fwd`` / ``xent_fwd`` helpers take
 and return CUDA tensors (they allocate the outputs with PyTorch and then call
 the C entry points).
 """
@@ -21,6 +21,7 @@ LIBRARY = os.path.join(_HERE, "_lib", "libqk.so")
 QK_F32, QK_BF16 = 0, 1
 QK_OP_SOFTMAX, QK_OP_RMSNORM, QK_OP_XENT = 0, 1, 2
 QK_OP_SOFTMAX_BWD, QK_OP_RMSNORM_BWD, QK_OP_XENT_BWD = 3, 4, 5
+QK_OP_LAYERNORM = 6
 QK_OK = 0
 QK_ERR_INVALID_ARG = 1
 QK_ERR_UNSUPPORTED = 2
@@ -34,7 +35,7 @@ _EXPORTS = (
     "qk_get_device_status", "qk_max_row_elements", "qk_get_plan",
     "qk_set_plan_override", "qk_test_wait_timeout", "qk_softmax_bwd", "qk_rmsnorm_bwd",
     "qk_rmsnorm_bwd_workspace_size", "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc",
-    "qk_xent_fwd_ex", "qk_xent_bwd_ex",
+    "qk_xent_fwd_ex", "qk_xent_bwd_ex", "qk_layernorm_fwd",
 )
 QK_NO_IGNORE_INDEX = -(2 ** 63)
 
@@ -94,10 +95,12 @@ def load_library(path: str = LIBRARY):
         op = ctypes.POINTER(qk_xent_options)
         lib.qk_xent_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, op, vp]
         lib.qk_xent_bwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, op, vp]
+        lib.qk_layernorm_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, ctypes.c_float, i32, vp]
         for name in ("qk_softmax_fwd", "qk_rmsnorm_fwd", "qk_xent_fwd", "qk_get_device_status",
                      "qk_get_plan", "qk_set_plan_override", "qk_test_wait_timeout",
                      "qk_softmax_bwd", "qk_rmsnorm_bwd_workspace_size", "qk_rmsnorm_bwd",
-                     "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc", "qk_xent_fwd_ex", "qk_xent_bwd_ex"):
+                     "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc", "qk_xent_fwd_ex", "qk_xent_bwd_ex",
+                     "qk_layernorm_fwd"):
             getattr(lib, name).restype = i32
         del fp
         _lib = lib
@@ -140,6 +143,13 @@ def qk_softmax_fwd(x, y, M: int, N: int, dtype: int, stream=None) -> None:
 def qk_rmsnorm_fwd(x, w, y, rstd, M: int, N: int, eps: float, dtype: int, stream=None) -> None:
     _check(load_library().qk_rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), M, N, eps, dtype,
                                          _stream(stream)), "qk_rmsnorm_fwd")
+
+
+def qk_layernorm_fwd(x, w, b, y, mean, rstd, M: int, N: int, eps: float, dtype: int,
+                     stream=None) -> None:
+    _check(load_library().qk_layernorm_fwd(_ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(mean),
+                                           _ptr(rstd), M, N, eps, dtype, _stream(stream)),
+           "qk_layernorm_fwd")
 
 
 def qk_xent_fwd(logits, targets, loss, lse, M: int, N: int, dtype: int, stream=None) -> None:
@@ -270,6 +280,24 @@ def rmsnorm_fwd(x, w, eps: float = 1e-6, out=None, want_rstd: bool = True, strea
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if want_rstd else None
     qk_rmsnorm_fwd(x, w, y, rstd, M, N, eps, _dtype_code(x), stream)
     return y, rstd
+
+
+def layernorm_fwd(x, w, b=None, eps: float = 1e-5, out=None, want_stats: bool = True,
+                  stream=None):
+    """LayerNorm over the last dimension; returns (y, mean, rstd) (the two
+    statistics are None if not wanted).  b may be None (no bias)."""
+    import torch
+    M, N = _rows(x)
+    for name, t in (("w", w), ("b", b)):
+        if t is not None and (t.dtype != x.dtype or t.numel() != N or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous [N] tensor of x's dtype")
+    y = torch.empty_like(x) if out is None else out
+    mean = rstd = None
+    if want_stats:
+        mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    qk_layernorm_fwd(x, w, b, y, mean, rstd, M, N, eps, _dtype_code(x), stream)
+    return y, mean, rstd
 
 
 def xent_fwd(logits, targets, want_lse: bool = True, ignore_index=None, z_loss: float = 0.0,

@@ -59,13 +59,15 @@ struct Override {
   bool on = false;
   qk_plan plan{};
 };
-constexpr int kNumOps = 6;  // forward: softmax, RMSNorm, x-entropy; then their backward passes
+constexpr int kNumOps = 7;  // softmax, RMSNorm, x-entropy; their backward passes; LayerNorm
 Override g_override[kNumOps][2];
 std::atomic<uint64_t> g_override_gen{1};  // bumped by every qk_set_plan_override
 
-// Backward operator codes of the ABI (qk_op 3, 4, 5).
-constexpr int kOpSoftmaxBwd = 3, kOpRmsNormBwd = 4, kOpXentBwd = 5;
-bool is_bwd(int op) { return op >= kOpSoftmaxBwd; }
+// Operator codes of the ABI (qk_op): the forward passes 0-2 match the kernels'
+// Op values; the backward passes are 3-5 and LayerNorm (kernel Op kLayerNorm)
+// is 6.
+constexpr int kOpSoftmaxBwd = 3, kOpRmsNormBwd = 4, kOpXentBwd = 5, kOpLayerNorm = 6;
+bool is_bwd(int op) { return op >= kOpSoftmaxBwd && op <= kOpXentBwd; }
 // Input matrices one work item loads (both y/x and dy for two backward passes).
 int inputs_per_item(int op) { return (op == kOpSoftmaxBwd || op == kOpRmsNormBwd) ? 2 : 1; }
 bool streams_rows(int op) { return op == kXent || op == kOpXentBwd; }
@@ -83,7 +85,9 @@ KernelTable table_for(int op, int dt) {
     case 8: return bwd_kernels_rmsnorm_f32();
     case 9: return bwd_kernels_rmsnorm_bf16();
     case 10: return bwd_kernels_xent_f32();
-    default: return bwd_kernels_xent_bf16();
+    case 11: return bwd_kernels_xent_bf16();
+    case 12: return kernels_layernorm_f32();
+    default: return kernels_layernorm_bf16();
   }
 }
 
@@ -238,6 +242,15 @@ const Choice kRmsNormTable[] = {
     {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 8, 8, 3},  {32768, 256, 256, 8, 16, 2},  {65536, 512, 512, 8, 16, 2},
 };
+// LayerNorm: from a sweep of every compiled configuration on GB300 (M = 16384,
+// N = 256 ... 262144, fp32 and bf16).  Its parameters not held in registers
+// take shared memory, so long rows keep fewer ring slots than RMSNorm.
+const Choice kLayerNormTable[] = {
+    {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 2},       {128, 256, 32, 4, 1, 2},
+    {256, 256, 32, 8, 1, 3},     {512, 128, 128, 4, 1, 2},     {1024, 128, 128, 8, 1, 1},
+    {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {16384, 256, 256, 8, 8, 2},  {32768, 512, 512, 8, 8, 1},   {65536, 512, 512, 8, 16, 2},
+};
 const Choice kSoftmaxTable[] = {
     {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 2},       {128, 256, 32, 4, 1, 2},
     {256, 256, 64, 4, 1, 2},     {512, 256, 128, 4, 1, 1},     {1024, 256, 256, 4, 1, 1},
@@ -282,6 +295,7 @@ qk_status choose_ring(int op, int64_t NV, int* th, int* tpr, int* vpt, int* cl, 
     case kXent: QK_TABLE(kXentTable); break;
     case kOpSoftmaxBwd: QK_TABLE(kSoftmaxBwdTable); break;
     case kOpRmsNormBwd: QK_TABLE(kRmsNormBwdTable); break;
+    case kOpLayerNorm: QK_TABLE(kLayerNormTable); break;
     default: QK_TABLE(kXentBwdTable); break;
   }
 #undef QK_TABLE
@@ -366,10 +380,18 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
     p->num_items = (M + R - 1) / R;
   }
   const uint32_t slot_bytes = uint32_t((item_bytes + 127) / 128 * 128);
+  // LayerNorm parameters not held in registers sit after the ring slots.
+  int64_t param_bytes = 0;
+  if (op == kOpLayerNorm) {
+    const int64_t slice = cl > 1 ? (NV + cl - 1) / cl : NV;
+    if (vpt > kAffineRegsMaxVpt) param_bytes += param_slice_bytes(slice);
+    if (vpt > kLnBiasRegsMaxVpt) param_bytes += param_slice_bytes(slice);
+  }
   if (slots <= 0) slots = 2;  // an override without a slot count
   slots = std::min(slots, kMaxSlots);
-  while (slots > 1 && kSmemHeader + int64_t(slots) * nin * slot_bytes > d.smem_optin) --slots;
-  const int64_t smem = kSmemHeader + int64_t(slots) * nin * slot_bytes;
+  while (slots > 1 && kSmemHeader + int64_t(slots) * nin * slot_bytes + param_bytes > d.smem_optin)
+    --slots;
+  const int64_t smem = kSmemHeader + int64_t(slots) * nin * slot_bytes + param_bytes;
   if (smem > d.smem_optin) return QK_ERR_UNSUPPORTED;
 
   qk_status st = prepare_kernel(dev, d, *ke);
@@ -491,8 +513,8 @@ qk_status run(int op, int dt, RowArgs a, bool fast, void* stream) {
     uint64_t gen = 0;
     Plan plan;
   };
-  thread_local Cached cache[3][2][2];
-  Cached& c = cache[op][dt][fast ? 1 : 0];
+  thread_local Cached cache[4][2][2];  // softmax, RMSNorm, x-entropy, LayerNorm
+  Cached& c = cache[op == kOpLayerNorm ? 3 : op][dt][fast ? 1 : 0];
   const uint64_t gen = g_override_gen.load(std::memory_order_acquire);
   if (!(c.dev == dev && c.M == a.M && c.N == a.N && c.gen == gen)) {
     Plan np;
@@ -647,6 +669,43 @@ qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int
   const bool fast =
       aligned16(x) && aligned16(y) && aligned16(w) && (N * int64_t(es)) % 16 == 0;
   return run(kRmsNorm, dtype, a, fast, stream);
+}
+
+qk_status qk_layernorm_fwd(const void* x, const void* w, const void* b, void* y, float* mean,
+                           float* rstd, int64_t M, int64_t N, float eps, qk_dtype dtype,
+                           void* stream) {
+  qk_status st = check_sizes(kOpLayerNorm, dtype, M, N);
+  if (st != QK_OK) return st;
+  if (!(std::isfinite(eps) && eps >= 0.f)) return QK_ERR_INVALID_ARG;
+  if (M == 0) return QK_OK;
+  if (x == nullptr || w == nullptr || y == nullptr) return QK_ERR_INVALID_ARG;
+  const size_t es = size_t(elem_size(dtype));
+  if (!aligned_to(x, es) || !aligned_to(y, es) || !aligned_to(w, es) || !aligned_to(b, es) ||
+      !aligned_to(mean, 4) || !aligned_to(rstd, 4))
+    return QK_ERR_MISALIGNED;
+  const int64_t bytes = M * N * int64_t(es), wbytes = N * int64_t(es), rbytes = M * 4;
+  if ((x != y && overlap(x, bytes, y, bytes)) || overlap(y, bytes, w, wbytes) ||
+      overlap(y, bytes, b, wbytes))
+    return QK_ERR_INVALID_ARG;
+  for (const float* o : {mean, rstd}) {  // the per-row outputs overlap nothing
+    if (overlap(o, rbytes, x, bytes) || overlap(o, rbytes, y, bytes) ||
+        overlap(o, rbytes, w, wbytes) || overlap(o, rbytes, b, wbytes))
+      return QK_ERR_INVALID_ARG;
+  }
+  if (overlap(mean, rbytes, rstd, rbytes)) return QK_ERR_INVALID_ARG;
+  RowArgs a = {};
+  a.x = x;
+  a.w = w;
+  a.bias = b;
+  a.y = y;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.M = M;
+  a.N = N;
+  a.eps = eps;
+  const bool fast = aligned16(x) && aligned16(y) && aligned16(w) && aligned16(b) &&
+                    (N * int64_t(es)) % 16 == 0;
+  return run(kOpLayerNorm, dtype, a, fast, stream);
 }
 
 qk_status qk_xent_fwd_ex(const void* logits, const int64_t* targets, float* loss, float* lse,

@@ -245,6 +245,89 @@ __device__ __forceinline__ void group_ms(float& m, float& s) {
   m = mg;
 }
 
+// (count, mean, M2) of a set of values, merged pairwise (the parallel form of
+// Welford's update, Chan et al.): with a the side with more values and
+// d = mean_b - mean_a,
+//   n = n_a + n_b,  mean = mean_a + d n_b / n,  M2 = M2_a + M2_b + d^2 n_a n_b / n.
+// With equal counts this is mean = (mean_a + mean_b) / 2 and
+// M2 = M2_a + M2_b + d^2 n_a / 2, which needs no division; otherwise 1/n is
+// one approximate reciprocal (a relative error of an ulp or two in the update
+// terms).  Both forms leave the mean exact when the two means are equal.
+// Every product and sum is rounded explicitly and the result does not depend
+// on the argument order, so merge(a, b) == merge(b, a) bit for bit (butterfly
+// lanes agree).  An empty side leaves the other one unchanged.
+__device__ __forceinline__ void welford_merge_equal(float& mean, float& m2, float n, float mean2,
+                                                    float m22) {
+  const float d = __fsub_rn(mean2, mean);
+  mean = __fmul_rn(__fadd_rn(mean, mean2), 0.5f);
+  m2 = __fadd_rn(__fadd_rn(m2, m22), __fmul_rn(__fmul_rn(d, d), __fmul_rn(n, 0.5f)));
+}
+__device__ __forceinline__ void welford_merge(float& n, float& mean, float& m2, float n2,
+                                              float mean2, float m22) {
+  if (n2 == 0.f) return;
+  if (n == 0.f) {
+    n = n2;
+    mean = mean2;
+    m2 = m22;
+    return;
+  }
+  if (n == n2) {
+    welford_merge_equal(mean, m2, n, mean2, m22);
+    n = __fadd_rn(n, n);
+    return;
+  }
+  const bool a_first = n > n2;  // the same choice from either side
+  const float na = a_first ? n : n2, ma = a_first ? mean : mean2;
+  const float nb = a_first ? n2 : n, mb = a_first ? mean2 : mean;
+  const float nt = __fadd_rn(na, nb);
+  const float rn = __fdividef(1.f, nt);
+  const float d = __fsub_rn(mb, ma);
+  mean = __fadd_rn(ma, __fmul_rn(d, __fmul_rn(nb, rn)));
+  m2 = __fadd_rn(__fadd_rn(m2, m22), __fmul_rn(__fmul_rn(d, d), __fmul_rn(__fmul_rn(na, nb), rn)));
+  n = nt;
+}
+// Butterfly over WIDTH lanes (a power of two): every lane ends with the merge
+// of all WIDTH partials.  Lanes with n = 0 are neutral.
+template <int WIDTH = 32>
+__device__ __forceinline__ void group_welford(float& n, float& mean, float& m2) {
+#pragma unroll
+  for (int o = WIDTH / 2; o > 0; o >>= 1) {
+    const float n2 = __shfl_xor_sync(0xffffffffu, n, o);
+    const float mean2 = __shfl_xor_sync(0xffffffffu, mean, o);
+    const float m22 = __shfl_xor_sync(0xffffffffu, m2, o);
+    welford_merge(n, mean, m2, n2, mean2, m22);
+  }
+}
+// Sum form of the equal-count butterfly, for counts that are powers of two:
+// lanes carry (S = n mean, M2) and each side of a merge holds n values, so
+//   S = S_a + S_b,  M2 = M2_a + M2_b + (S_b - S_a)^2 / (2 n),
+// which is the equal-count merge above scaled by n (exact for a power of
+// two).  N0 is every lane's count before the first level; 1/(2n) folds to a
+// constant at each level.
+template <int WIDTH, int N0>
+__device__ __forceinline__ void group_welford_sum(float& s, float& m2) {
+#pragma unroll
+  for (int o = WIDTH / 2, n = N0; o > 0; o >>= 1, n *= 2) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float q2 = __shfl_xor_sync(0xffffffffu, m2, o);
+    const float d = __fsub_rn(s2, s);
+    s = __fadd_rn(s, s2);
+    m2 = __fmaf_rn(__fmul_rn(d, d), 0.5f / float(n), __fadd_rn(m2, q2));
+  }
+}
+// The same when every lane's count is n (it doubles at each level): no
+// counts travel and no branch is taken.
+template <int WIDTH = 32>
+__device__ __forceinline__ void group_welford_equal(float& n, float& mean, float& m2) {
+#pragma unroll
+  for (int o = WIDTH / 2; o > 0; o >>= 1) {
+    const float mean2 = __shfl_xor_sync(0xffffffffu, mean, o);
+    const float m22 = __shfl_xor_sync(0xffffffffu, m2, o);
+    welford_merge_equal(mean, m2, n, mean2, m22);
+    n = __fadd_rn(n, n);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 16-byte vectors of fp32 (4 elements) or bf16 (8 elements)
 // ---------------------------------------------------------------------------

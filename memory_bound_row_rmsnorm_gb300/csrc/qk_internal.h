@@ -5,15 +5,18 @@
 
 namespace qk {
 
-enum Op : int { kSoftmax = 0, kRmsNorm = 1, kXent = 2 };
+// Kernel-side operator codes (the ABI numbers LayerNorm 6; see qk_api.cu).
+enum Op : int { kSoftmax = 0, kRmsNorm = 1, kXent = 2, kLayerNorm = 3 };
 enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Everything a row kernel needs, passed by value as its only parameter.
 struct RowArgs {
   const void* x;          // [M, N] input rows (logits for cross-entropy)
   void* y;                // [M, N] output rows (softmax, RMSNorm)
-  const void* w;          // [N] RMSNorm weight
-  float* rstd;            // [M] RMSNorm 1/rms, may be null
+  const void* w;          // [N] RMSNorm / LayerNorm weight
+  const void* bias;       // [N] LayerNorm bias, may be null
+  float* rstd;            // [M] RMSNorm 1/rms or LayerNorm 1/std, may be null
+  float* mean;            // [M] LayerNorm row mean, may be null
   const int64_t* target;  // [M] cross-entropy targets
   float* loss;            // [M] cross-entropy loss
   float* lse;             // [M] cross-entropy log-sum-exp, may be null
@@ -35,6 +38,17 @@ struct RowArgs {
 // the block-reduction buffer and the cluster exchange buffer.
 constexpr int kSmemHeader = 1024;
 constexpr int kMaxSlots = 32;
+// Per-column parameters of the ring kernels: RMSNorm / LayerNorm keep their
+// share of w in registers up to kAffineRegsMaxVpt vectors a thread, LayerNorm
+// its share of b up to kLnBiasRegsMaxVpt.  Beyond that LayerNorm stages the
+// CTA's slice of the parameter in shared memory once, after the ring slots
+// (w first, then b, each param_slice_bytes long); the planner sizes the
+// shared memory with the same rule.
+constexpr int kAffineRegsMaxVpt = 8;
+constexpr int kLnBiasRegsMaxVpt = 4;
+__host__ __device__ constexpr int64_t param_slice_bytes(int64_t slice_vectors) {
+  return (slice_vectors * 16 + 127) / 128 * 128;
+}
 constexpr int kMaxCluster = 16;
 
 // One compiled kernel.  `path` 1: TMA ring kernel (threads, row_threads,
@@ -62,6 +76,8 @@ KernelTable kernels_rmsnorm_f32();
 KernelTable kernels_rmsnorm_bf16();
 KernelTable kernels_xent_f32();
 KernelTable kernels_xent_bf16();
+KernelTable kernels_layernorm_f32();
+KernelTable kernels_layernorm_bf16();
 KernelTable bwd_kernels_softmax_f32();
 KernelTable bwd_kernels_softmax_bf16();
 KernelTable bwd_kernels_rmsnorm_f32();

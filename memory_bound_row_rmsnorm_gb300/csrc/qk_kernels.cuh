@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
                 "a row group is whole warps or a power-of-two part of one");
   static_assert(!CLUSTER || TPR == THREADS, "a clustered row spans the whole CTA");
   static_assert(NW <= 16, "block-reduction buffer holds 16 warps");
-  static_assert(!TWO_PASS || (TPR == THREADS && OP != kXent), "two passes: one row per CTA");
+  static_assert(!TWO_PASS || (TPR == THREADS && (OP == kSoftmax || OP == kRmsNorm)),
+                "two passes: softmax and RMSNorm, one row per CTA");
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);                  // [kMaxSlots]
@@ -183,15 +184,37 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   // of w is loaded once into registers -- unless that would take more than
   // 8 vectors of registers, in which case the finish re-reads it through L1
   // (the slice a CTA needs stays cached there; HBM sees w once).
-  constexpr bool kWeightInRegs = VPT <= 8 && !TWO_PASS;  // two passes: columns change per chunk
+  // two passes: columns change per chunk
+  constexpr bool kWeightInRegs = VPT <= kAffineRegsMaxVpt && !TWO_PASS;
+  constexpr bool kAffine = (OP == kRmsNorm || OP == kLayerNorm);
+  // LayerNorm's bias likewise, but only up to 4 vectors: with 8, w and b
+  // together would cost a second CTA per SM.  What LayerNorm does not hold in
+  // registers it stages in shared memory, so that the finish never waits on
+  // a global load.
+  constexpr bool kBiasInRegs = OP == kLayerNorm && VPT <= kLnBiasRegsMaxVpt && !TWO_PASS;
+  constexpr bool kWeightInSmem = OP == kLayerNorm && !kWeightInRegs;
+  constexpr bool kBiasInSmem = OP == kLayerNorm && !kBiasInRegs;
   uint4 wv[kWeightInRegs ? VPT : 1];
+  uint4 bv[kBiasInRegs ? VPT : 1];
+  uint4* wsm = reinterpret_cast<uint4*>(ring + size_t(S) * a.slot_bytes);
+  uint4* bsm = wsm + (kWeightInSmem ? param_slice_bytes(SV) / 16 : 0);
   const uint4* wg = static_cast<const uint4*>(a.w) + v0;
-  if constexpr (OP == kRmsNorm && kWeightInRegs) {
+  const uint4* bg = static_cast<const uint4*>(a.bias) + v0;  // unused when bias is null
+  if constexpr (kAffine && kWeightInRegs) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int64_t lv = l + int64_t(k) * TPR;
       wv[k] = lv < nv ? __ldg(wg + lv) : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (kBiasInRegs)
+        bv[k] = (lv < nv && a.bias != nullptr) ? __ldg(bg + lv) : make_uint4(0u, 0u, 0u, 0u);
     }
+  }
+  if constexpr (kWeightInSmem || kBiasInSmem) {
+    for (int64_t v = tid; v < nv; v += THREADS) {
+      if constexpr (kWeightInSmem) wsm[v] = __ldg(wg + v);
+      if constexpr (kBiasInSmem) bsm[v] = a.bias != nullptr ? __ldg(bg + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
   }
 
   // Softmax keeps exp(x - thread max) in registers for the finish, unless
@@ -212,6 +235,27 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   if constexpr (OP == kXent) {
     const int64_t row0 = (K > 1 || CLUSTER) ? int64_t(cid) : int64_t(cid) * R + g;
     if (q_total > 0 && row0 < M) t_next = __ldg(a.target + row0);
+  }
+  // LayerNorm merges (count, mean, M2) partials; the counts follow from the
+  // slice geometry (a LayerNorm slice is never chunked), so they are fixed
+  // for the launch: `ln_full` when every thread holds VPT vectors, the count
+  // of warp (lane % WPG) of this row group, and that of cluster rank (lane % 16).
+  bool ln_full = false;
+  float ln_wc = 0.f, ln_cc = 0.f;
+  if constexpr (OP == kLayerNorm) {
+    ln_full = (nv == int64_t(TPR) * VPT);
+    if constexpr (WPG > 1) {
+      const int w = lane % WPG;
+      int c = 0;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) c += max(0, min(32, int(nv) - k * TPR - w * 32));
+      ln_wc = float(c * E);
+    }
+    if constexpr (CLUSTER) {
+      const uint32_t r = uint32_t(lane) & 15u;
+      const int64_t s0 = min(NV, int64_t(r) * SV);
+      ln_cc = r < C ? float((min(NV, s0 + SV) - s0) * E) : 0.f;
+    }
   }
   bool failed = false;  // a wait of this thread ran out
   bool abort = false;   // block-uniform: some thread's wait ran out
@@ -242,7 +286,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     // Padding lanes get the reduction's neutral element (0 for a sum of
     // squares, -inf for a maximum / sum of exponentials), so the arithmetic
     // below needs no per-element masking.
-    constexpr uint32_t kFill = (OP == kRmsNorm) ? 0u : V::kNegInfBits;
+    constexpr uint32_t kFill = (OP == kRmsNorm || OP == kLayerNorm) ? 0u : V::kNegInfBits;
     bool valid[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -254,6 +298,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
 
     // ---- thread-level reduction (registers) ----
     float pm = kNegInf, ps = 0.f;  // partial (max, sum-exp), or (-, sum of squares)
+    float pn = 0.f;                // LayerNorm: element count of the partial (mean pm, M2 ps)
     float tm = kNegInf;            // softmax: this thread's own maximum
     if (second) {
       // two-pass, second pass: nothing to reduce
@@ -271,6 +316,40 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       }
       run_ss = (j == 0 ? 0.f : run_ss) + (acc.x + acc.y);
       ps = run_ss;
+    } else if constexpr (OP == kLayerNorm) {
+      // (count, mean, M2) of this thread's elements: the mean first, then the
+      // squared deviations from it, both over the registers
+      float cnt = 0.f;
+      float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;  // padding is 0 and adds nothing, but it is not counted
+        float f[E];
+        V::unpack(xr[k], f);
+        cnt += float(E);
+#pragma unroll
+        for (int e = 0; e < E; e += 2) s2 = add2(s2, make_float2(f[e], f[e + 1]));
+      }
+      constexpr float kInvFull = 1.f / float(E * VPT);  // a power of two: exact
+      const float mu = cnt == float(E * VPT) ? (s2.x + s2.y) * kInvFull
+                       : cnt > 0.f           ? __fdiv_rn(s2.x + s2.y, cnt)
+                                             : 0.f;
+      const float2 nmu = make_float2(-mu, -mu);
+      float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;
+        float f[E];
+        V::unpack(xr[k], f);
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          const float2 d = add2(make_float2(f[e], f[e + 1]), nmu);
+          q2 = fma2(d, d, q2);
+        }
+      }
+      pn = cnt;
+      pm = ln_full ? s2.x + s2.y : mu;  // full rows reduce in sum form (below)
+      ps = q2.x + q2.y;
     } else if constexpr (OP == kRmsNorm) {
       float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
@@ -355,7 +434,15 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     // ---- warp butterfly; warp partials to the block buffer ----
     const bool row_end = (j == K - 1);  // the row's reduction is complete (first pass)
     if (row_end) {
-      warp_reduce<OP, GW>(pm, ps);
+      if constexpr (OP == kLayerNorm) {
+        if (ln_full) {  // the same for every row group of the launch
+          group_welford_sum<GW, E * VPT>(pm, ps);
+        } else {
+          group_welford<GW>(pn, pm, ps);
+        }
+      } else {
+        warp_reduce<OP, GW>(pm, ps);
+      }
       if (WPG > 1 && lane == 0) red[ibit * 16 + warp] = make_float2(pm, ps);
     }
     // One barrier per step: the slot is free again (every thread has its data
@@ -421,7 +508,28 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     }
 
     // ---- block reduction over the warps of this row group ----
-    if constexpr (WPG > 1) merge_partials<OP>(red + row_ibit * 16 + g * WPG, WPG, pm, ps);
+    if constexpr (OP == kLayerNorm) {
+      // Every warp of the group merges the group's WPG warp partials with a
+      // butterfly of width WPG (lane l takes partial l % WPG).
+      if constexpr (WPG > 1) {
+        const float2 v = red[row_ibit * 16 + g * WPG + lane % WPG];
+        pm = v.x;
+        ps = v.y;
+        if (ln_full) {
+          group_welford_sum<WPG, 32 * VPT * E>(pm, ps);
+        } else {
+          pn = ln_wc;
+          group_welford<WPG>(pn, pm, ps);
+        }
+      }
+      if (ln_full) {  // back to (count, mean): the count is a power of two
+        constexpr float kInvGroup = 1.f / float(TPR * VPT * E);
+        pn = float(TPR * VPT * E);
+        pm = pm * kInvGroup;
+      }
+    } else if constexpr (WPG > 1) {
+      merge_partials<OP>(red + row_ibit * 16 + g * WPG, WPG, pm, ps);
+    }
 
     // ---- cluster reduction: every CTA's partial into every peer (DSMEM) ----
     if constexpr (CLUSTER) {
@@ -436,7 +544,30 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         report_status(a.status, kStatusTimeout);
         failed = true;
       }
-      merge_partials<OP>(xbuf + b * kMaxCluster, int(C), pm, ps);
+      if constexpr (OP == kLayerNorm) {  // a butterfly over the C partials
+        if (NV % C == 0 && (C & (C - 1)) == 0) {  // equal slices, C a power of two
+          const float2 v = xbuf[b * kMaxCluster + (uint32_t(lane) & (C - 1))];
+          pn = float(SV * E);
+          pm = v.x;
+          ps = v.y;
+          switch (C) {
+            case 2: group_welford_equal<2>(pn, pm, ps); break;
+            case 4: group_welford_equal<4>(pn, pm, ps); break;
+            case 8: group_welford_equal<8>(pn, pm, ps); break;
+            case 16: group_welford_equal<16>(pn, pm, ps); break;
+            default: break;  // C == 1: nothing to merge
+          }
+        } else {  // width 16; lanes beyond C hold count 0 and are neutral
+          const uint32_t r = uint32_t(lane) & 15u;
+          const float2 v = r < C ? xbuf[b * kMaxCluster + r] : make_float2(0.f, 0.f);
+          pn = ln_cc;
+          pm = v.x;
+          ps = v.y;
+          group_welford<16>(pn, pm, ps);
+        }
+      } else {
+        merge_partials<OP>(xbuf + b * kMaxCluster, int(C), pm, ps);
+      }
     }
 
     if constexpr (TWO_PASS) {  // keep the totals for the second pass
@@ -501,6 +632,42 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         yg[l + k * TPR] = V::pack(o);
       }
       if (l == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = r;
+    } else if constexpr (OP == kLayerNorm) {
+      const float r = rsqrtf(fmaf(ps, a.inv_n, a.eps));  // 1/sqrt(population variance + eps)
+      const float2 r2 = make_float2(r, r), c2 = make_float2(-pm * r, -pm * r);
+      uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;
+        float f[E], w[E], bb[E], o[E];
+        if constexpr (VPT <= 4) {
+          V::unpack(xr[k], f);  // may reuse the unpacked values of the reduction
+        } else {
+          V::unpack_fresh(xr[k], f);
+        }
+        if constexpr (kWeightInRegs) {
+          V::unpack_fresh(wv[k], w);
+        } else {
+          V::unpack(wsm[l + k * TPR], w);
+        }
+        if constexpr (kBiasInRegs) {
+          V::unpack_fresh(bv[k], bb);
+        } else {
+          V::unpack(bsm[l + k * TPR], bb);
+        }
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {  // (x * rstd - mean * rstd) * w + b
+          const float2 v = fma2(fma2(make_float2(f[e], f[e + 1]), r2, c2),
+                                make_float2(w[e], w[e + 1]), make_float2(bb[e], bb[e + 1]));
+          o[e] = v.x;
+          o[e + 1] = v.y;
+        }
+        yg[l + k * TPR] = V::pack(o);
+      }
+      if (l == 0 && rank == 0) {
+        if (a.rstd != nullptr) a.rstd[row] = r;
+        if (a.mean != nullptr) a.mean[row] = pm;
+      }
     } else {
       const bool leader = (l == 0 && rank == 0);
       const bool ignored = (trow == a.ignore_index);
@@ -576,6 +743,7 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
   const T* xrow = static_cast<const T*>(a.x) + row * N + e0;
   float f[EPT];
   float pm = kNegInf, ps = 0.f, tm = kNegInf, xt = 0.f;
+  float pn = 0.f;  // LayerNorm: element count of the partial (mean pm, M2 ps)
   bool own_t = false;
   const int64_t trow = (OP == kXent) ? a.target[row] : -1;
 
@@ -583,9 +751,26 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
       const int64_t e = c0 + tid + int64_t(k) * THREADS;
-      f[k] = e < ne ? V::load1(xrow + e) : (OP == kRmsNorm ? 0.f : kNegInf);
+      f[k] = e < ne ? V::load1(xrow + e) : ((OP == kRmsNorm || OP == kLayerNorm) ? 0.f : kNegInf);
     }
-    if constexpr (OP == kRmsNorm) {
+    if constexpr (OP == kLayerNorm) {  // one chunk: the row slice fits the registers
+      float sum = 0.f;
+      int cnt = 0;
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        const bool in = c0 + tid + int64_t(k) * THREADS < ne;
+        sum += f[k];  // padding is 0
+        cnt += in ? 1 : 0;
+      }
+      pn = float(cnt);
+      pm = cnt > 0 ? __fdiv_rn(sum, pn) : 0.f;
+      ps = 0.f;
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        const float d = f[k] - pm;
+        if (c0 + tid + int64_t(k) * THREADS < ne) ps = fmaf(d, d, ps);
+      }
+    } else if constexpr (OP == kRmsNorm) {
 #pragma unroll
       for (int k = 0; k < EPT; ++k) ps = fmaf(f[k], f[k], ps);
     } else {
@@ -617,10 +802,28 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
     }
   }
 
-  warp_reduce<OP>(pm, ps);
+  if constexpr (OP == kLayerNorm) {
+    group_welford<32>(pn, pm, ps);
+  } else {
+    warp_reduce<OP>(pm, ps);
+  }
   if (lane == 0) red[warp] = make_float2(pm, ps);
   __syncthreads();
-  merge_partials<OP>(red, NW, pm, ps);
+  if constexpr (OP == kLayerNorm) {  // warp w holds elements w*32 .. w*32+31 of each chunk column
+    auto warp_count = [&](int w) {
+      int64_t c = 0;
+#pragma unroll
+      for (int k = 0; k < EPT; ++k)
+        c += max(int64_t(0), min(int64_t(32), ne - int64_t(k) * THREADS - int64_t(w) * 32));
+      return float(c);
+    };
+    pn = warp_count(0);
+    pm = red[0].x;
+    ps = red[0].y;
+    for (int w = 1; w < NW; ++w) welford_merge(pn, pm, ps, warp_count(w), red[w].x, red[w].y);
+  } else {
+    merge_partials<OP>(red, NW, pm, ps);
+  }
   if constexpr (CLUSTER) {
     if (tid == 0) {
       mbar_arrive_expect_tx(xb, C * 8u);
@@ -628,7 +831,18 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
       for (uint32_t r = 0; r < C; ++r) st_async_f2(map_to_rank(mine, r), pm, ps, map_to_rank(xb, r));
     }
     if (!mbar_wait<true>(xb, 0u, a.timeout_ns)) report_status(a.status, kStatusTimeout);
-    merge_partials<OP>(xbuf, int(C), pm, ps);
+    if constexpr (OP == kLayerNorm) {  // CTA r holds the ne_r elements of its slice
+      auto cta_count = [&](uint32_t r) {
+        const int64_t s0 = min(N, int64_t(r) * SE);
+        return float(min(N, s0 + SE) - s0);
+      };
+      pn = cta_count(0);
+      pm = xbuf[0].x;
+      ps = xbuf[0].y;
+      for (uint32_t r = 1; r < C; ++r) welford_merge(pn, pm, ps, cta_count(r), xbuf[r].x, xbuf[r].y);
+    } else {
+      merge_partials<OP>(xbuf, int(C), pm, ps);
+    }
   }
 
   if constexpr (OP == kSoftmax) {
@@ -649,6 +863,23 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
       if (e < ne) V::store1(yrow + e, __fmul_rn(__fmul_rn(f[k], r), V::load1(wrow + e)));
     }
     if (tid == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = r;
+  } else if constexpr (OP == kLayerNorm) {
+    const float r = rsqrtf(fmaf(ps, a.inv_n, a.eps));  // 1/sqrt(population variance + eps)
+    T* yrow = static_cast<T*>(a.y) + row * N + e0;
+    const T* wrow = static_cast<const T*>(a.w) + e0;
+    const T* brow = static_cast<const T*>(a.bias) + e0;  // unused when bias is null
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int64_t e = tid + int64_t(k) * THREADS;
+      if (e < ne) {
+        const float b = a.bias != nullptr ? V::load1(brow + e) : 0.f;
+        V::store1(yrow + e, fmaf(__fmul_rn(__fsub_rn(f[k], pm), r), V::load1(wrow + e), b));
+      }
+    }
+    if (tid == 0 && rank == 0) {
+      if (a.rstd != nullptr) a.rstd[row] = r;
+      if (a.mean != nullptr) a.mean[row] = pm;
+    }
   } else {
     const float lse = pm + logf(ps);
     const bool ignored = (trow == a.ignore_index);

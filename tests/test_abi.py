@@ -53,6 +53,8 @@ def test_max_row_elements(lib):
     assert qb.qk_max_row_elements(qb.QK_OP_SOFTMAX_BWD, qb.QK_F32) == 131072
     assert qb.qk_max_row_elements(qb.QK_OP_RMSNORM_BWD, qb.QK_BF16) == 262144
     assert qb.qk_max_row_elements(qb.QK_OP_XENT_BWD, qb.QK_F32) == 2 ** 63 - 1
+    assert qb.qk_max_row_elements(qb.QK_OP_LAYERNORM, qb.QK_F32) == 262144  # 1 MiB rows
+    assert qb.qk_max_row_elements(qb.QK_OP_LAYERNORM, qb.QK_BF16) == 524288
 
 
 # Fake, never-dereferenced device addresses: every call below must be refused
@@ -116,7 +118,8 @@ def test_plan_override_validation(lib):
     ok = qb.qk_plan(threads=256, row_threads=256, vec_per_thread=4, cluster=1)
     assert lib.qk_set_plan_override(qb.QK_OP_SOFTMAX, qb.QK_F32, ctypes.byref(ok)) == qb.QK_OK
     assert lib.qk_set_plan_override(qb.QK_OP_SOFTMAX, qb.QK_F32, None) == qb.QK_OK
-    assert lib.qk_set_plan_override(6, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
+    assert lib.qk_set_plan_override(qb.QK_OP_LAYERNORM, qb.QK_BF16, None) == qb.QK_OK
+    assert lib.qk_set_plan_override(7, qb.QK_F32, None) == qb.QK_ERR_INVALID_ARG
 
 
 def test_timeout_hook_argument_checks(lib):
@@ -159,3 +162,35 @@ def test_backward_argument_checks(lib):
     assert lib.qk_xent_bwd(A, A + 4096, None, None, A + 8192, 4, 8, F, None) == qb.QK_ERR_INVALID_ARG
     assert lib.qk_xent_bwd(A, A + 4096, A + 4608, None, A + 4096, 4, 8, F, None) == qb.QK_ERR_INVALID_ARG
     assert lib.qk_xent_bwd(A, A + 4096, A + 4608, None, A + 8192, 4, 6, F, None) == qb.QK_ERR_UNSUPPORTED
+
+
+def test_layernorm_argument_checks(lib):
+    F, B = qb.QK_F32, qb.QK_BF16
+    ln = lib.qk_layernorm_fwd
+    # x, w, b, y, mean, rstd, M, N, eps, dtype, stream
+    ok = [A, A + 4096, A + 8192, A + 12288, A + 16384, A + 20480]
+    assert ln(None, None, None, None, None, None, 0, 4, 1e-5, F, None) == qb.QK_OK  # M == 0
+    assert ln(None, *ok[1:], 4, 4, 1e-5, F, None) == qb.QK_ERR_INVALID_ARG
+    assert ln(ok[0], None, *ok[2:], 4, 4, 1e-5, F, None) == qb.QK_ERR_INVALID_ARG
+    assert ln(*ok[:3], None, *ok[4:], 4, 4, 1e-5, F, None) == qb.QK_ERR_INVALID_ARG
+    for eps in (-1.0, float("nan"), float("inf")):
+        assert ln(*ok, 4, 4, eps, F, None) == qb.QK_ERR_INVALID_ARG
+    assert ln(*ok, 4, 4, 1e-5, 5, None) == qb.QK_ERR_INVALID_ARG
+    assert ln(*ok, 4, 262148, 1e-5, F, None) == qb.QK_ERR_UNSUPPORTED  # beyond 1 MiB rows
+    assert ln(*ok, 4, 524292, 1e-5, B, None) == qb.QK_ERR_UNSUPPORTED
+    for i, off in ((0, 2), (2, 1), (4, 2), (5, 1)):  # x, b, mean, rstd misaligned
+        bad = list(ok)
+        bad[i] += off
+        assert ln(*bad, 4, 4, 1e-5, F, None) == qb.QK_ERR_MISALIGNED
+    bad = list(ok)
+    bad[3] = A + 8  # y partly over x
+    assert ln(*bad, 4, 4, 1e-5, F, None) == qb.QK_ERR_INVALID_ARG
+    bad = list(ok)
+    bad[3] = A + 8192  # y over b
+    assert ln(*bad, 4, 4, 1e-5, F, None) == qb.QK_ERR_INVALID_ARG
+    bad = list(ok)
+    bad[4] = A + 20480 + 8  # mean over rstd
+    assert ln(*bad, 4, 4, 1e-5, F, None) == qb.QK_ERR_INVALID_ARG
+    bad = list(ok)
+    bad[5] = A + 4096  # rstd over w
+    assert ln(*bad, 4, 4, 1e-5, F, None) == qb.QK_ERR_INVALID_ARG
