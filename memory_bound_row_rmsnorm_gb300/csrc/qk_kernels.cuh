@@ -1,6 +1,8 @@
 // qk_kernels.cuh -- the row-reduction kernels for sm_103a (GB300).
 //
-// row_kernel: the fast path (16-byte aligned rows).
+// row_kernel: the fast path (16-byte aligned rows).  The row reduction is a
+// (max, sum of exponentials) pair for softmax and cross-entropy, a sum of
+// squares for RMSNorm, and a (count, mean, M2) triple for LayerNorm.
 //   * Persistent grid: each CTA (or each cluster of CTAs) walks a strided list
 //     of work items.  An item is a block of `threads / row_threads` consecutive
 //     rows (contiguous in memory), one row slice of a cluster, or one chunk of
@@ -318,27 +320,28 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       ps = run_ss;
     } else if constexpr (OP == kLayerNorm) {
       // (count, mean, M2) of this thread's elements: the mean first, then the
-      // squared deviations from it, both over the registers
-      float cnt = 0.f;
+      // squared deviations from it, both over the registers.  Padding is 0,
+      // so it adds nothing to the sum; it is left out of the count and of M2.
+      constexpr float kInvFull = 1.f / float(E * VPT);  // a power of two: exact
       float2 s2 = make_float2(0.f, 0.f);
+      float cnt = 0.f;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
-        if (!valid[k]) continue;  // padding is 0 and adds nothing, but it is not counted
         float f[E];
         V::unpack(xr[k], f);
-        cnt += float(E);
+        cnt += valid[k] ? float(E) : 0.f;
 #pragma unroll
         for (int e = 0; e < E; e += 2) s2 = add2(s2, make_float2(f[e], f[e + 1]));
       }
-      constexpr float kInvFull = 1.f / float(E * VPT);  // a power of two: exact
-      const float mu = cnt == float(E * VPT) ? (s2.x + s2.y) * kInvFull
-                       : cnt > 0.f           ? __fdiv_rn(s2.x + s2.y, cnt)
-                                             : 0.f;
+      const float sum = s2.x + s2.y;
+      // Full rows: every thread holds VPT vectors (a padded thread of a row
+      // that is not written has sum 0 and M2 0, which harms nothing).
+      const float mu = ln_full ? sum * kInvFull : (cnt > 0.f ? __fdiv_rn(sum, cnt) : 0.f);
       const float2 nmu = make_float2(-mu, -mu);
       float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
-        if (!valid[k]) continue;
+        if (!ln_full && !valid[k]) continue;
         float f[E];
         V::unpack(xr[k], f);
 #pragma unroll
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         }
       }
       pn = cnt;
-      pm = ln_full ? s2.x + s2.y : mu;  // full rows reduce in sum form (below)
+      pm = ln_full ? sum : mu;  // full rows reduce in sum form (below)
       ps = q2.x + q2.y;
     } else if constexpr (OP == kRmsNorm) {
       float2 acc = make_float2(0.f, 0.f);
@@ -643,7 +646,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         if constexpr (VPT <= 4) {
           V::unpack(xr[k], f);  // may reuse the unpacked values of the reduction
         } else {
-          V::unpack_fresh(xr[k], f);
+          V::unpack_fresh(xr[k], f);  // only the packed input stays live across the reduction
         }
         if constexpr (kWeightInRegs) {
           V::unpack_fresh(wv[k], w);
