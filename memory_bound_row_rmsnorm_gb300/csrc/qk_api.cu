@@ -237,9 +237,9 @@ struct Choice {
 };
 constexpr int64_t kStream = INT64_MAX;  // cross-entropy: any longer row is streamed
 const Choice kRmsNormTable[] = {
-    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 2},       {128, 256, 32, 4, 1, 2},
-    {256, 256, 64, 4, 1, 1},     {512, 128, 128, 4, 1, 1},     {1024, 128, 128, 8, 1, 1},
-    {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 3},       {128, 256, 32, 4, 1, 2},
+    {256, 256, 64, 4, 1, 2},     {512, 128, 128, 4, 1, 1},     {1024, 128, 128, 8, 1, 1},
+    {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 1},
     {16384, 256, 256, 8, 8, 3},  {32768, 256, 256, 8, 16, 2},  {65536, 512, 512, 8, 16, 2},
 };
 // LayerNorm: from a sweep of every compiled configuration on GB300 (M = 16384,
@@ -252,14 +252,14 @@ const Choice kLayerNormTable[] = {
     {16384, 256, 256, 8, 8, 2},  {32768, 512, 512, 8, 8, 1},   {65536, 512, 512, 8, 16, 2},
 };
 const Choice kSoftmaxTable[] = {
-    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 2},       {128, 256, 32, 4, 1, 2},
+    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 3},       {128, 256, 32, 4, 1, 3},
     {256, 256, 64, 4, 1, 2},     {512, 256, 128, 4, 1, 1},     {1024, 256, 256, 4, 1, 1},
-    {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
-    {16384, 256, 256, 8, 8, 3},  {32768, 256, 256, 16, 8, 1},  {65536, 256, 256, 16, 16, 1},
+    {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {16384, 256, 256, 16, 4, 2},  {32768, 256, 256, 16, 8, 1},  {65536, 256, 256, 16, 16, 1},
 };
 const Choice kXentTable[] = {
-    {32, 256, 8, 4, 1, 1},       {64, 256, 8, 8, 1, 1},        {128, 256, 16, 8, 1, 1},
-    {256, 256, 32, 8, 1, 2},     {512, 256, 64, 8, 1, 2},      {1024, 256, 128, 8, 1, 2},
+    {32, 256, 8, 4, 1, 1},       {64, 256, 8, 8, 1, 2},        {128, 256, 16, 8, 1, 2},
+    {256, 256, 32, 8, 1, 2},     {512, 256, 64, 8, 1, 2},      {1024, 128, 128, 8, 1, 1},
     {2048, 256, 256, 8, 1, 2},   {kStream, 256, 256, 4, 1, 2},  // 16 KB chunks
 };
 
