@@ -152,10 +152,13 @@ QK_API qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* 
  * Backward passes.  The article benchmarks the forward passes only; these are
  * the derivatives of the same definitions, built on the same read-once ring
  * kernels (each input element read from HBM once, each output written once).
- * They take the fast path only: x, y, dy, dx, w and the logits must be 16-byte
- * aligned and N * sizeof(dtype) a multiple of 16 (QK_ERR_UNSUPPORTED
- * otherwise), and rows may hold up to half of qk_max_row_elements' forward
- * limit (softmax, RMSNorm; see qk_max_row_elements(QK_OP_*_BWD, dtype)).
+ * The fast path wants x, y, dy, dx, w and the logits 16-byte aligned and
+ * N * sizeof(dtype) a multiple of 16; rows may then hold up to half of
+ * qk_max_row_elements' forward limit (softmax, RMSNorm; see
+ * qk_max_row_elements(QK_OP_*_BWD, dtype)).  Other inputs (pointers aligned to
+ * their element size) take a masked path with the same results: any N for
+ * cross-entropy, rows of up to 131,072 elements for softmax and RMSNorm
+ * (QK_ERR_UNSUPPORTED beyond).
  */
 
 /*
@@ -168,7 +171,8 @@ QK_API qk_status qk_softmax_bwd(const void* y, const void* dy, void* dx, int64_t
 
 /*
  * Bytes of device workspace qk_rmsnorm_bwd needs for these sizes on the
- * current device (fp32 partial column sums of dw, one row per CTA).
+ * current device (fp32 partial column sums of dw, one row per CTA): enough
+ * for the fast and for the masked path, whichever the pointers select.
  */
 QK_API qk_status qk_rmsnorm_bwd_workspace_size(int64_t M, int64_t N, qk_dtype dtype,
                                                size_t* bytes);

@@ -41,6 +41,8 @@ constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s bound on any in-kerne
 constexpr int kMaxDevices = 64;
 constexpr int kRingMaxVectorsPerCta = 4096;  // 256 threads x 16 vectors, or 512 x 8
 constexpr int64_t kMaxRowBytes = int64_t(kMaxCluster) * kRingMaxVectorsPerCta * 16;  // 1 MiB
+// Masked backward softmax / RMSNorm: 16 clusters of 512 threads x 16 elements.
+constexpr int64_t kMaskedBwdMaxRow = int64_t(kMaxCluster) * 512 * 16;  // 131,072 elements
 
 struct DeviceInfo {
   std::atomic<bool> ready{false};  // set once, after the fields below
@@ -148,7 +150,7 @@ qk_status prepare_kernel(int dev, const DeviceInfo& d, const KernelEntry& k) {
   std::lock_guard<std::mutex> lock(g_mu);
   auto key = std::make_tuple(dev, k.func);
   if (g_attr_done.count(key)) return QK_OK;
-  if (k.path != 2 &&  // the ring kernels (forward and backward) take dynamic shared memory
+  if ((k.path == 1 || k.path == 3 || k.path == 4 || k.path == 6) &&  // ring kernels: dynamic smem
       cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin) !=
           cudaSuccess) {
     cudaGetLastError();
@@ -416,6 +418,83 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   return QK_OK;
 }
 
+// Rows that do not start on a 16-byte boundary (shifted ring kernel): each
+// step copies the aligned range around its elements, so a row group must hold
+// ceil((15 + slice bytes) / 16) vectors.  Row groups from 8 to 256 threads of 4
+// vectors, then 256 x 8, then clusters of those for softmax / RMSNorm /
+// LayerNorm; cross-entropy streams longer rows in chunks of 2047 vectors.
+struct ShiftChoice {
+  int threads, row_threads, vec_per_thread, slots;
+};
+constexpr ShiftChoice kShiftTable[] = {
+    {256, 8, 4, 2},   {256, 16, 4, 2},  {256, 32, 4, 2}, {256, 64, 4, 2},
+    {256, 128, 4, 2}, {256, 256, 4, 2}, {256, 256, 8, 1},
+};
+int64_t span_vectors(int64_t elems, int es) { return (15 + elems * es + 15) / 16; }
+
+qk_status plan_shifted(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p) {
+  const int es = elem_size(dt);
+  const int kinds = int(sizeof(kShiftTable) / sizeof(ShiftChoice));
+  const int last = kinds - 1;
+  int pick = -1, cl = 1, k = 1;
+  for (int i = 0; i <= last && pick < 0; ++i)
+    if (span_vectors(N, es) <= int64_t(kShiftTable[i].row_threads) * kShiftTable[i].vec_per_thread)
+      pick = i;
+  if (pick < 0 && op == kXent) {  // stream the row in chunks of (cap - 1) vectors
+    pick = last;
+    const int64_t che = (int64_t(kShiftTable[pick].row_threads) * kShiftTable[pick].vec_per_thread - 1) *
+                        (16 / es);
+    k = int((N + che - 1) / che);
+  } else if (pick < 0) {  // clusters of 256 x 8
+    pick = kinds - 1;
+    const int64_t cap = int64_t(kShiftTable[pick].row_threads) * kShiftTable[pick].vec_per_thread;
+    while (cl <= kMaxCluster && span_vectors((N + cl - 1) / cl, es) > cap) cl <<= 1;
+    if (cl > kMaxCluster) return QK_ERR_UNSUPPORTED;
+  }
+  const ShiftChoice& c = kShiftTable[pick];
+  const KernelEntry* ke = find_kernel(op, dt, 6, c.threads, c.row_threads, c.vec_per_thread, cl > 1);
+  if (ke == nullptr) return QK_ERR_UNSUPPORTED;
+  const int R = c.threads / c.row_threads;
+  int64_t item_bytes;
+  if (k > 1) {
+    item_bytes = int64_t(c.row_threads) * c.vec_per_thread * 16;
+    p->num_items = M;
+  } else if (cl > 1) {
+    item_bytes = span_vectors((N + cl - 1) / cl, es) * 16;
+    p->num_items = M;
+  } else {
+    item_bytes = span_vectors(int64_t(R) * N, es) * 16;
+    p->num_items = (M + R - 1) / R;
+  }
+  const uint32_t slot_bytes = uint32_t((item_bytes + 127) / 128 * 128);
+  int64_t param_bytes = 0;  // staged w (and b), element slices of the CTA
+  if (op == kRmsNorm || op == kOpLayerNorm) {
+    const int64_t slice = ((N + cl - 1) / cl * es + 15) / 16;
+    param_bytes = param_slice_bytes(slice) * (op == kOpLayerNorm ? 2 : 1);
+  }
+  int slots = c.slots;
+  while (slots > 1 && kSmemHeader + int64_t(slots) * slot_bytes + param_bytes > d.smem_optin) --slots;
+  const int64_t smem = kSmemHeader + int64_t(slots) * slot_bytes + param_bytes;
+  if (smem > d.smem_optin) return QK_ERR_UNSUPPORTED;
+  qk_status st = prepare_kernel(dev, d, *ke);
+  if (st != QK_OK) return st;
+  int occ = 0;
+  st = occupancy(dev, *ke, int(smem), cl > 1 ? cl : 0, &occ);
+  if (st != QK_OK) return st;
+  if (occ <= 0) return QK_ERR_UNSUPPORTED;
+  p->kernel = ke;
+  p->cluster = cl;
+  p->slots = slots;
+  p->chunks = k;
+  p->slot_bytes = slot_bytes;
+  p->smem = int(smem);
+  int64_t units = cl > 1 ? int64_t(occ) : int64_t(occ) * d.sms;
+  units = std::min<int64_t>(units, p->num_items);
+  p->ctas_per_sm = cl > 1 ? std::max(1, occ * cl / std::max(1, d.sms)) : occ;
+  p->grid = units * cl;
+  return QK_OK;
+}
+
 // Masked direct path: one row per CTA, or per cluster for long rows.
 qk_status plan_direct(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p) {
   int th, ept, cl = 1;
@@ -481,7 +560,18 @@ qk_status launch(const Plan& p, void* args, void* stream) {
   return QK_OK;
 }
 
+// Forward kernels: the ring (16-byte aligned rows), the shifted ring (rows
+// that start anywhere, x and y with the same alignment modulo 16), the masked
+// direct kernel (everything else, and shifted rows beyond its capacity).
+enum RowPath : int { kPathDirect = 0, kPathRing = 1, kPathShifted = 2 };
+
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+bool same_mod16(const void* a, const void* b) {
+  return ((reinterpret_cast<uintptr_t>(a) ^ reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
+}
+int row_path(bool fast, bool same_alignment) {
+  return fast ? kPathRing : same_alignment ? kPathShifted : kPathDirect;
+}
 bool aligned_to(const void* ptr, size_t n) { return (reinterpret_cast<uintptr_t>(ptr) % n) == 0; }
 
 // [a, a+na) and [b, b+nb) share a byte.
@@ -500,7 +590,7 @@ qk_status check_sizes(int op, int dt, int64_t M, int64_t N) {
 }
 
 // Shared tail of the three entry points: plan, fill args, launch.
-qk_status run(int op, int dt, RowArgs a, bool fast, void* stream) {
+qk_status run(int op, int dt, RowArgs a, int path, void* stream) {
   int dev;
   DeviceInfo* d;
   qk_status st = device_info(&dev, &d);
@@ -513,13 +603,19 @@ qk_status run(int op, int dt, RowArgs a, bool fast, void* stream) {
     uint64_t gen = 0;
     Plan plan;
   };
-  thread_local Cached cache[4][2][2];  // softmax, RMSNorm, x-entropy, LayerNorm
-  Cached& c = cache[op == kOpLayerNorm ? 3 : op][dt][fast ? 1 : 0];
+  thread_local Cached cache[4][2][3];  // (softmax, RMSNorm, x-entropy, LayerNorm) x dtype x path
+  Cached& c = cache[op == kOpLayerNorm ? 3 : op][dt][path];
   const uint64_t gen = g_override_gen.load(std::memory_order_acquire);
   if (!(c.dev == dev && c.M == a.M && c.N == a.N && c.gen == gen)) {
     Plan np;
-    st = fast ? plan_ring(dev, *d, op, dt, a.M, a.N, &np)
-              : plan_direct(dev, *d, op, dt, a.M, a.N, &np);
+    if (path == kPathRing) {
+      st = plan_ring(dev, *d, op, dt, a.M, a.N, &np);
+    } else if (path == kPathShifted) {
+      st = plan_shifted(dev, *d, op, dt, a.M, a.N, &np);
+      if (st == QK_ERR_UNSUPPORTED) st = plan_direct(dev, *d, op, dt, a.M, a.N, &np);
+    } else {
+      st = plan_direct(dev, *d, op, dt, a.M, a.N, &np);
+    }
     if (st != QK_OK) return st;
     c.dev = dev, c.M = a.M, c.N = a.N, c.gen = gen, c.plan = np;
   }
@@ -538,8 +634,49 @@ qk_status run(int op, int dt, RowArgs a, bool fast, void* stream) {
 // per cluster), hence its workspace: rows * N * 4 bytes.
 int64_t dw_partial_rows(const Plan& p) { return p.grid / std::max(1, p.cluster); }
 
-qk_status plan_bwd_cached(int op, int dt, int64_t M, int64_t N, int* dev, DeviceInfo** d,
-                          const Plan** out) {
+// Masked backward path: a persistent grid of one-row CTAs (or clusters for
+// rows beyond 8192 elements), each thread holding up to 16 elements of each
+// input in registers, so rows are limited to kMaskedBwdMaxRow elements.
+// Cross-entropy streams any row in chunks.
+qk_status plan_direct_bwd(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N,
+                          Plan* p) {
+  int th, ept, cl = 1;
+  if (op == kOpXentBwd) {
+    th = 256, ept = 8;
+  } else if (N <= 512) {
+    th = 128, ept = 4;
+  } else if (N <= 2048) {
+    th = 256, ept = 8;
+  } else if (N <= 8192) {
+    th = 512, ept = 16;
+  } else {
+    if (N > kMaskedBwdMaxRow) return QK_ERR_UNSUPPORTED;
+    th = 512, ept = 16;
+    cl = next_pow2((N + 8191) / 8192);
+  }
+  const KernelEntry* ke = find_kernel(op, dt, 5, th, th, ept, cl > 1);
+  if (ke == nullptr) return QK_ERR_UNSUPPORTED;
+  qk_status st = prepare_kernel(dev, d, *ke);
+  if (st != QK_OK) return st;
+  int occ = 0;
+  st = occupancy(dev, *ke, 0, cl > 1 ? cl : 0, &occ);
+  if (st != QK_OK) return st;
+  if (occ <= 0) return QK_ERR_UNSUPPORTED;
+  const int64_t units = std::min<int64_t>(M, cl > 1 ? int64_t(occ) : int64_t(occ) * d.sms);
+  p->kernel = ke;
+  p->cluster = cl;
+  p->slots = 0;
+  p->chunks = 1;
+  p->num_items = M;
+  p->slot_bytes = 0;
+  p->smem = 0;
+  p->ctas_per_sm = cl > 1 ? std::max(1, occ * cl / std::max(1, d.sms)) : occ;
+  p->grid = units * cl;
+  return QK_OK;
+}
+
+qk_status plan_bwd_cached(int op, int dt, int64_t M, int64_t N, bool fast, int* dev,
+                          DeviceInfo** d, const Plan** out) {
   qk_status st = device_info(dev, d);
   if (st != QK_OK) return st;
   struct Cached {
@@ -548,12 +685,12 @@ qk_status plan_bwd_cached(int op, int dt, int64_t M, int64_t N, int* dev, Device
     uint64_t gen = 0;
     Plan plan;
   };
-  thread_local Cached cache[3][2];
-  Cached& c = cache[op - kOpSoftmaxBwd][dt];
+  thread_local Cached cache[3][2][2];  // (op, dtype, ring or masked)
+  Cached& c = cache[op - kOpSoftmaxBwd][dt][fast ? 1 : 0];
   const uint64_t gen = g_override_gen.load(std::memory_order_acquire);
   if (!(c.dev == *dev && c.M == M && c.N == N && c.gen == gen)) {
     Plan np;
-    st = plan_ring(*dev, **d, op, dt, M, N, &np);
+    st = fast ? plan_ring(*dev, **d, op, dt, M, N, &np) : plan_direct_bwd(*dev, **d, op, dt, M, N, &np);
     if (st != QK_OK) return st;
     c.dev = *dev, c.M = M, c.N = N, c.gen = gen, c.plan = np;
   }
@@ -561,12 +698,14 @@ qk_status plan_bwd_cached(int op, int dt, int64_t M, int64_t N, int* dev, Device
   return QK_OK;
 }
 
-// Backward launch: the ring kernel, then (RMSNorm) the fixed-order dw sum.
-qk_status run_bwd(int op, int dt, BwdArgs a, float* dw, size_t workspace_bytes, void* stream) {
+// Backward launch: the ring kernel (or the masked one), then (RMSNorm) the
+// fixed-order dw sum.
+qk_status run_bwd(int op, int dt, BwdArgs a, float* dw, size_t workspace_bytes, bool fast,
+                  void* stream) {
   int dev;
   DeviceInfo* d;
   const Plan* pp;
-  qk_status st = plan_bwd_cached(op, dt, a.M, a.N, &dev, &d, &pp);
+  qk_status st = plan_bwd_cached(op, dt, a.M, a.N, fast, &dev, &d, &pp);
   if (st != QK_OK) return st;
   const Plan& p = *pp;
   const int64_t rows = dw_partial_rows(p);
@@ -640,7 +779,7 @@ qk_status qk_softmax_fwd(const void* x, void* y, int64_t M, int64_t N, qk_dtype 
   a.M = M;
   a.N = N;
   const bool fast = aligned16(x) && aligned16(y) && (N * int64_t(es)) % 16 == 0;
-  return run(kSoftmax, dtype, a, fast, stream);
+  return run(kSoftmax, dtype, a, row_path(fast, same_mod16(x, y)), stream);
 }
 
 qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M,
@@ -668,7 +807,7 @@ qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int
   a.eps = eps;
   const bool fast =
       aligned16(x) && aligned16(y) && aligned16(w) && (N * int64_t(es)) % 16 == 0;
-  return run(kRmsNorm, dtype, a, fast, stream);
+  return run(kRmsNorm, dtype, a, row_path(fast, same_mod16(x, y)), stream);
 }
 
 qk_status qk_layernorm_fwd(const void* x, const void* w, const void* b, void* y, float* mean,
@@ -705,7 +844,7 @@ qk_status qk_layernorm_fwd(const void* x, const void* w, const void* b, void* y,
   a.eps = eps;
   const bool fast = aligned16(x) && aligned16(y) && aligned16(w) && aligned16(b) &&
                     (N * int64_t(es)) % 16 == 0;
-  return run(kOpLayerNorm, dtype, a, fast, stream);
+  return run(kOpLayerNorm, dtype, a, row_path(fast, same_mod16(x, y)), stream);
 }
 
 qk_status qk_xent_fwd_ex(const void* logits, const int64_t* targets, float* loss, float* lse,
@@ -739,7 +878,7 @@ qk_status qk_xent_fwd_ex(const void* logits, const int64_t* targets, float* loss
   a.ignore_index = ignore;
   a.z_loss = z;
   const bool fast = aligned16(logits) && (N * int64_t(es)) % 16 == 0;
-  st = run(kXent, dtype, a, fast, stream);
+  st = run(kXent, dtype, a, row_path(fast, true), stream);
   if (st != QK_OK || mean_loss == nullptr) return st;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -783,14 +922,15 @@ qk_status qk_softmax_bwd(const void* y, const void* dy, void* dx, int64_t M, int
   const int64_t bytes = M * N * int64_t(es);
   if ((dx != y && overlap(dx, bytes, y, bytes)) || (dx != dy && overlap(dx, bytes, dy, bytes)))
     return QK_ERR_INVALID_ARG;
-  if (!bwd_aligned(dtype, N, {y, dy, dx})) return QK_ERR_UNSUPPORTED;
+  const bool fast = bwd_aligned(dtype, N, {y, dy, dx});
+  if (!fast && N > kMaskedBwdMaxRow) return QK_ERR_UNSUPPORTED;
   BwdArgs a = {};
   a.in0 = y;
   a.in1 = dy;
   a.out = dx;
   a.M = M;
   a.N = N;
-  return run_bwd(kOpSoftmaxBwd, dtype, a, nullptr, 0, stream);
+  return run_bwd(kOpSoftmaxBwd, dtype, a, nullptr, 0, fast, stream);
 }
 
 qk_status qk_rmsnorm_bwd_workspace_size(int64_t M, int64_t N, qk_dtype dtype, size_t* bytes) {
@@ -798,12 +938,25 @@ qk_status qk_rmsnorm_bwd_workspace_size(int64_t M, int64_t N, qk_dtype dtype, si
   *bytes = 0;
   qk_status st = check_sizes(kOpRmsNormBwd, dtype, M, N);
   if (st != QK_OK || M == 0) return st;
+  // The path depends on the pointers, which are not known here: enough for
+  // either path that these sizes may take.
   int dev;
   DeviceInfo* d;
   const Plan* p;
-  st = plan_bwd_cached(kOpRmsNormBwd, dtype, M, N, &dev, &d, &p);
-  if (st != QK_OK) return st;
-  *bytes = size_t(dw_partial_rows(*p)) * size_t(N) * 4;
+  int64_t rows = 0;
+  const bool may_be_fast = (N * int64_t(elem_size(dtype))) % 16 == 0;
+  if (may_be_fast) {
+    st = plan_bwd_cached(kOpRmsNormBwd, dtype, M, N, true, &dev, &d, &p);
+    if (st != QK_OK) return st;
+    rows = dw_partial_rows(*p);
+  }
+  st = plan_bwd_cached(kOpRmsNormBwd, dtype, M, N, false, &dev, &d, &p);
+  if (st == QK_OK) {
+    rows = std::max(rows, dw_partial_rows(*p));
+  } else if (!(may_be_fast && st == QK_ERR_UNSUPPORTED)) {
+    return st;  // a masked row too long is only an error when the row cannot be aligned
+  }
+  *bytes = size_t(rows) * size_t(N) * 4;
   return QK_OK;
 }
 
@@ -829,7 +982,8 @@ qk_status qk_rmsnorm_bwd(const void* x, const void* w, const float* rstd, const 
       overlap(workspace, wsb, dy, bytes) || overlap(workspace, wsb, dx, bytes) ||
       overlap(workspace, wsb, dw, N * 4))
     return QK_ERR_INVALID_ARG;
-  if (!bwd_aligned(dtype, N, {x, w, dy, dx})) return QK_ERR_UNSUPPORTED;
+  const bool fast = bwd_aligned(dtype, N, {x, w, dy, dx});
+  if (!fast && N > kMaskedBwdMaxRow) return QK_ERR_UNSUPPORTED;
   BwdArgs a = {};
   a.in0 = x;
   a.in1 = dy;
@@ -839,7 +993,7 @@ qk_status qk_rmsnorm_bwd(const void* x, const void* w, const float* rstd, const 
   a.dw_partial = static_cast<float*>(workspace);
   a.M = M;
   a.N = N;
-  return run_bwd(kOpRmsNormBwd, dtype, a, dw, workspace_bytes, stream);
+  return run_bwd(kOpRmsNormBwd, dtype, a, dw, workspace_bytes, fast, stream);
 }
 
 qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float* lse,
@@ -862,7 +1016,7 @@ qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float
       overlap(dlogits, bytes, targets, M * 8) || overlap(dlogits, bytes, lse, M * 4) ||
       overlap(dlogits, bytes, dloss, M * 4))
     return QK_ERR_INVALID_ARG;
-  if (!bwd_aligned(dtype, N, {logits, dlogits})) return QK_ERR_UNSUPPORTED;
+  const bool fast = bwd_aligned(dtype, N, {logits, dlogits});
   BwdArgs a = {};
   a.in0 = logits;
   a.target = targets;
@@ -873,7 +1027,7 @@ qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float
   a.N = N;
   a.ignore_index = ignore;
   a.z_loss = z;
-  return run_bwd(kOpXentBwd, dtype, a, nullptr, 0, stream);
+  return run_bwd(kOpXentBwd, dtype, a, nullptr, 0, fast, stream);
 }
 
 qk_status qk_xent_bwd(const void* logits, const int64_t* targets, const float* lse,
@@ -914,10 +1068,17 @@ qk_status qk_get_plan(qk_op op, qk_dtype dtype, int64_t M, int64_t N, qk_plan* p
   DeviceInfo* d;
   st = device_info(&dev, &d);
   if (st != QK_OK) return st;
-  const bool fast = (N * int64_t(elem_size(dtype))) % 16 == 0 || is_bwd(op);
+  const bool fast = (N * int64_t(elem_size(dtype))) % 16 == 0;
+  const int64_t m = std::max<int64_t>(M, 1);
   Plan p;
-  st = fast ? plan_ring(dev, *d, op, dtype, std::max<int64_t>(M, 1), N, &p)
-            : plan_direct(dev, *d, op, dtype, std::max<int64_t>(M, 1), N, &p);
+  if (fast) {
+    st = plan_ring(dev, *d, op, dtype, m, N, &p);
+  } else if (is_bwd(op)) {
+    st = plan_direct_bwd(dev, *d, op, dtype, m, N, &p);
+  } else {  // x and y 16-byte aligned, N not: the shifted ring, else the masked kernel
+    st = plan_shifted(dev, *d, op, dtype, m, N, &p);
+    if (st == QK_ERR_UNSUPPORTED) st = plan_direct(dev, *d, op, dtype, m, N, &p);
+  }
   if (st != QK_OK) return st;
   plan->path = p.kernel->path;
   plan->threads = p.kernel->threads;

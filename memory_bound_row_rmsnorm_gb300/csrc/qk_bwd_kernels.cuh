@@ -398,6 +398,168 @@ __global__ void __launch_bounds__(THREADS) bwd_kernel(const BwdArgs a) {
   if constexpr (CLUSTER) cluster_sync_all();
 }
 
+// ---------------------------------------------------------------------------
+// Masked backward path: rows whose start or length is not a multiple of 16
+// bytes.  A persistent grid of CTAs (or of clusters, for long rows) walks the
+// rows; each thread holds EPT elements of each input of its slice in
+// registers (element loads), the row's dot product goes through the warp,
+// block and cluster levels as in bwd_kernel, and every output element is
+// stored once.  RMSNorm's dw partials stay in registers for the columns a
+// thread owns and are written as one partial row per CTA (or per cluster,
+// its own slice).  Cross-entropy has no row reduction: any N is streamed in
+// chunks of THREADS * EPT elements.
+// ---------------------------------------------------------------------------
+template <int OP, typename T, int THREADS, int EPT, bool CLUSTER>
+__global__ void __launch_bounds__(THREADS) bwd_direct_kernel(const BwdArgs a) {
+  using V = Vec16<T>;
+  constexpr int NW = THREADS / 32;
+  constexpr int64_t CH = int64_t(THREADS) * EPT;
+  static_assert(!(CLUSTER && OP == kXentBwd), "x-entropy rows are streamed, not split");
+  __shared__ float red[2][NW];
+  __shared__ float2 xbuf[2][kMaxCluster];
+  __shared__ __align__(8) uint64_t xbar[2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t C = 1, rank = 0;
+  int64_t cid = blockIdx.x, ncl = gridDim.x;
+  if constexpr (CLUSTER) {
+    C = cluster_nctarank();
+    rank = cluster_ctarank();
+    cid = cluster_id_x();
+    ncl = num_clusters_x();
+  }
+  const int64_t M = a.M, N = a.N;
+  const int64_t SE = (N + C - 1) / C;
+  const int64_t e0 = min(N, int64_t(rank) * SE);
+  const int64_t ne = min(N, e0 + SE) - e0;
+  const uint32_t xb0 = smem_addr(&xbar[0]);
+  if constexpr (CLUSTER) {
+    if (tid == 0) {
+      mbar_init(xb0, 1);
+      mbar_init(xb0 + 8, 1);
+      fence_mbar_init();
+    }
+    cluster_sync_all();  // peers' barriers exist before anyone stores into them
+  }
+  grid_dependency_wait();
+  allow_dependent_launch();
+
+  const T* in0 = static_cast<const T*>(a.in0);
+  const T* in1 = static_cast<const T*>(a.in1);
+  T* out = static_cast<T*>(a.out);
+
+  if constexpr (OP == kXentBwd) {  // dloss * ((1 + 2 z lse) exp(x - lse) - onehot(t))
+    for (int64_t row = cid; row < M; row += ncl) {
+      const float lse = __ldg(a.lse + row);
+      const float gr = a.dloss != nullptr ? __ldg(a.dloss + row) : 1.f;
+      const int64_t t = __ldg(a.target + row);
+      const bool ignored = (t == a.ignore_index), tok = t >= 0 && t < N;
+      const float gv = ignored ? 0.f : (tok ? gr : __int_as_float(0x7fc00000));
+      const float zf = fmaf(2.f * a.z_loss, lse, 1.f);
+      const float lb = lse * kLog2e;
+      const T* xr = in0 + row * N;
+      T* orow = out + row * N;
+      for (int64_t c0 = 0; c0 < N; c0 += CH) {
+        float f[EPT];
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {  // all loads first, then the math and stores
+          const int64_t e = c0 + tid + int64_t(k) * THREADS;
+          f[k] = e < N ? V::load1(xr + e) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+          const int64_t e = c0 + tid + int64_t(k) * THREADS;
+          if (e >= N) continue;
+          float p = exp2_approx(fmaf(f[k], kLog2e, -lb)) * zf;
+          if (e == t) p -= 1.f;
+          V::store1(orow + e, p * gv);
+        }
+      }
+    }
+    return;
+  } else {
+    // RMSNorm: the weight of the columns this thread owns, and their dw partials.
+    float wf[OP == kRmsNormBwd ? EPT : 1];
+    float dwacc[OP == kRmsNormBwd ? EPT : 1];
+    if constexpr (OP == kRmsNormBwd) {
+      const T* wr = static_cast<const T*>(a.w) + e0;
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        const int64_t e = tid + int64_t(k) * THREADS;
+        wf[k] = e < ne ? V::load1(wr + e) : 0.f;
+        dwacc[k] = 0.f;
+      }
+    }
+    uint32_t ib = 0, xph = 0;  // row parity: buffers; phase of the cluster barrier
+    bool failed = false;
+    for (int64_t row = cid; row < M; row += ncl) {
+      const T* ra = in0 + row * N + e0;  // y (softmax) or x (RMSNorm)
+      const T* rb = in1 + row * N + e0;  // dy
+      float fa[EPT], fb[EPT];
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        const int64_t e = tid + int64_t(k) * THREADS;
+        fa[k] = e < ne ? V::load1(ra + e) : 0.f;
+        fb[k] = e < ne ? V::load1(rb + e) : 0.f;
+      }
+      const float rs = (OP == kRmsNormBwd) ? __ldg(a.rstd + row) : 0.f;
+      float ps = 0.f;  // sum dy * y, or sum dy * w * x (padding is zero)
+#pragma unroll
+      for (int k = 0; k < EPT; ++k)
+        ps = (OP == kSoftmaxBwd) ? fmaf(fb[k], fa[k], ps) : fmaf(fb[k] * wf[k], fa[k], ps);
+      ps = group_sum<32>(ps);
+      if (lane == 0) red[ib][warp] = ps;
+      __syncthreads();
+      float dot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) dot += red[ib][w];  // index order
+      if constexpr (CLUSTER) {
+        const uint32_t xb = xb0 + 8u * ib;
+        if (tid == 0) {
+          mbar_arrive_expect_tx(xb, C * 8u);
+          const uint32_t mine = smem_addr(&xbuf[ib][rank]);
+          for (uint32_t r = 0; r < C; ++r) st_async_f2(map_to_rank(mine, r), 0.f, dot, map_to_rank(xb, r));
+        }
+        if (!mbar_wait<true>(xb, xph, a.timeout_ns)) {
+          report_status(a.status, 5);
+          failed = true;
+        }
+        if (__syncthreads_or(failed)) break;  // leave together; peers time out the same way
+        dot = 0.f;
+        for (uint32_t r = 0; r < C; ++r) dot += xbuf[ib][r].y;  // rank order
+        xph ^= ib;  // buffer b's barrier completes every second row
+      }
+      ib ^= 1u;
+      T* orow = out + row * N + e0;
+      if constexpr (OP == kSoftmaxBwd) {  // y * (dy - dot)
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+          const int64_t e = tid + int64_t(k) * THREADS;
+          if (e < ne) V::store1(orow + e, fa[k] * (fb[k] - dot));
+        }
+      } else {  // (r dy) w - x (r^3 dot / N); dw partial (dy x) r
+        const float c = rs * rs * rs * dot * a.inv_n;
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+          const int64_t e = tid + int64_t(k) * THREADS;
+          if (e >= ne) continue;
+          V::store1(orow + e, fmaf(fa[k], -c, (rs * fb[k]) * wf[k]));
+          dwacc[k] += (fb[k] * fa[k]) * rs;
+        }
+      }
+    }
+    if constexpr (OP == kRmsNormBwd) {  // one partial row per CTA (per cluster: this slice)
+      float* dst = a.dw_partial + cid * N + e0;
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        const int64_t e = tid + int64_t(k) * THREADS;
+        if (e < ne) dst[e] = dwacc[k];
+      }
+    }
+    if constexpr (CLUSTER) cluster_sync_all();  // no CTA leaves while peers may write to it
+  }
+}
+
 // dw[j] = sum over the partial rows p of partial[p][j], in a fixed order:
 // 32 columns per CTA (one per lane), 8 warps each summing every 8th row,
 // then the 8 warp sums in index order.

@@ -6,6 +6,9 @@
 
 #define QK_BWD(TH, TPR, VPT, CL) \
   {3, TH, TPR, VPT, CL, reinterpret_cast<const void*>(&bwd_kernel<QK_BOP, QK_T, TH, TPR, VPT, CL>)}
+// Masked path (path 5): (threads, elements per thread, clustered).
+#define QK_BWD_DIRECT(TH, EPT, CL) \
+  {5, TH, TH, EPT, CL, reinterpret_cast<const void*>(&bwd_direct_kernel<QK_BOP, QK_T, TH, EPT, CL>)}
 
 namespace qk {
 namespace {
@@ -23,6 +26,12 @@ const KernelEntry kBwdTable[] = {
     QK_BWD(256, 128, 2, false), QK_BWD(256, 256, 2, false), QK_BWD(512, 512, 2, false),
     QK_BWD(256, 256, 2, true),  QK_BWD(512, 512, 2, true),
     QK_BWD(256, 256, 4, true),  QK_BWD(512, 512, 4, true),
+#endif
+#if QK_BOP == 12
+    QK_BWD_DIRECT(256, 8, false),
+#else
+    QK_BWD_DIRECT(128, 4, false),  QK_BWD_DIRECT(256, 8, false),  QK_BWD_DIRECT(512, 16, false),
+    QK_BWD_DIRECT(512, 16, true),
 #endif
 };
 }  // namespace

@@ -359,6 +359,11 @@ struct Vec16<float> {
     return *static_cast<const float*>(p);
   }
   __device__ __forceinline__ static void store1(void* p, float v) { *static_cast<float*>(p) = v; }
+  // v with the elements outside [lo, hi) replaced by the element with bits fill.
+  __device__ __forceinline__ static uint4 keep(uint4 v, int lo, int hi, uint32_t fill) {
+    return make_uint4(0 >= lo && 0 < hi ? v.x : fill, 1 >= lo && 1 < hi ? v.y : fill,
+                      2 >= lo && 2 < hi ? v.z : fill, 3 >= lo && 3 < hi ? v.w : fill);
+  }
 };
 
 template <>
@@ -411,6 +416,18 @@ struct Vec16<__nv_bfloat16> {
   }
   __device__ __forceinline__ static void store1(void* p, float v) {
     *static_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+  }
+  // v with the elements outside [lo, hi) replaced by the element with bits
+  // fill (both halves of fill hold that element).
+  __device__ __forceinline__ static uint32_t keep2(uint32_t u, int e, int lo, int hi, uint32_t fill) {
+    const uint32_t mlo = (e >= lo && e < hi) ? 0x0000ffffu : 0u;
+    const uint32_t mhi = (e + 1 >= lo && e + 1 < hi) ? 0xffff0000u : 0u;
+    const uint32_t m = mlo | mhi;
+    return (u & m) | (fill & ~m);
+  }
+  __device__ __forceinline__ static uint4 keep(uint4 v, int lo, int hi, uint32_t fill) {
+    return make_uint4(keep2(v.x, 0, lo, hi, fill), keep2(v.y, 2, lo, hi, fill),
+                      keep2(v.z, 4, lo, hi, fill), keep2(v.w, 6, lo, hi, fill));
   }
 };
 

@@ -7,12 +7,16 @@
 #pragma once
 
 #include "qk_kernels.cuh"
+#include "qk_shifted_kernels.cuh"
 
 #define QK_RING(TH, TPR, VPT, CL) \
   {1, TH, TPR, VPT, CL, reinterpret_cast<const void*>(&row_kernel<QK_OP, QK_T, TH, TPR, VPT, CL>)}
 #define QK_RING2(TH, TPR, VPT, CL)                                                    \
   {4, TH, TPR, VPT, CL,                                                               \
    reinterpret_cast<const void*>(&row_kernel<QK_OP, QK_T, TH, TPR, VPT, CL, true>)}
+// Rows that do not start on a 16-byte boundary (path 6): aligned superset copies.
+#define QK_SHIFT(TH, TPR, VPT, CL) \
+  {6, TH, TPR, VPT, CL, reinterpret_cast<const void*>(&shifted_kernel<QK_OP, QK_T, TH, TPR, VPT, CL>)}
 #define QK_DIRECT(TH, EPT, CL) \
   {2, TH, TH, EPT, CL, reinterpret_cast<const void*>(&direct_kernel<QK_OP, QK_T, TH, EPT, CL>)}
 
@@ -53,6 +57,16 @@ const KernelEntry kTable[] = {
     QK_RING2(256, 256, 8, false),
     QK_RING2(256, 256, 8, true),
 #endif
+#endif
+    QK_SHIFT(256, 8, 4, false),
+    QK_SHIFT(256, 16, 4, false),
+    QK_SHIFT(256, 32, 4, false),
+    QK_SHIFT(256, 64, 4, false),
+    QK_SHIFT(256, 128, 4, false),
+    QK_SHIFT(256, 256, 4, false),
+    QK_SHIFT(256, 256, 8, false),
+#if QK_OP != 2
+    QK_SHIFT(256, 256, 8, true),
 #endif
     QK_DIRECT(128, 4, false),
     QK_DIRECT(256, 16, false),

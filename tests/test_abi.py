@@ -135,14 +135,15 @@ def test_binding_raises_on_error(lib):
 
 def test_backward_argument_checks(lib):
     F, B = qb.QK_F32, qb.QK_BF16
-    # softmax backward: nulls, element alignment, partial overlap, 16-byte fast-path requirement
+    G = 1 << 30  # spacing of fake buffers that must not overlap
+    # softmax backward: nulls, element alignment, partial overlap, row limits
     assert lib.qk_softmax_bwd(None, A, A + 8192, 4, 4, F, None) == qb.QK_ERR_INVALID_ARG
     assert lib.qk_softmax_bwd(A + 2, A + 4096, A + 8192, 4, 4, F, None) == qb.QK_ERR_MISALIGNED
     assert lib.qk_softmax_bwd(A, A + 4096, A + 16, 4, 4, F, None) == qb.QK_ERR_INVALID_ARG
-    assert lib.qk_softmax_bwd(A, A + 4096, A + 8192, 4, 3, F, None) == qb.QK_ERR_UNSUPPORTED
-    assert lib.qk_softmax_bwd(A + 4, A + 4096, A + 8192, 4, 4, F, None) == qb.QK_ERR_UNSUPPORTED
     assert lib.qk_softmax_bwd(A, A + 4096, A + 8192, 4, 131076, F, None) == qb.QK_ERR_UNSUPPORTED
-    assert lib.qk_softmax_bwd(A, A + (1 << 30), A + (2 << 30), 4, 262148, B, None) == qb.QK_ERR_UNSUPPORTED
+    assert lib.qk_softmax_bwd(A, A + G, A + 2 * G, 4, 262148, B, None) == qb.QK_ERR_UNSUPPORTED
+    # the masked path (unaligned N) holds rows of up to 131,072 elements
+    assert lib.qk_softmax_bwd(A, A + G, A + 2 * G, 4, 131073, B, None) == qb.QK_ERR_UNSUPPORTED
     assert lib.qk_softmax_bwd(None, None, None, 0, 4, F, None) == qb.QK_OK
     # RMSNorm backward: workspace is required; dw must not overlap an input
     args = [A, A + 4096, A + 8192, A + 12288, A + 16384, A + 20480, A + 24576, 1 << 20]
@@ -153,7 +154,8 @@ def test_backward_argument_checks(lib):
     bad = list(args)
     bad[6] = A + 24576 + 4  # workspace not 16-byte aligned
     assert lib.qk_rmsnorm_bwd(*bad, 4, 8, B, None) == qb.QK_ERR_MISALIGNED
-    assert lib.qk_rmsnorm_bwd(*args, 4, 7, B, None) == qb.QK_ERR_UNSUPPORTED
+    far = [A, A + G, A + 2 * G, A + 3 * G, A + 4 * G, A + 5 * G, A + 6 * G, 1 << 20]
+    assert lib.qk_rmsnorm_bwd(*far, 4, 131073, B, None) == qb.QK_ERR_UNSUPPORTED
     n = ctypes.c_size_t(123)
     assert lib.qk_rmsnorm_bwd_workspace_size(-1, 8, B, ctypes.byref(n)) == qb.QK_ERR_INVALID_ARG
     assert lib.qk_rmsnorm_bwd_workspace_size(0, 8, B, ctypes.byref(n)) == qb.QK_OK and n.value == 0
@@ -161,7 +163,6 @@ def test_backward_argument_checks(lib):
     # cross-entropy backward: lse is required; dlogits must not overlap the targets
     assert lib.qk_xent_bwd(A, A + 4096, None, None, A + 8192, 4, 8, F, None) == qb.QK_ERR_INVALID_ARG
     assert lib.qk_xent_bwd(A, A + 4096, A + 4608, None, A + 4096, 4, 8, F, None) == qb.QK_ERR_INVALID_ARG
-    assert lib.qk_xent_bwd(A, A + 4096, A + 4608, None, A + 8192, 4, 6, F, None) == qb.QK_ERR_UNSUPPORTED
 
 
 def test_layernorm_argument_checks(lib):

@@ -195,3 +195,101 @@ def test_backward_benchmark_shapes(op, dtype, M, N):
     """The forward workloads' shapes, checked on every row (oracle in a few seconds)."""
     case = make_case(op, dtype, M, N, seed=9100)
     check(op, dtype, case, run_gpu(op, dtype, case), f"{dtype} {M}x{N}")
+
+
+# ---- masked path: rows whose length or start is not a multiple of 16 bytes ----
+
+MASKED_N = [1, 3, 7, 101, 513, 2047, 2049, 5001, 8191, 8193, 20001, 131071]
+
+
+@pytest.mark.parametrize("N", MASKED_N)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "xent"])
+def test_backward_masked_shapes(op, dtype, N):
+    """Ragged rows take the masked kernels: one row per CTA (per cluster of up
+    to 16 CTAs beyond 8192 elements), persistent over the rows."""
+    M = rows_for(N)
+    assert qb.qk_get_plan(OPC[op], DT[dtype], M, N)["path"] == 5
+    case = make_case(op, dtype, M, N, seed=9300 + N)
+    check(op, dtype, case, run_gpu(op, dtype, case), f"masked {dtype} {M}x{N}")
+
+
+@pytest.mark.parametrize("M,N", [(3000, 1001), (400, 20001), (1500, 5001)])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm"])
+def test_backward_masked_many_rows_per_cta(op, M, N):
+    """More rows than resident CTAs (clusters): every CTA walks several rows,
+    reusing both reduction buffers and both phases of the cluster barrier,
+    and RMSNorm's dw partials accumulate over the rows a CTA takes."""
+    plan = qb.qk_get_plan(OPC[op], qb.QK_F32, M, N)
+    assert plan["path"] == 5 and plan["grid"] // plan["cluster"] < M
+    case = make_case(op, "f32", M, N, seed=9400 + N)
+    check(op, "f32", case, run_gpu(op, "f32", case), f"masked {M}x{N}")
+
+
+def _offset(t):
+    """A copy of t whose data starts one element past a 16-byte boundary."""
+    store = torch.empty(t.numel() + 1, dtype=t.dtype, device=DEV)
+    v = store[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "xent"])
+def test_backward_unaligned_pointers(op, dtype):
+    """Aligned N but inputs and outputs one element off a 16-byte boundary."""
+    M, N = 9, 4096
+    case = make_case(op, dtype, M, N, seed=9500)
+    d = {k: v.to(DEV) for k, v in case.items()}
+    code = DT[dtype]
+    if op == "softmax":
+        y, dy = _offset(d["y"]), _offset(d["dy"])
+        dx = _offset(torch.full_like(d["y"], float("nan")))
+        qb.qk_softmax_bwd(y, dy, dx, M, N, code)
+        out = {"dx": dx}
+    elif op == "rmsnorm":
+        x, dy, w = _offset(d["x"]), _offset(d["dy"]), _offset(d["w"])
+        dx = _offset(torch.full_like(d["x"], float("nan")))
+        dw = torch.full((N,), float("nan"), dtype=torch.float32, device=DEV)
+        nbytes = qb.qk_rmsnorm_bwd_workspace_size(M, N, code)
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=DEV)
+        qb.qk_rmsnorm_bwd(x, w, d["rstd"], dy, dx, dw, ws, nbytes, M, N, code)
+        out = {"dx": dx, "dw": dw}
+    else:
+        x = _offset(d["x"])
+        dx = _offset(torch.full_like(d["x"], float("nan")))
+        qb.qk_xent_bwd(x, d["targets"], d["lse"], d["dloss"], dx, M, N, code)
+        out = {"dx": dx}
+    torch.cuda.synchronize()
+    assert qb.qk_get_device_status() == qb.QK_OK
+    check(op, dtype, case, out, "unaligned pointers")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "xent"])
+def test_backward_masked_in_place(op, dtype):
+    case = make_case(op, dtype, 13, 1001, seed=9600)
+    check(op, dtype, case, run_gpu(op, dtype, case, inplace=True), "masked, in place")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_xent_backward_masked_bad_targets(dtype):
+    N = 1001
+    case = make_case("xent", dtype, 6, N, seed=9700)
+    case["targets"] = torch.tensor([-1, N, 0, N - 1, 2 ** 40, 5], dtype=torch.int64)
+    d = {k: v.to(DEV) for k, v in case.items()}
+    dx = torch.empty_like(d["x"])
+    qb.qk_xent_bwd(d["x"], d["targets"], d["lse"], None, dx, 6, N, DT[dtype])  # dloss = 1
+    torch.cuda.synchronize()
+    case["dloss"] = torch.ones(6)
+    check("xent", dtype, case, {"dx": dx}, "masked, bad targets, dloss = 1")
+    assert torch.isnan(dx[[0, 1, 4]]).all() and torch.isfinite(dx[[2, 3, 5]]).all()
+
+
+def test_masked_rows_beyond_the_limit_are_refused():
+    N = 131073  # odd, so masked; beyond 16 clusters x 8192 elements
+    for op, dtype in (("softmax", "bf16"), ("rmsnorm", "bf16")):
+        case = make_case(op, dtype, 1, N, seed=9800)
+        with pytest.raises(qb.QkError) as e:
+            run_gpu(op, dtype, case)
+        assert e.value.status == qb.QK_ERR_UNSUPPORTED
