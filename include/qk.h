@@ -33,8 +33,10 @@
  *  - M == 0 is a no-op returning QK_OK.  N <= 0 or M < 0 is QK_ERR_INVALID_ARG.
  *  - Pointers must be aligned to their element size (QK_ERR_MISALIGNED
  *    otherwise).  The fast path additionally wants 16-byte aligned x, y, w and
- *    N * sizeof(dtype) a multiple of 16; other inputs take a slower masked
- *    path that gives the same results.
+ *    N * sizeof(dtype) a multiple of 16.  Other forward inputs take a shifted
+ *    ring kernel when y has x's alignment modulo 16 (rows start anywhere inside
+ *    a 16-byte vector) and a masked element kernel otherwise; both give the
+ *    same results as the fast path.
  *  - Accumulation is float32; bf16 outputs are rounded to nearest even once.
  */
 #ifndef QK_H_
