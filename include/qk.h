@@ -126,7 +126,9 @@ QK_API qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rs
  *   y      [M, N] dtype, written once; y == x allowed, other overlaps rejected.
  *   mean   [M] float32, may be NULL; rstd [M] float32, may be NULL.
  *   eps    added to the variance; must be finite and >= 0.
- *   Rows up to qk_max_row_elements(QK_OP_LAYERNORM, dtype) elements (1 MiB).
+ *   Any N on the aligned path: rows longer than a cluster holds (1 MiB) are
+ *   streamed through shared memory twice (three HBM passes).  Unaligned rows
+ *   go up to 524,288 elements.
  */
 QK_API qk_status qk_layernorm_fwd(const void* x, const void* w, const void* b, void* y,
                                   float* mean, float* rstd, int64_t M, int64_t N, float eps,

@@ -41,6 +41,9 @@ constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s bound on any in-kerne
 constexpr int kMaxDevices = 64;
 constexpr int kRingMaxVectorsPerCta = 4096;  // 256 threads x 16 vectors, or 512 x 8
 constexpr int64_t kMaxRowBytes = int64_t(kMaxCluster) * kRingMaxVectorsPerCta * 16;  // 1 MiB
+// Masked forward kernel (unaligned rows beyond the shifted kernel): 16
+// clusters of 512 threads x 64 elements.
+constexpr int64_t kMaskedMaxRow = int64_t(kMaxCluster) * 512 * 64;  // 524,288 elements
 // Masked backward softmax / RMSNorm: 16 clusters of 512 threads x 16 elements.
 constexpr int64_t kMaskedBwdMaxRow = int64_t(kMaxCluster) * 512 * 16;  // 131,072 elements
 
@@ -312,12 +315,13 @@ qk_status choose_ring(int op, int64_t NV, int* th, int* tpr, int* vpt, int* cl, 
   return QK_ERR_UNSUPPORTED;
 }
 
-// Rows of the forward softmax / RMSNorm longer than the largest cluster plan
+// Rows of the forward softmax / RMSNorm / LayerNorm longer than the largest cluster plan
 // (64K vectors, 1 MiB) are streamed twice.  A cluster splits each row when
 // there are too few rows to occupy the GPU.
 constexpr int64_t kTwoPassChunkVectors = 256 * 8;  // 32 KB chunks
 bool wants_two_pass(int op, int64_t NV) {
-  return (op == kSoftmax || op == kRmsNorm) && NV > int64_t(kMaxCluster) * kRingMaxVectorsPerCta;
+  return (op == kSoftmax || op == kRmsNorm || op == kOpLayerNorm) &&
+         NV > int64_t(kMaxCluster) * kRingMaxVectorsPerCta;
 }
 
 qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p) {
@@ -328,7 +332,7 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   bool two_pass = false;
   const Override& ov = g_override[op][dt];
   if (ov.on && ov.plan.path == 4) {  // forced two-pass plan (tuning, tests)
-    if (!(op == kSoftmax || op == kRmsNorm)) return QK_ERR_UNSUPPORTED;
+    if (!(op == kSoftmax || op == kRmsNorm || op == kOpLayerNorm)) return QK_ERR_UNSUPPORTED;
     th = ov.plan.threads, tpr = ov.plan.row_threads, vpt = ov.plan.vec_per_thread;
     cl = std::max(1, int(ov.plan.cluster));
     slots = ov.plan.slots;
@@ -384,7 +388,7 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   const uint32_t slot_bytes = uint32_t((item_bytes + 127) / 128 * 128);
   // LayerNorm parameters not held in registers sit after the ring slots.
   int64_t param_bytes = 0;
-  if (op == kOpLayerNorm) {
+  if (op == kOpLayerNorm && !two_pass) {  // streamed rows read w and b through L1
     const int64_t slice = cl > 1 ? (NV + cl - 1) / cl : NV;
     if (vpt > kAffineRegsMaxVpt) param_bytes += param_slice_bytes(slice);
     if (vpt > kLnBiasRegsMaxVpt) param_bytes += param_slice_bytes(slice);
@@ -527,7 +531,8 @@ qk_status plan_direct(int dev, const DeviceInfo& d, int op, int dt, int64_t M, i
 }
 
 int64_t max_row_elements(int op, int dt) {
-  if (streams_rows(op) || op == kSoftmax || op == kRmsNorm) return INT64_MAX;  // streamed rows
+  if (streams_rows(op) || op == kSoftmax || op == kRmsNorm || op == kOpLayerNorm)
+    return INT64_MAX;  // streamed rows
   if (is_bwd(op)) return kMaxRowBytes / 2 / elem_size(dt);  // 512 KiB rows (two inputs)
   return kMaxRowBytes / elem_size(dt);
 }
@@ -779,6 +784,7 @@ qk_status qk_softmax_fwd(const void* x, void* y, int64_t M, int64_t N, qk_dtype 
   a.M = M;
   a.N = N;
   const bool fast = aligned16(x) && aligned16(y) && (N * int64_t(es)) % 16 == 0;
+  if (!fast && N > kMaskedMaxRow) return QK_ERR_UNSUPPORTED;
   return run(kSoftmax, dtype, a, row_path(fast, same_mod16(x, y)), stream);
 }
 
@@ -807,6 +813,7 @@ qk_status qk_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int
   a.eps = eps;
   const bool fast =
       aligned16(x) && aligned16(y) && aligned16(w) && (N * int64_t(es)) % 16 == 0;
+  if (!fast && N > kMaskedMaxRow) return QK_ERR_UNSUPPORTED;
   return run(kRmsNorm, dtype, a, row_path(fast, same_mod16(x, y)), stream);
 }
 
@@ -844,6 +851,7 @@ qk_status qk_layernorm_fwd(const void* x, const void* w, const void* b, void* y,
   a.eps = eps;
   const bool fast = aligned16(x) && aligned16(y) && aligned16(w) && aligned16(b) &&
                     (N * int64_t(es)) % 16 == 0;
+  if (!fast && N > kMaskedMaxRow) return QK_ERR_UNSUPPORTED;
   return run(kOpLayerNorm, dtype, a, row_path(fast, same_mod16(x, y)), stream);
 }
 

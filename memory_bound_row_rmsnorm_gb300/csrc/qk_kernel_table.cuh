@@ -52,7 +52,7 @@ const KernelEntry kTable[] = {
     QK_RING(512, 512, 4, true),
     QK_RING(512, 512, 8, true),
     QK_RING(256, 256, 16, true),
-#if QK_OP == 0 || QK_OP == 1
+#if QK_OP != 2
     // rows longer than a cluster holds: streamed twice in 32 KB chunks
     QK_RING2(256, 256, 8, false),
     QK_RING2(256, 256, 8, true),

@@ -69,7 +69,7 @@ __device__ __forceinline__ void merge_partials(const float2* p, int n, float& m,
   }
 }
 
-// TWO_PASS (softmax, RMSNorm rows longer than a cluster holds): every row
+// TWO_PASS (softmax, RMSNorm, LayerNorm rows longer than a cluster holds): every row
 // slice is streamed through the ring twice in chunks -- the first pass
 // accumulates the reduction, the second re-reads each chunk and writes its
 // outputs with the row's totals (three HBM passes instead of two).
@@ -86,12 +86,13 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
                 "a row group is whole warps or a power-of-two part of one");
   static_assert(!CLUSTER || TPR == THREADS, "a clustered row spans the whole CTA");
   static_assert(NW <= 16, "block-reduction buffer holds 16 warps");
-  static_assert(!TWO_PASS || (TPR == THREADS && (OP == kSoftmax || OP == kRmsNorm)),
-                "two passes: softmax and RMSNorm, one row per CTA");
+  static_assert(!TWO_PASS || (TPR == THREADS && OP != kXent),
+                "two passes: softmax, RMSNorm and LayerNorm, one row per CTA");
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);                  // [kMaxSlots]
   uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + 8 * kMaxSlots);  // [2]
+  float* cnt_red = reinterpret_cast<float*>(smem + 384);               // [2][16] LayerNorm counts
   float2* red = reinterpret_cast<float2*>(smem + 512);                 // [2][16]
   float2* xbuf = reinterpret_cast<float2*>(smem + 768);                // [2][kMaxCluster]
   unsigned char* ring = smem + kSmemHeader;
@@ -194,8 +195,8 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   // registers it stages in shared memory, so that the finish never waits on
   // a global load.
   constexpr bool kBiasInRegs = OP == kLayerNorm && VPT <= kLnBiasRegsMaxVpt && !TWO_PASS;
-  constexpr bool kWeightInSmem = OP == kLayerNorm && !kWeightInRegs;
-  constexpr bool kBiasInSmem = OP == kLayerNorm && !kBiasInRegs;
+  constexpr bool kWeightInSmem = OP == kLayerNorm && !kWeightInRegs && !TWO_PASS;
+  constexpr bool kBiasInSmem = OP == kLayerNorm && !kBiasInRegs && !TWO_PASS;
   uint4 wv[kWeightInRegs ? VPT : 1];
   uint4 bv[kBiasInRegs ? VPT : 1];
   uint4* wsm = reinterpret_cast<uint4*>(ring + size_t(S) * a.slot_bytes);
@@ -228,7 +229,8 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   uint4 xr[VPT];                       // raw input vectors of the current row (chunk)
   float ef[kKeepExp ? VPT * E : 1];    // softmax: exp(x - thread max)
   float run_m = kNegInf, run_s = 0.f;  // cross-entropy, two-pass softmax: running pair
-  float run_ss = 0.f;                  // two-pass RMSNorm: running sum of squares
+  float run_ss = 0.f;                  // two-pass RMSNorm: running sum of squares (LayerNorm: M2)
+  float run_n = 0.f;                   // two-pass LayerNorm: running count (mean in run_m)
   float tot_a = 0.f, tot_b = 0.f;      // two-pass: the row's totals for the second pass
   float xt = 0.f;                      // cross-entropy: x[target] if this thread holds it
   bool own_t = false;
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   bool ln_full = false;
   float ln_wc = 0.f, ln_cc = 0.f;
   if constexpr (OP == kLayerNorm) {
-    ln_full = (nv == int64_t(TPR) * VPT);
+    ln_full = !TWO_PASS && (nv == int64_t(TPR) * VPT);
     if constexpr (WPG > 1) {
       const int w = lane % WPG;
       int c = 0;
@@ -353,6 +355,14 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       pn = cnt;
       pm = ln_full ? sum : mu;  // full rows reduce in sum form (below)
       ps = q2.x + q2.y;
+      if constexpr (TWO_PASS) {  // fold the chunk into the thread's running (count, mean, M2)
+        if (j == 0) {
+          run_n = pn, run_m = pm, run_ss = ps;
+        } else {
+          welford_merge(run_n, run_m, run_ss, pn, pm, ps);
+        }
+        pn = run_n, pm = run_m, ps = run_ss;
+      }
     } else if constexpr (OP == kRmsNorm) {
       float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
@@ -443,6 +453,9 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         } else {
           group_welford<GW>(pn, pm, ps);
         }
+        // Streamed rows: the counts of the warps no longer follow from the
+        // geometry of one slot, so they travel through shared memory.
+        if (TWO_PASS && WPG > 1 && lane == 0) cnt_red[ibit * 16 + warp] = pn;
       } else {
         warp_reduce<OP, GW>(pm, ps);
       }
@@ -492,13 +505,27 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
                 o[e] = v.x;
                 o[e + 1] = v.y;
               }
-            } else {  // (x * rstd) * w
+            } else if constexpr (OP == kRmsNorm) {  // (x * rstd) * w
               float w[E];
               V::unpack(__ldg(wg2 + l + k * TPR), w);
 #pragma unroll
               for (int e = 0; e < E; e += 2) {
                 const float2 v = mul2(mul2(make_float2(f[e], f[e + 1]), make_float2(tot_a, tot_a)),
                                       make_float2(w[e], w[e + 1]));
+                o[e] = v.x;
+                o[e + 1] = v.y;
+              }
+            } else {  // LayerNorm: (x * rstd - mean * rstd) * w + b
+              float w[E], bb[E];
+              V::unpack(__ldg(wg2 + l + k * TPR), w);
+              V::unpack(a.bias != nullptr ? __ldg(static_cast<const uint4*>(a.bias) + cbase + l + k * TPR)
+                                          : make_uint4(0u, 0u, 0u, 0u),
+                        bb);
+#pragma unroll
+              for (int e = 0; e < E; e += 2) {
+                const float2 v = fma2(fma2(make_float2(f[e], f[e + 1]), make_float2(tot_a, tot_a),
+                                           make_float2(tot_b, tot_b)),
+                                      make_float2(w[e], w[e + 1]), make_float2(bb[e], bb[e + 1]));
                 o[e] = v.x;
                 o[e + 1] = v.y;
               }
@@ -521,7 +548,7 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         if (ln_full) {
           group_welford_sum<WPG, 32 * VPT * E>(pm, ps);
         } else {
-          pn = ln_wc;
+          pn = TWO_PASS ? cnt_red[row_ibit * 16 + g * WPG + lane % WPG] : ln_wc;
           group_welford<WPG>(pn, pm, ps);
         }
       }
@@ -577,9 +604,16 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       if constexpr (OP == kSoftmax) {
         tot_a = (pm == kNegInf) ? 0.f : pm * kLog2e;  // M log2 e
         tot_b = __fdividef(1.f, ps);                  // 1 / S
-      } else {
+      } else if constexpr (OP == kRmsNorm) {
         tot_a = rsqrtf(fmaf(ps, a.inv_n, a.eps));     // rstd
         if (l == 0 && rank == 0 && row_ok && a.rstd != nullptr) a.rstd[row] = tot_a;
+      } else {                                        // LayerNorm
+        tot_a = rsqrtf(fmaf(ps, a.inv_n, a.eps));     // rstd
+        tot_b = -pm * tot_a;                          // -mean * rstd
+        if (l == 0 && rank == 0 && row_ok) {
+          if (a.rstd != nullptr) a.rstd[row] = tot_a;
+          if (a.mean != nullptr) a.mean[row] = pm;
+        }
       }
       continue;
     }

@@ -53,8 +53,8 @@ def test_max_row_elements(lib):
     assert qb.qk_max_row_elements(qb.QK_OP_SOFTMAX_BWD, qb.QK_F32) == 131072
     assert qb.qk_max_row_elements(qb.QK_OP_RMSNORM_BWD, qb.QK_BF16) == 262144
     assert qb.qk_max_row_elements(qb.QK_OP_XENT_BWD, qb.QK_F32) == 2 ** 63 - 1
-    assert qb.qk_max_row_elements(qb.QK_OP_LAYERNORM, qb.QK_F32) == 262144  # 1 MiB rows
-    assert qb.qk_max_row_elements(qb.QK_OP_LAYERNORM, qb.QK_BF16) == 524288
+    assert qb.qk_max_row_elements(qb.QK_OP_LAYERNORM, qb.QK_F32) == 2 ** 63 - 1  # streamed twice
+    assert qb.qk_max_row_elements(qb.QK_OP_LAYERNORM, qb.QK_BF16) == 2 ** 63 - 1
 
 
 # Fake, never-dereferenced device addresses: every call below must be refused
@@ -177,8 +177,11 @@ def test_layernorm_argument_checks(lib):
     for eps in (-1.0, float("nan"), float("inf")):
         assert ln(*ok, 4, 4, eps, F, None) == qb.QK_ERR_INVALID_ARG
     assert ln(*ok, 4, 4, 1e-5, 5, None) == qb.QK_ERR_INVALID_ARG
-    assert ln(*ok, 4, 262148, 1e-5, F, None) == qb.QK_ERR_UNSUPPORTED  # beyond 1 MiB rows
-    assert ln(*ok, 4, 524292, 1e-5, B, None) == qb.QK_ERR_UNSUPPORTED
+    G = 1 << 30  # unaligned rows beyond the masked kernel's 524,288 elements
+    far = [A, A + G, A + 2 * G, A + 3 * G, A + 4 * G, A + 5 * G]
+    assert ln(*far, 4, 524289, 1e-5, B, None) == qb.QK_ERR_UNSUPPORTED
+    assert ln(*far, 4, 524291, 1e-5, F, None) == qb.QK_ERR_UNSUPPORTED
+    assert lib.qk_softmax_fwd(A, A + G, 4, 524289, B, None) == qb.QK_ERR_UNSUPPORTED
     for i, off in ((0, 2), (2, 1), (4, 2), (5, 1)):  # x, b, mean, rstd misaligned
         bad = list(ok)
         bad[i] += off

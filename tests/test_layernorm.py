@@ -106,7 +106,8 @@ def test_optional_bias_and_stats(dtype, N, bias, stats):
 @pytest.mark.parametrize("N", [65536, 131072, 262144, 524288, 262148, 300001])
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_long_rows(dtype, N):
-    """Clustered rows up to 1 MiB; masked long rows; beyond 1 MiB is refused."""
+    """Clustered rows up to 1 MiB, rows beyond it streamed twice, unaligned long
+    rows on the shifted or the masked kernel."""
     if N > qb.qk_max_row_elements(OP, DT_CODE[dtype]):
         x = torch.empty((1, N), dtype=syn.DTYPES[dtype], device=DEV)
         w = torch.empty(N, dtype=syn.DTYPES[dtype], device=DEV)
@@ -202,17 +203,6 @@ def test_forced_plans(dtype, plan):
         qb.qk_set_plan_override(OP, DT_CODE[dtype], None)
 
 
-def test_two_pass_plans_are_refused():
-    plan = dict(path=4, threads=256, row_threads=256, vec_per_thread=8, cluster=1, slots=2)
-    qb.qk_set_plan_override(OP, qb.QK_F32, plan)
-    try:
-        with pytest.raises(qb.QkError) as e:
-            qb.qk_get_plan(OP, qb.QK_F32, 4, 4096)
-        assert e.value.status == qb.QK_ERR_UNSUPPORTED
-    finally:
-        qb.qk_set_plan_override(OP, qb.QK_F32, None)
-
-
 def test_tensor_helper():
     inp = syn.make_inputs("layernorm", "bf16", 33, 1536, 1800, "cpu")
     dev = {k: v.to(DEV) for k, v in inp.items()}
@@ -240,3 +230,41 @@ def test_benchmark_workload_sampled_rows():
     assert torch.isfinite(out["y"]).all()
     assert (out["mean"].abs() <= 1.5).all()            # row offsets are in [-1, 1]
     assert ((out["rstd"] > 0.8) & (out["rstd"] < 1.25)).all()  # unit variance rows
+
+
+# Rows longer than a cluster holds stream through shared memory twice; the
+# forced plans give several chunks per slice, ring reuse, clusters splitting
+# the row, a ragged last chunk and a short last slice.
+TWO_PASS_PLANS = [
+    dict(path=4, threads=256, row_threads=256, vec_per_thread=8, cluster=1, slots=2, grid=3),
+    dict(path=4, threads=256, row_threads=256, vec_per_thread=8, cluster=4, slots=2, grid=8),
+    dict(path=4, threads=256, row_threads=256, vec_per_thread=8, cluster=16, slots=3, grid=16),
+]
+
+
+@pytest.mark.parametrize("pi", range(len(TWO_PASS_PLANS)))
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_forced_two_pass(dtype, pi):
+    plan = TWO_PASS_PLANS[pi]
+    E = 4 if dtype == "f32" else 8
+    N = (5 * 2048 * plan["cluster"] + 37) * E  # about 5 chunks per slice, ragged
+    qb.qk_set_plan_override(OP, DT_CODE[dtype], plan)
+    try:
+        got = qb.qk_get_plan(OP, DT_CODE[dtype], 7, N)
+        assert got["path"] == 4 and got["cluster"] == plan["cluster"] and got["chunks"] >= 5
+        full_check(dtype, 7, N, seed=2100 + pi, what=f"two-pass plan {plan}")
+    finally:
+        qb.qk_set_plan_override(OP, DT_CODE[dtype], None)
+
+
+@pytest.mark.parametrize("M", [1, 5, 400])
+def test_rows_beyond_a_cluster(M):
+    """Default two-pass plans: split over a cluster when there are few rows,
+    one CTA per row when there are many."""
+    N = 3 * 2 ** 19 if M <= 5 else 2 ** 18 + 4096
+    assert qb.qk_get_plan(OP, qb.QK_F32, M, N)["path"] == 4
+    inp = syn.make_inputs("layernorm", "f32", M, N, 2200 + M, "cpu")
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    out = run_gpu(dev, "f32")
+    rows = None if M <= 5 else torch.tensor([0, 1, 199, 398, 399])
+    check(inp, out, "f32", rows=rows, what=f"two-pass {M}x{N}")
