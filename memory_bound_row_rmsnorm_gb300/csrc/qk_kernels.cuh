@@ -324,8 +324,10 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       // (count, mean, M2) of this thread's elements: the mean first, then the
       // squared deviations from it, both over the registers.  Padding is 0,
       // so it adds nothing to the sum; it is left out of the count and of M2.
+      // (Four independent accumulator pairs: short dependency chains.)
       constexpr float kInvFull = 1.f / float(E * VPT);  // a power of two: exact
-      float2 s2 = make_float2(0.f, 0.f);
+      float2 s4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
       float cnt = 0.f;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -333,14 +335,19 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         V::unpack(xr[k], f);
         cnt += valid[k] ? float(E) : 0.f;
 #pragma unroll
-        for (int e = 0; e < E; e += 2) s2 = add2(s2, make_float2(f[e], f[e + 1]));
+        for (int e = 0; e < E; e += 2) {
+          const int c = ((k * E + e) / 2) & 3;
+          s4[c] = add2(s4[c], make_float2(f[e], f[e + 1]));
+        }
       }
+      const float2 s2 = add2(add2(s4[0], s4[1]), add2(s4[2], s4[3]));
       const float sum = s2.x + s2.y;
       // Full rows: every thread holds VPT vectors (a padded thread of a row
       // that is not written has sum 0 and M2 0, which harms nothing).
       const float mu = ln_full ? sum * kInvFull : (cnt > 0.f ? __fdiv_rn(sum, cnt) : 0.f);
       const float2 nmu = make_float2(-mu, -mu);
-      float2 q2 = make_float2(0.f, 0.f);
+      float2 q4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!ln_full && !valid[k]) continue;
@@ -348,10 +355,12 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         V::unpack(xr[k], f);
 #pragma unroll
         for (int e = 0; e < E; e += 2) {
+          const int c = ((k * E + e) / 2) & 3;
           const float2 d = add2(make_float2(f[e], f[e + 1]), nmu);
-          q2 = fma2(d, d, q2);
+          q4[c] = fma2(d, d, q4[c]);
         }
       }
+      const float2 q2 = add2(add2(q4[0], q4[1]), add2(q4[2], q4[3]));
       pn = cnt;
       pm = ln_full ? sum : mu;  // full rows reduce in sum form (below)
       ps = q2.x + q2.y;
