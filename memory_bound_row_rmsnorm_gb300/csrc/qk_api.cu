@@ -1,7 +1,8 @@
 // qk_api.cu -- the C ABI of libqk.so: argument checks, launch plans, launches.
 //
 // Host side only: every element of every row is processed by the kernels in
-// qk_kernels.cuh; nothing here touches row data.
+// qk_kernels.cuh, qk_shifted_kernels.cuh and qk_bwd_kernels.cuh; nothing here
+// touches row data.
 #include <cuda_runtime.h>
 
 #include <algorithm>
