@@ -425,15 +425,18 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
 
 // Rows that do not start on a 16-byte boundary (shifted ring kernel): each
 // step copies the aligned range around its elements, so a row group must hold
-// ceil((15 + slice bytes) / 16) vectors.  Row groups from 8 to 256 threads of 4
-// vectors, then 256 x 8, then clusters of those for softmax / RMSNorm /
-// LayerNorm; cross-entropy streams longer rows in chunks of 2047 vectors.
+// ceil((15 + slice bytes) / 16) vectors: one more than the aligned row when
+// it is misaligned, hence row groups of 5 (or 9) vectors a thread.  Row groups
+// from 8 to 256 threads of 5 vectors, then 256 x 9, then the smallest cluster
+// of 256 x 9 CTAs (256 x 8 when the slice fits: fewer registers) for softmax / RMSNorm /
+// LayerNorm; cross-entropy streams longer rows in equal chunks of at most 2303
+// vectors.
 struct ShiftChoice {
   int threads, row_threads, vec_per_thread, slots;
 };
 constexpr ShiftChoice kShiftTable[] = {
-    {256, 8, 4, 2},   {256, 16, 4, 2},  {256, 32, 4, 2}, {256, 64, 4, 2},
-    {256, 128, 4, 2}, {256, 256, 4, 2}, {256, 256, 8, 1},
+    {256, 8, 5, 2},   {256, 16, 5, 2},  {256, 32, 5, 2}, {256, 64, 5, 2},
+    {256, 128, 5, 2}, {256, 256, 5, 2}, {256, 256, 9, 1},
 };
 int64_t span_vectors(int64_t elems, int es) { return (15 + elems * es + 15) / 16; }
 
@@ -450,13 +453,14 @@ qk_status plan_shifted(int dev, const DeviceInfo& d, int op, int dt, int64_t M, 
     const int64_t che = (int64_t(kShiftTable[pick].row_threads) * kShiftTable[pick].vec_per_thread - 1) *
                         (16 / es);
     k = int((N + che - 1) / che);
-  } else if (pick < 0) {  // clusters of 256 x 8
-    pick = kinds - 1;
-    const int64_t cap = int64_t(kShiftTable[pick].row_threads) * kShiftTable[pick].vec_per_thread;
-    while (cl <= kMaxCluster && span_vectors((N + cl - 1) / cl, es) > cap) cl <<= 1;
-    if (cl > kMaxCluster) return QK_ERR_UNSUPPORTED;
   }
-  const ShiftChoice& c = kShiftTable[pick];
+  ShiftChoice c = pick >= 0 ? kShiftTable[pick] : ShiftChoice{256, 256, 8, 1};
+  if (pick < 0) {  // the smallest cluster of 256 x 9 CTAs, as 256 x 8 when that fits too
+    cl = 2;
+    while (cl <= kMaxCluster && span_vectors((N + cl - 1) / cl, es) > 256 * 9) cl <<= 1;
+    if (cl > kMaxCluster) return QK_ERR_UNSUPPORTED;
+    c.vec_per_thread = span_vectors((N + cl - 1) / cl, es) <= 256 * 8 ? 8 : 9;
+  }
   const KernelEntry* ke = find_kernel(op, dt, 6, c.threads, c.row_threads, c.vec_per_thread, cl > 1);
   if (ke == nullptr) return QK_ERR_UNSUPPORTED;
   const int R = c.threads / c.row_threads;
@@ -627,6 +631,7 @@ qk_status run(int op, int dt, RowArgs a, int path, void* stream) {
   }
   const Plan& p = c.plan;
   a.chunks = p.chunks;
+  a.chunk_elems = (a.N + p.chunks - 1) / p.chunks;
   a.slots = p.slots;
   a.slot_bytes = p.slot_bytes;
   a.num_items = p.num_items;

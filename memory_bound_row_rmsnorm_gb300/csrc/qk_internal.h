@@ -27,6 +27,7 @@ struct RowArgs {
   float z_loss;         // cross-entropy: coefficient of z * lse^2 added to the loss (0: none)
   int64_t ignore_index; // cross-entropy: rows with this target give loss 0 (INT64_MIN: none)
   int32_t chunks;       // ring slots one row slice spans (streamed rows), else 1
+  int64_t chunk_elems;  // shifted kernel, streamed rows: elements of one chunk, ceil(N / chunks)
   int32_t slots;        // ring slots per CTA
   uint32_t slot_bytes;  // bytes per ring slot (multiple of 128)
   int64_t num_items;    // work items: row blocks of threads/row_threads rows, or rows

@@ -58,15 +58,17 @@ const KernelEntry kTable[] = {
     QK_RING2(256, 256, 8, true),
 #endif
 #endif
-    QK_SHIFT(256, 8, 4, false),
-    QK_SHIFT(256, 16, 4, false),
-    QK_SHIFT(256, 32, 4, false),
-    QK_SHIFT(256, 64, 4, false),
-    QK_SHIFT(256, 128, 4, false),
-    QK_SHIFT(256, 256, 4, false),
-    QK_SHIFT(256, 256, 8, false),
+    // one vector more than a power of two: a misaligned row of 2^k vectors spans 2^k + 1
+    QK_SHIFT(256, 8, 5, false),
+    QK_SHIFT(256, 16, 5, false),
+    QK_SHIFT(256, 32, 5, false),
+    QK_SHIFT(256, 64, 5, false),
+    QK_SHIFT(256, 128, 5, false),
+    QK_SHIFT(256, 256, 5, false),
+    QK_SHIFT(256, 256, 9, false),
 #if QK_OP != 2
     QK_SHIFT(256, 256, 8, true),
+    QK_SHIFT(256, 256, 9, true),
 #endif
     QK_DIRECT(128, 4, false),
     QK_DIRECT(256, 16, false),

@@ -35,8 +35,19 @@
 
 namespace qk {
 
+// Resident CTAs per SM asked of the register allocator (256-thread CTAs):
+// left alone it gave some configurations 110-118 registers and others 74-80
+// for the same code, i.e. two CTAs per SM instead of three.  These requests
+// compile without spilling: 4 (5 vectors a thread) and 3 (8-9 vectors), and
+// 3 and 2 for LayerNorm, which carries counts and a bias.
+template <int OP, int VPT>
+constexpr int shifted_min_blocks() {
+  return OP == kLayerNorm ? (VPT >= 8 ? 2 : 3) : (VPT >= 8 ? 3 : 4);
+}
+
 template <int OP, typename T, int THREADS, int TPR, int VPT, bool CLUSTER>
-__global__ void __launch_bounds__(THREADS) shifted_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
+    shifted_kernel(const RowArgs a) {
   using V = Vec16<T>;
   constexpr int E = V::kElems;
   constexpr int ES = int(sizeof(T));
@@ -45,7 +56,6 @@ __global__ void __launch_bounds__(THREADS) shifted_kernel(const RowArgs a) {
   constexpr int GW = TPR < 32 ? TPR : 32;
   constexpr int R = THREADS / TPR;
   constexpr int64_t CH = int64_t(TPR) * VPT;   // slot vectors a row group holds
-  constexpr int64_t CHE = (CH - 1) * E;        // elements of one chunk of a streamed row
   static_assert((TPR % 32 == 0 || 32 % TPR == 0) && THREADS % TPR == 0 && TPR >= 4, "row groups");
   static_assert(!CLUSTER || TPR == THREADS, "a clustered row spans the whole CTA");
   static_assert(NW <= 16, "block-reduction buffer holds 16 warps");
@@ -64,6 +74,9 @@ __global__ void __launch_bounds__(THREADS) shifted_kernel(const RowArgs a) {
   const int64_t M = a.M, N = a.N;
   const int S = a.slots;
   const int64_t K = a.chunks;  // chunks per row slice (cross-entropy streaming), else 1
+  // Elements of one chunk of a streamed row (a.chunk_elems): the row in K
+  // equal parts, each at most (CH - 1) * E elements so that its aligned copy
+  // fits CH vectors.
 
   uint32_t C = 1, rank = 0, cid = blockIdx.x, ncl = gridDim.x;
   if constexpr (CLUSTER) {
@@ -76,6 +89,7 @@ __global__ void __launch_bounds__(THREADS) shifted_kernel(const RowArgs a) {
   const int64_t SE = (N + C - 1) / C;
   const int64_t e0 = min(N, int64_t(rank) * SE);
   const int64_t ne = min(N, e0 + SE) - e0;
+  const int64_t CHE = a.chunk_elems;  // streamed rows never span a cluster: ne = N
 
   const int64_t n_local = a.num_items > int64_t(cid) ? (a.num_items - 1 - cid) / ncl + 1 : 0;
   const int64_t q_total = n_local * K;
@@ -447,9 +461,9 @@ __global__ void __launch_bounds__(THREADS) shifted_kernel(const RowArgs a) {
         for (int e = 0; e < E; e += 2) {
           const float2 x2 = make_float2(f[e], f[e + 1]);
           float2 v;
-          if constexpr (OP == kSoftmax) {  // exp(x - m_t) * scale
-            const float2 t = fma2(x2, make_float2(kLog2e, kLog2e), make_float2(-sb2, -sb2));
-            v = mul2(make_float2(exp2_approx(t.x), exp2_approx(t.y)), a2);
+          if constexpr (OP == kSoftmax) {  // exp(x - m_t) * scale (scalar: fewer live registers)
+            v = make_float2(exp2_approx(fmaf(x2.x, kLog2e, -sb2)) * sa,
+                            exp2_approx(fmaf(x2.y, kLog2e, -sb2)) * sa);
           } else if constexpr (OP == kRmsNorm) {  // (x * rstd) * w
             v = mul2(mul2(x2, a2), make_float2(w[e], w[e + 1]));
           } else {  // (x * rstd - mean * rstd) * w + b

@@ -37,9 +37,10 @@ def shifted_copy(t, elems, fill=None):
 
 
 # Lengths around every plan boundary of the shifted kernel (row groups of
-# 8 ... 256 threads, 256 x 8, clusters of 2 ... 16, streamed cross-entropy).
-SHIFT_N = [1, 5, 9, 60, 123, 250, 251, 500, 1003, 1021, 2045, 4093, 4097, 8185, 16379,
-           16385, 32761, 50257, 65537, 131071, 250001]
+# 8 ... 256 threads of 5 vectors, 256 x 9, clusters of 2 ... 16, streamed
+# cross-entropy in equal chunks).
+SHIFT_N = [1, 5, 9, 60, 123, 153, 251, 311, 313, 627, 1003, 1263, 2045, 2547, 4097, 5111,
+           9209, 10227, 16385, 18415, 18419, 32761, 50257, 65537, 131071, 250001]
 
 
 @pytest.mark.parametrize("N", SHIFT_N)
@@ -66,7 +67,7 @@ def test_shifted_layernorm(dtype, N):
 def test_plan_is_the_shifted_kernel(op, dtype):
     """Unaligned N (with aligned pointers) takes path 6 up to its capacity."""
     assert qb.qk_get_plan(OP_CODE[op], DT_CODE[dtype], 64, 4097)["path"] == 6
-    if op != "xent":  # rows too long for 16 CTAs of 2048 vectors fall back to the masked kernel
+    if op != "xent":  # rows too long for 16 CTAs of 2304 vectors fall back to the masked kernel
         assert qb.qk_get_plan(OP_CODE[op], DT_CODE[dtype], 4, 400003)["path"] == 2
 
 
