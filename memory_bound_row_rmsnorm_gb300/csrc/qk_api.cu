@@ -444,11 +444,12 @@ qk_status plan_shifted(int dev, const DeviceInfo& d, int op, int dt, int64_t M, 
   const int es = elem_size(dt);
   const int kinds = int(sizeof(kShiftTable) / sizeof(ShiftChoice));
   const int last = kinds - 1;
+  const bool streams = (op == kXent || op == kOpXentBwd);  // no row reduction to keep
   int pick = -1, cl = 1, k = 1;
   for (int i = 0; i <= last && pick < 0; ++i)
     if (span_vectors(N, es) <= int64_t(kShiftTable[i].row_threads) * kShiftTable[i].vec_per_thread)
       pick = i;
-  if (pick < 0 && op == kXent) {  // stream the row in chunks of (cap - 1) vectors
+  if (pick < 0 && streams) {  // stream the row in chunks of (cap - 1) vectors
     pick = last;
     const int64_t che = (int64_t(kShiftTable[pick].row_threads) * kShiftTable[pick].vec_per_thread - 1) *
                         (16 / es);
@@ -613,8 +614,9 @@ qk_status run(int op, int dt, RowArgs a, int path, void* stream) {
     uint64_t gen = 0;
     Plan plan;
   };
-  thread_local Cached cache[4][2][3];  // (softmax, RMSNorm, x-entropy, LayerNorm) x dtype x path
-  Cached& c = cache[op == kOpLayerNorm ? 3 : op][dt][path];
+  // (softmax, RMSNorm, x-entropy, LayerNorm, x-entropy backward) x dtype x path
+  thread_local Cached cache[5][2][3];
+  Cached& c = cache[op == kOpLayerNorm ? 3 : op == kOpXentBwd ? 4 : op][dt][path];
   const uint64_t gen = g_override_gen.load(std::memory_order_acquire);
   if (!(c.dev == dev && c.M == a.M && c.N == a.N && c.gen == gen)) {
     Plan np;
@@ -622,7 +624,7 @@ qk_status run(int op, int dt, RowArgs a, int path, void* stream) {
       st = plan_ring(dev, *d, op, dt, a.M, a.N, &np);
     } else if (path == kPathShifted) {
       st = plan_shifted(dev, *d, op, dt, a.M, a.N, &np);
-      if (st == QK_ERR_UNSUPPORTED) st = plan_direct(dev, *d, op, dt, a.M, a.N, &np);
+      if (st == QK_ERR_UNSUPPORTED && !is_bwd(op)) st = plan_direct(dev, *d, op, dt, a.M, a.N, &np);
     } else {
       st = plan_direct(dev, *d, op, dt, a.M, a.N, &np);
     }
@@ -1031,6 +1033,20 @@ qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float
       overlap(dlogits, bytes, dloss, M * 4))
     return QK_ERR_INVALID_ARG;
   const bool fast = bwd_aligned(dtype, N, {logits, dlogits});
+  if (!fast && same_mod16(logits, dlogits)) {  // the shifted ring kernel, as in the forward pass
+    RowArgs r = {};
+    r.x = logits;
+    r.y = dlogits;
+    r.lse = const_cast<float*>(lse);  // read only
+    r.dloss = dloss;
+    r.target = targets;
+    r.M = M;
+    r.N = N;
+    r.ignore_index = ignore;
+    r.z_loss = z;
+    st = run(kOpXentBwd, dtype, r, kPathShifted, stream);
+    if (st != QK_ERR_UNSUPPORTED) return st;
+  }
   BwdArgs a = {};
   a.in0 = logits;
   a.target = targets;
@@ -1087,8 +1103,9 @@ qk_status qk_get_plan(qk_op op, qk_dtype dtype, int64_t M, int64_t N, qk_plan* p
   Plan p;
   if (fast) {
     st = plan_ring(dev, *d, op, dtype, m, N, &p);
-  } else if (is_bwd(op)) {
-    st = plan_direct_bwd(dev, *d, op, dtype, m, N, &p);
+  } else if (is_bwd(op)) {  // cross-entropy: the shifted kernel when it fits, else the masked one
+    st = op == kOpXentBwd ? plan_shifted(dev, *d, op, dtype, m, N, &p) : QK_ERR_UNSUPPORTED;
+    if (st == QK_ERR_UNSUPPORTED) st = plan_direct_bwd(dev, *d, op, dtype, m, N, &p);
   } else {  // x and y 16-byte aligned, N not: the shifted ring, else the masked kernel
     st = plan_shifted(dev, *d, op, dtype, m, N, &p);
     if (st == QK_ERR_UNSUPPORTED) st = plan_direct(dev, *d, op, dtype, m, N, &p);

@@ -3,10 +3,14 @@
 #pragma once
 
 #include "qk_bwd_kernels.cuh"
+#include "qk_shifted_kernels.cuh"
 
 #define QK_BWD(TH, TPR, VPT, CL) \
   {3, TH, TPR, VPT, CL, reinterpret_cast<const void*>(&bwd_kernel<QK_BOP, QK_T, TH, TPR, VPT, CL>)}
 // Masked path (path 5): (threads, elements per thread, clustered).
+#define QK_SHIFT_GRAD(TH, TPR, VPT) \
+  {6, TH, TPR, VPT, false,                 \
+   reinterpret_cast<const void*>(&shifted_kernel<kXentGrad, QK_T, TH, TPR, VPT, false>)}
 #define QK_BWD_DIRECT(TH, EPT, CL) \
   {5, TH, TH, EPT, CL, reinterpret_cast<const void*>(&bwd_direct_kernel<QK_BOP, QK_T, TH, EPT, CL>)}
 
@@ -29,6 +33,10 @@ const KernelEntry kBwdTable[] = {
 #endif
 #if QK_BOP == 12
     QK_BWD_DIRECT(256, 8, false),
+    // unaligned rows whose dlogits share the logits' alignment (path 6)
+    QK_SHIFT_GRAD(256, 8, 5),   QK_SHIFT_GRAD(256, 16, 5),  QK_SHIFT_GRAD(256, 32, 5),
+    QK_SHIFT_GRAD(256, 64, 5),  QK_SHIFT_GRAD(256, 128, 5), QK_SHIFT_GRAD(256, 256, 5),
+    QK_SHIFT_GRAD(256, 256, 9),
 #else
     QK_BWD_DIRECT(128, 4, false),  QK_BWD_DIRECT(256, 8, false),  QK_BWD_DIRECT(512, 16, false),
     QK_BWD_DIRECT(512, 16, true),

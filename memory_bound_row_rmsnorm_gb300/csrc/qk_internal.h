@@ -6,7 +6,8 @@
 namespace qk {
 
 // Kernel-side operator codes (the ABI numbers LayerNorm 6; see qk_api.cu).
-enum Op : int { kSoftmax = 0, kRmsNorm = 1, kXent = 2, kLayerNorm = 3 };
+// kXentGrad: cross-entropy backward on the shifted kernel (unaligned rows).
+enum Op : int { kSoftmax = 0, kRmsNorm = 1, kXent = 2, kLayerNorm = 3, kXentGrad = 4 };
 enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Everything a row kernel needs, passed by value as its only parameter.
@@ -19,7 +20,8 @@ struct RowArgs {
   float* mean;            // [M] LayerNorm row mean, may be null
   const int64_t* target;  // [M] cross-entropy targets
   float* loss;            // [M] cross-entropy loss
-  float* lse;             // [M] cross-entropy log-sum-exp, may be null
+  float* lse;             // [M] cross-entropy log-sum-exp, may be null (kXentGrad: input)
+  const float* dloss;     // [M] kXentGrad: upstream gradient, null for 1
   int64_t M;
   int64_t N;
   float eps;

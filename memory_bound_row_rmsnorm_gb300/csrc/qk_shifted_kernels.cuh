@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
   static_assert((TPR % 32 == 0 || 32 % TPR == 0) && THREADS % TPR == 0 && TPR >= 4, "row groups");
   static_assert(!CLUSTER || TPR == THREADS, "a clustered row spans the whole CTA");
   static_assert(NW <= 16, "block-reduction buffer holds 16 warps");
-  static_assert(!(CLUSTER && OP == kXent), "cross-entropy rows are streamed, not split");
+  static_assert(!(CLUSTER && (OP == kXent || OP == kXentGrad)), "cross-entropy rows are streamed, not split");
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -186,6 +186,8 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
     const int64_t row0 = (K > 1) ? int64_t(cid) : int64_t(cid) * R + g;
     if (q_total > 0 && row0 < M) t_next = __ldg(a.target + row0);
   }
+  float g_lb = 0.f, g_zf = 1.f, g_gv = 1.f;  // kXentGrad: lse log2 e, 1 + 2 z lse, upstream factor
+  int64_t g_t = -1;                          // kXentGrad: the row's target
   float ln_cc = 0.f;  // LayerNorm: elements of cluster rank (lane % 16)
   if constexpr (OP == kLayerNorm && CLUSTER) {
     const uint32_t r = uint32_t(lane) & 15u;
@@ -228,6 +230,61 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         const int i0 = (vb + lv) * E;
         xr[k] = V::keep(xr[k], s_lo - i0, s_hi - i0, kFill);
       }
+    }
+
+    // ---- cross-entropy backward: no reduction, every step writes its chunk ----
+    // dlogits = dloss * ((1 + 2 z lse) exp(x - lse) - onehot(t)); a row whose
+    // target is ignore_index gets 0, one with a target outside [0, N) NaN.
+    if constexpr (OP == kXentGrad) {
+      if (j == 0 && row_ok) {
+        const float lse = __ldg(a.lse + row);
+        g_t = __ldg(a.target + row);
+        const float gr = a.dloss != nullptr ? __ldg(a.dloss + row) : 1.f;
+        const bool ignored = (g_t == a.ignore_index), tok = g_t >= 0 && g_t < N;
+        g_gv = ignored ? 0.f : (tok ? gr : __int_as_float(0x7fc00000));
+        g_zf = fmaf(2.f * a.z_loss, lse, 1.f);
+        g_lb = lse * kLog2e;
+      }
+      if (__syncthreads_or(failed)) {  // the slot is free: every thread holds its vectors
+        abort = true;
+        break;
+      }
+      if (tid == 0 && p_left > 0) issue_next();
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      if (j == K - 1) {
+        j = 0;
+        item += ncl;
+      } else {
+        ++j;
+      }
+      const int64_t it_t = row * N + g_t - F0;  // slot element of the target (if in range)
+      unsigned char* yb = static_cast<unsigned char*>(a.y);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;
+        const int i0 = (vb + l + k * TPR) * E;
+        const int lo = max(0, s_lo - i0), hi = min(E, s_hi - i0);
+        float f[E], o[E];
+        V::unpack_fresh(xr[k], f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          float pe = exp2_approx(fmaf(f[e], kLog2e, -g_lb)) * g_zf;
+          if (int64_t(i0 + e) == it_t) pe -= 1.f;
+          o[e] = pe * g_gv;
+        }
+        unsigned char* dst = yb + (F0 + i0) * ES;  // 16-byte aligned: dlogits has the logits' alignment
+        if (lo == 0 && hi == E) {
+          *reinterpret_cast<uint4*>(dst) = V::pack(o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if (e >= lo && e < hi) V::store1(dst + e * ES, o[e]);
+        }
+      }
+      continue;
     }
 
     // ---- thread-level reduction ----

@@ -206,10 +206,12 @@ MASKED_N = [1, 3, 7, 101, 513, 2047, 2049, 5001, 8191, 8193, 20001, 131071]
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("op", ["softmax", "rmsnorm", "xent"])
 def test_backward_masked_shapes(op, dtype, N):
-    """Ragged rows take the masked kernels: one row per CTA (per cluster of up
-    to 16 CTAs beyond 8192 elements), persistent over the rows."""
+    """Ragged rows take the masked kernels (one row per CTA, per cluster of up
+    to 16 CTAs beyond 8192 elements, persistent over the rows), cross-entropy
+    the shifted ring kernel."""
     M = rows_for(N)
-    assert qb.qk_get_plan(OPC[op], DT[dtype], M, N)["path"] == 5
+    # cross-entropy streams unaligned rows through the shifted ring kernel (path 6)
+    assert qb.qk_get_plan(OPC[op], DT[dtype], M, N)["path"] == (6 if op == "xent" else 5)
     case = make_case(op, dtype, M, N, seed=9300 + N)
     check(op, dtype, case, run_gpu(op, dtype, case), f"masked {dtype} {M}x{N}")
 
@@ -293,3 +295,19 @@ def test_masked_rows_beyond_the_limit_are_refused():
         with pytest.raises(qb.QkError) as e:
             run_gpu(op, dtype, case)
         assert e.value.status == qb.QK_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [4096, 50257])
+def test_xent_backward_different_offsets(dtype, N):
+    """dlogits not sharing the logits' alignment: the masked kernel."""
+    M = 5
+    case = make_case("xent", dtype, M, N, seed=9900 + N)
+    d = {k: v.to(DEV) for k, v in case.items()}
+    x = _offset(d["x"])
+    store = torch.full((M * N + 16,), float("nan"), dtype=d["x"].dtype, device=DEV)
+    dx = store[2:2 + M * N].view(M, N)
+    qb.qk_xent_bwd(x, d["targets"], d["lse"], d["dloss"], dx, M, N, DT[dtype])
+    torch.cuda.synchronize()
+    assert qb.qk_get_device_status() == qb.QK_OK
+    check("xent", dtype, case, {"dx": dx}, "different offsets")
