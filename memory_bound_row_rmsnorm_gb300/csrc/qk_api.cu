@@ -482,9 +482,11 @@ qk_status plan_shifted(int dev, const DeviceInfo& d, int op, int dt, int64_t M, 
     const int64_t slice = ((N + cl - 1) / cl * es + 15) / 16;
     param_bytes = param_slice_bytes(slice) * (op == kOpLayerNorm ? 2 : 1);
   }
+  const int nin = op == kOpSoftmaxBwd ? 2 : 1;  // y and dy share each slot
   int slots = c.slots;
-  while (slots > 1 && kSmemHeader + int64_t(slots) * slot_bytes + param_bytes > d.smem_optin) --slots;
-  const int64_t smem = kSmemHeader + int64_t(slots) * slot_bytes + param_bytes;
+  while (slots > 1 && kSmemHeader + int64_t(slots) * nin * slot_bytes + param_bytes > d.smem_optin)
+    --slots;
+  const int64_t smem = kSmemHeader + int64_t(slots) * nin * slot_bytes + param_bytes;
   if (smem > d.smem_optin) return QK_ERR_UNSUPPORTED;
   qk_status st = prepare_kernel(dev, d, *ke);
   if (st != QK_OK) return st;
@@ -614,9 +616,10 @@ qk_status run(int op, int dt, RowArgs a, int path, void* stream) {
     uint64_t gen = 0;
     Plan plan;
   };
-  // (softmax, RMSNorm, x-entropy, LayerNorm, x-entropy backward) x dtype x path
-  thread_local Cached cache[5][2][3];
-  Cached& c = cache[op == kOpLayerNorm ? 3 : op == kOpXentBwd ? 4 : op][dt][path];
+  // (softmax, RMSNorm, x-entropy, LayerNorm, x-entropy and softmax backward) x dtype x path
+  thread_local Cached cache[6][2][3];
+  const int oi = op == kOpLayerNorm ? 3 : op == kOpXentBwd ? 4 : op == kOpSoftmaxBwd ? 5 : op;
+  Cached& c = cache[oi][dt][path];
   const uint64_t gen = g_override_gen.load(std::memory_order_acquire);
   if (!(c.dev == dev && c.M == a.M && c.N == a.N && c.gen == gen)) {
     Plan np;
@@ -940,6 +943,16 @@ qk_status qk_softmax_bwd(const void* y, const void* dy, void* dx, int64_t M, int
     return QK_ERR_INVALID_ARG;
   const bool fast = bwd_aligned(dtype, N, {y, dy, dx});
   if (!fast && N > kMaskedBwdMaxRow) return QK_ERR_UNSUPPORTED;
+  if (!fast && same_mod16(y, dy) && same_mod16(y, dx)) {  // the shifted ring kernel
+    RowArgs r = {};
+    r.x = y;
+    r.x2 = dy;
+    r.y = dx;
+    r.M = M;
+    r.N = N;
+    st = run(kOpSoftmaxBwd, dtype, r, kPathShifted, stream);
+    if (st != QK_ERR_UNSUPPORTED) return st;
+  }
   BwdArgs a = {};
   a.in0 = y;
   a.in1 = dy;
@@ -1103,8 +1116,9 @@ qk_status qk_get_plan(qk_op op, qk_dtype dtype, int64_t M, int64_t N, qk_plan* p
   Plan p;
   if (fast) {
     st = plan_ring(dev, *d, op, dtype, m, N, &p);
-  } else if (is_bwd(op)) {  // cross-entropy: the shifted kernel when it fits, else the masked one
-    st = op == kOpXentBwd ? plan_shifted(dev, *d, op, dtype, m, N, &p) : QK_ERR_UNSUPPORTED;
+  } else if (is_bwd(op)) {  // softmax, x-entropy: the shifted kernel when it fits, else the masked one
+    st = (op == kOpXentBwd || op == kOpSoftmaxBwd) ? plan_shifted(dev, *d, op, dtype, m, N, &p)
+                                                   : QK_ERR_UNSUPPORTED;
     if (st == QK_ERR_UNSUPPORTED) st = plan_direct_bwd(dev, *d, op, dtype, m, N, &p);
   } else {  // x and y 16-byte aligned, N not: the shifted ring, else the masked kernel
     st = plan_shifted(dev, *d, op, dtype, m, N, &p);

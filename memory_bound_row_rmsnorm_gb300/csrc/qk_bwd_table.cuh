@@ -11,6 +11,9 @@
 #define QK_SHIFT_GRAD(TH, TPR, VPT) \
   {6, TH, TPR, VPT, false,                 \
    reinterpret_cast<const void*>(&shifted_kernel<kXentGrad, QK_T, TH, TPR, VPT, false>)}
+#define QK_SHIFT_SGRAD(TH, TPR, VPT, CL) \
+  {6, TH, TPR, VPT, CL,                     \
+   reinterpret_cast<const void*>(&shifted_kernel<kSoftmaxGrad, QK_T, TH, TPR, VPT, CL>)}
 #define QK_BWD_DIRECT(TH, EPT, CL) \
   {5, TH, TH, EPT, CL, reinterpret_cast<const void*>(&bwd_direct_kernel<QK_BOP, QK_T, TH, EPT, CL>)}
 
@@ -40,6 +43,13 @@ const KernelEntry kBwdTable[] = {
 #else
     QK_BWD_DIRECT(128, 4, false),  QK_BWD_DIRECT(256, 8, false),  QK_BWD_DIRECT(512, 16, false),
     QK_BWD_DIRECT(512, 16, true),
+#endif
+#if QK_BOP == 10  // softmax: unaligned rows with y, dy and dx aligned alike (path 6)
+    QK_SHIFT_SGRAD(256, 8, 5, false),   QK_SHIFT_SGRAD(256, 16, 5, false),
+    QK_SHIFT_SGRAD(256, 32, 5, false),  QK_SHIFT_SGRAD(256, 64, 5, false),
+    QK_SHIFT_SGRAD(256, 128, 5, false), QK_SHIFT_SGRAD(256, 256, 5, false),
+    QK_SHIFT_SGRAD(256, 256, 9, false), QK_SHIFT_SGRAD(256, 256, 8, true),
+    QK_SHIFT_SGRAD(256, 256, 9, true),
 #endif
 };
 }  // namespace

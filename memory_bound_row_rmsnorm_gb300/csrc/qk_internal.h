@@ -6,8 +6,9 @@
 namespace qk {
 
 // Kernel-side operator codes (the ABI numbers LayerNorm 6; see qk_api.cu).
-// kXentGrad: cross-entropy backward on the shifted kernel (unaligned rows).
-enum Op : int { kSoftmax = 0, kRmsNorm = 1, kXent = 2, kLayerNorm = 3, kXentGrad = 4 };
+// kXentGrad, kSoftmaxGrad: cross-entropy and softmax backward on the shifted
+// kernel (unaligned rows).
+enum Op : int { kSoftmax = 0, kRmsNorm = 1, kXent = 2, kLayerNorm = 3, kXentGrad = 4, kSoftmaxGrad = 5 };
 enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Everything a row kernel needs, passed by value as its only parameter.
@@ -22,6 +23,7 @@ struct RowArgs {
   float* loss;            // [M] cross-entropy loss
   float* lse;             // [M] cross-entropy log-sum-exp, may be null (kXentGrad: input)
   const float* dloss;     // [M] kXentGrad: upstream gradient, null for 1
+  const void* x2;         // [M, N] kSoftmaxGrad: dy (x holds y), with x's alignment modulo 16
   int64_t M;
   int64_t N;
   float eps;

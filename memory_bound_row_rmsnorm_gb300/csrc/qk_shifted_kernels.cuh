@@ -39,10 +39,10 @@ namespace qk {
 // left alone it gave some configurations 110-118 registers and others 74-80
 // for the same code, i.e. two CTAs per SM instead of three.  These requests
 // compile without spilling: 4 (5 vectors a thread) and 3 (8-9 vectors), and
-// 3 and 2 for LayerNorm, which carries counts and a bias.
+// 3 and 2 for LayerNorm (counts and a bias) and softmax backward (two inputs).
 template <int OP, int VPT>
 constexpr int shifted_min_blocks() {
-  return OP == kLayerNorm ? (VPT >= 8 ? 2 : 3) : (VPT >= 8 ? 3 : 4);
+  return (OP == kLayerNorm || OP == kSoftmaxGrad) ? (VPT >= 8 ? 2 : 3) : (VPT >= 8 ? 3 : 4);
 }
 
 template <int OP, typename T, int THREADS, int TPR, int VPT, bool CLUSTER>
@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
   constexpr int GW = TPR < 32 ? TPR : 32;
   constexpr int R = THREADS / TPR;
   constexpr int64_t CH = int64_t(TPR) * VPT;   // slot vectors a row group holds
+  constexpr int NIN = (OP == kSoftmaxGrad) ? 2 : 1;  // input matrices per slot (y and dy)
+  constexpr int RED = (OP == kSoftmaxGrad) ? kRmsNorm : OP;  // softmax backward reduces a plain sum
   static_assert((TPR % 32 == 0 || 32 % TPR == 0) && THREADS % TPR == 0 && TPR >= 4, "row groups");
   static_assert(!CLUSTER || TPR == THREADS, "a clustered row spans the whole CTA");
   static_assert(NW <= 16, "block-reduction buffer holds 16 warps");
@@ -144,12 +146,18 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
       const uintptr_t end = (xaddr + uintptr_t(H * ES) + 15) & ~uintptr_t(15);
       bytes = int64_t(end - src);
     }
-    const uint32_t dst = ring0 + uint32_t(p_slot) * a.slot_bytes;
+    const uint32_t dst = ring0 + uint32_t(p_slot) * uint32_t(NIN) * a.slot_bytes;
     const uint32_t bar = full0 + 8u * uint32_t(p_slot);
-    mbar_arrive_expect_tx(bar, uint32_t(bytes));
-    for (int64_t o = 0; o < bytes; o += kCopyBytes)
-      bulk_copy_g2s(dst + uint32_t(o), reinterpret_cast<const void*>(src + uintptr_t(o)),
-                    uint32_t(min(kCopyBytes, bytes - o)), bar, policy);
+    mbar_arrive_expect_tx(bar, uint32_t(bytes) * NIN);
+#pragma unroll
+    for (int in = 0; in < NIN; ++in) {
+      // the second input (dy) has x's alignment modulo 16, so the same element range
+      const uintptr_t s_in = in == 0 ? src : src - xaddr + reinterpret_cast<uintptr_t>(a.x2);
+      for (int64_t o = 0; o < bytes; o += kCopyBytes)
+        bulk_copy_g2s(dst + uint32_t(in) * a.slot_bytes + uint32_t(o),
+                      reinterpret_cast<const void*>(s_in + uintptr_t(o)),
+                      uint32_t(min(kCopyBytes, bytes - o)), bar, policy);
+    }
     if (++p_slot == S) p_slot = 0;
     if (++p_chunk == K) {
       p_chunk = 0;
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
 
   // ---- per-column parameters, staged once (RMSNorm w; LayerNorm w and b) ----
   constexpr bool kAffine = (OP == kRmsNorm || OP == kLayerNorm);
-  T* wsm = reinterpret_cast<T*>(ring + size_t(S) * a.slot_bytes);
+  T* wsm = reinterpret_cast<T*>(ring + size_t(S) * NIN * a.slot_bytes);
   T* bsm = wsm + param_slice_bytes((SE * ES + 15) / 16) / ES;
   if constexpr (kAffine) {
     const T* wg = static_cast<const T*>(a.w) + e0;
@@ -176,8 +184,10 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
     __syncthreads();
   }
 
-  constexpr uint32_t kFill = (OP == kRmsNorm || OP == kLayerNorm) ? 0u : V::kNegInfBits;
+  constexpr uint32_t kFill =
+      (OP == kRmsNorm || OP == kLayerNorm || OP == kSoftmaxGrad) ? 0u : V::kNegInfBits;
   uint4 xr[VPT];
+  uint4 xr2[NIN == 2 ? VPT : 1];  // softmax backward: dy
   float run_m = kNegInf, run_s = 0.f;  // cross-entropy: running pair of a streamed row
   float xt = 0.f;                      // cross-entropy: x[target] if this thread holds it
   bool own_t = false;
@@ -217,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
     const int vb = s_lo / E;
     const int cn = (row_ok && Hg > Lg) ? (s_hi + E - 1) / E - vb : 0;
     const int64_t col0 = single ? L - item * N : 0;  // column of element s_lo
-    const unsigned char* sb = ring + size_t(slot) * a.slot_bytes + size_t(vb) * 16;
+    const unsigned char* sb = ring + size_t(slot) * NIN * a.slot_bytes + size_t(vb) * 16;
 
     bool valid[VPT];
 #pragma unroll
@@ -229,6 +239,14 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
       if (valid[k] && (lv == 0 || lv == cn - 1)) {  // a partial vector at an end of the window
         const int i0 = (vb + lv) * E;
         xr[k] = V::keep(xr[k], s_lo - i0, s_hi - i0, kFill);
+      }
+      if constexpr (NIN == 2) {  // dy, masked the same way (zero: its products vanish)
+        xr2[k] = valid[k] ? *reinterpret_cast<const uint4*>(sb + a.slot_bytes + lv * 16)
+                          : make_uint4(0u, 0u, 0u, 0u);
+        if (valid[k] && (lv == 0 || lv == cn - 1)) {
+          const int i0 = (vb + lv) * E;
+          xr2[k] = V::keep(xr2[k], s_lo - i0, s_hi - i0, 0u);
+        }
       }
     }
 
@@ -289,7 +307,19 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
 
     // ---- thread-level reduction ----
     float pm = kNegInf, ps = 0.f, pn = 0.f, tm = kNegInf;
-    if constexpr (OP == kRmsNorm) {
+    if constexpr (OP == kSoftmaxGrad) {  // sum dy * y
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        float f[E], d[E];
+        V::unpack(xr[k], f);
+        V::unpack(xr2[k], d);
+#pragma unroll
+        for (int e = 0; e < E; e += 2)
+          acc = fma2(make_float2(f[e], f[e + 1]), make_float2(d[e], d[e + 1]), acc);
+      }
+      ps = acc.x + acc.y;
+    } else if constexpr (OP == kRmsNorm) {
       float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -399,7 +429,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         group_welford<GW>(pn, pm, ps);
         if (WPG > 1 && lane == 0) cnt_red[ibit * 16 + warp] = pn;
       } else {
-        warp_reduce<OP, GW>(pm, ps);
+        warp_reduce<RED, GW>(pm, ps);
       }
       if (WPG > 1 && lane == 0) red[ibit * 16 + warp] = make_float2(pm, ps);
     }
@@ -434,7 +464,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         pn = cnt_red[w];
         group_welford<WPG>(pn, pm, ps);
       } else {
-        merge_partials<OP>(red + row_ibit * 16 + g * WPG, WPG, pm, ps);
+        merge_partials<RED>(red + row_ibit * 16 + g * WPG, WPG, pm, ps);
       }
     }
 
@@ -459,7 +489,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         ps = v.y;
         group_welford<16>(pn, pm, ps);
       } else {
-        merge_partials<OP>(xbuf + b * kMaxCluster, int(C), pm, ps);
+        merge_partials<RED>(xbuf + b * kMaxCluster, int(C), pm, ps);
       }
     }
 
@@ -489,6 +519,8 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
       } else if constexpr (OP == kRmsNorm) {
         sa = rsqrtf(fmaf(ps, a.inv_n, a.eps));
         if (l == 0 && rank == 0 && a.rstd != nullptr) a.rstd[row] = sa;
+      } else if constexpr (OP == kSoftmaxGrad) {
+        sb2 = -ps;  // -sum dy * y
       } else {  // LayerNorm
         sa = rsqrtf(fmaf(ps, a.inv_n, a.eps));
         sb2 = -pm * sa;
@@ -503,8 +535,9 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         if (!valid[k]) continue;
         const int i0 = (vb + l + k * TPR) * E;
         const int lo = max(0, s_lo - i0), hi = min(E, s_hi - i0);
-        float f[E], o[E], w[E], bb[E];
+        float f[E], o[E], w[E], bb[E], d[E];
         V::unpack_fresh(xr[k], f);
+        if constexpr (NIN == 2) V::unpack_fresh(xr2[k], d);
         if constexpr (kAffine) {  // the columns of this vector, from the staged slice
 #pragma unroll
           for (int e = 0; e < E; ++e) {
@@ -521,6 +554,8 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
           if constexpr (OP == kSoftmax) {  // exp(x - m_t) * scale (scalar: fewer live registers)
             v = make_float2(exp2_approx(fmaf(x2.x, kLog2e, -sb2)) * sa,
                             exp2_approx(fmaf(x2.y, kLog2e, -sb2)) * sa);
+          } else if constexpr (OP == kSoftmaxGrad) {  // y * (dy - sum dy * y)
+            v = mul2(x2, add2(make_float2(d[e], d[e + 1]), b2));
           } else if constexpr (OP == kRmsNorm) {  // (x * rstd) * w
             v = mul2(mul2(x2, a2), make_float2(w[e], w[e + 1]));
           } else {  // (x * rstd - mean * rstd) * w + b

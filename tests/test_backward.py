@@ -206,12 +206,12 @@ MASKED_N = [1, 3, 7, 101, 513, 2047, 2049, 5001, 8191, 8193, 20001, 131071]
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("op", ["softmax", "rmsnorm", "xent"])
 def test_backward_masked_shapes(op, dtype, N):
-    """Ragged rows take the masked kernels (one row per CTA, per cluster of up
-    to 16 CTAs beyond 8192 elements, persistent over the rows), cross-entropy
-    the shifted ring kernel."""
+    """Ragged rows: softmax and cross-entropy on the shifted ring kernel, RMSNorm
+    on the masked kernel (one row per CTA, per cluster of up to 16 CTAs beyond
+    8192 elements, persistent over the rows)."""
     M = rows_for(N)
-    # cross-entropy streams unaligned rows through the shifted ring kernel (path 6)
-    assert qb.qk_get_plan(OPC[op], DT[dtype], M, N)["path"] == (6 if op == "xent" else 5)
+    # softmax and cross-entropy take the shifted ring kernel (path 6)
+    assert qb.qk_get_plan(OPC[op], DT[dtype], M, N)["path"] == (5 if op == "rmsnorm" else 6)
     case = make_case(op, dtype, M, N, seed=9300 + N)
     check(op, dtype, case, run_gpu(op, dtype, case), f"masked {dtype} {M}x{N}")
 
@@ -223,7 +223,7 @@ def test_backward_masked_many_rows_per_cta(op, M, N):
     reusing both reduction buffers and both phases of the cluster barrier,
     and RMSNorm's dw partials accumulate over the rows a CTA takes."""
     plan = qb.qk_get_plan(OPC[op], qb.QK_F32, M, N)
-    assert plan["path"] == 5 and plan["grid"] // plan["cluster"] < M
+    assert plan["path"] == (5 if op == "rmsnorm" else 6) and plan["grid"] // plan["cluster"] < M
     case = make_case(op, "f32", M, N, seed=9400 + N)
     check(op, "f32", case, run_gpu(op, "f32", case), f"masked {M}x{N}")
 
@@ -311,3 +311,19 @@ def test_xent_backward_different_offsets(dtype, N):
     torch.cuda.synchronize()
     assert qb.qk_get_device_status() == qb.QK_OK
     check("xent", dtype, case, {"dx": dx}, "different offsets")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [4096, 20001])
+def test_softmax_backward_different_offsets(dtype, N):
+    """dx not sharing the alignment of y and dy: the masked kernel."""
+    M = 5
+    case = make_case("softmax", dtype, M, N, seed=9950 + N)
+    d = {k: v.to(DEV) for k, v in case.items()}
+    y, dy = _offset(d["y"]), _offset(d["dy"])
+    store = torch.full((M * N + 16,), float("nan"), dtype=d["y"].dtype, device=DEV)
+    dx = store[2:2 + M * N].view(M, N)
+    qb.qk_softmax_bwd(y, dy, dx, M, N, DT[dtype])
+    torch.cuda.synchronize()
+    assert qb.qk_get_device_status() == qb.QK_OK
+    check("softmax", dtype, case, {"dx": dx}, "different offsets")
