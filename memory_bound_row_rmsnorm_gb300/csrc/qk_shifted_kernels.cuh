@@ -348,6 +348,8 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
       const float sum = s2.x + s2.y;
       const float mu = cnt > 0 ? __fdiv_rn(sum, float(cnt)) : 0.f;
       float qd = 0.f;
+      float2 q2 = make_float2(0.f, 0.f);
+      const float2 nmu = make_float2(-mu, -mu);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!valid[k]) continue;
@@ -355,15 +357,23 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         const int lo = max(0, s_lo - i0), hi = min(E, s_hi - i0);
         float f[E];
         V::unpack(xr[k], f);
+        if (lo == 0 && hi == E) {  // a whole vector: packed
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float d = f[e] - mu;
-          if (e >= lo && e < hi) qd = fmaf(d, d, qd);
+          for (int e = 0; e < E; e += 2) {
+            const float2 d = add2(make_float2(f[e], f[e + 1]), nmu);
+            q2 = fma2(d, d, q2);
+          }
+        } else {  // a partial vector at an end of the window
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float d = f[e] - mu;
+            if (e >= lo && e < hi) qd = fmaf(d, d, qd);
+          }
         }
       }
       pn = float(cnt);
       pm = mu;
-      ps = qd;
+      ps = qd + (q2.x + q2.y);
     } else {
       if constexpr (OP == kXent) {
         if (j == 0) {
