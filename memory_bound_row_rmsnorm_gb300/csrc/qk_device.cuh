@@ -351,6 +351,21 @@ struct Vec16<float> {
     return fmaxf(fmaxf(m, fmaxf(__uint_as_float(v.x), __uint_as_float(v.y))),
                  fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
+  // Maximum over the elements of n vectors as a pairwise tree: depth
+  // log2(4n) instead of a chain of 4n comparisons.
+  template <int NV>
+  __device__ __forceinline__ static float max_all(const uint4* v) {
+    float t[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      t[k] = fmaxf(fmaxf(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
+                   fmaxf(__uint_as_float(v[k].z), __uint_as_float(v[k].w)));
+#pragma unroll
+    for (int s = 1; s < NV; s *= 2)
+#pragma unroll
+      for (int k = 0; k + s < NV; k += 2 * s) t[k] = fmaxf(t[k], t[k + s]);
+    return t[0];
+  }
   __device__ __forceinline__ static uint4 pack(const float* f) {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                       __float_as_uint(f[3]));
@@ -388,6 +403,22 @@ struct Vec16<__nv_bfloat16> {
     float lo, hi;
     unpack2(p, lo, hi);
     return fmaxf(m, fmaxf(lo, hi));
+  }
+  // Maximum over the elements of n vectors: a pairwise tree of packed bf16
+  // comparisons (exact), widened once at the end.
+  template <int NV>
+  __device__ __forceinline__ static float max_all(const uint4* v) {
+    uint32_t t[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      t[k] = max_bf16x2(max_bf16x2(v[k].x, v[k].y), max_bf16x2(v[k].z, v[k].w));
+#pragma unroll
+    for (int s = 1; s < NV; s *= 2)
+#pragma unroll
+      for (int k = 0; k + s < NV; k += 2 * s) t[k] = max_bf16x2(t[k], t[k + s]);
+    float lo, hi;
+    unpack2(t[0], lo, hi);
+    return fmaxf(lo, hi);
   }
   // Same as unpack, but opaque to the optimiser: it cannot be hoisted out of
   // a loop or merged with an earlier unpack, so the packed form (half the

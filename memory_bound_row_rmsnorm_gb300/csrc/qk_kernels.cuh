@@ -292,12 +292,23 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
     // below needs no per-element masking.
     constexpr uint32_t kFill = (OP == kRmsNorm || OP == kLayerNorm) ? 0u : V::kNegInfBits;
     bool valid[VPT];
+    // Cross-entropy: when every vector of the group is data, plain loads
+    // without the per-vector selects (the other operators measured no gain
+    // and, for some plans, a register more than a resident CTA allows).
+    if (OP == kXent && row_ok && !failed && cn == TPR * VPT) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int lv = l + k * TPR;
-      valid[k] = row_ok && lv < cn && !failed;
-      xr[k] = valid[k] ? *reinterpret_cast<const uint4*>(sb + lv * 16)
-                       : make_uint4(kFill, kFill, kFill, kFill);
+      for (int k = 0; k < VPT; ++k) {
+        valid[k] = true;
+        xr[k] = *reinterpret_cast<const uint4*>(sb + (l + k * TPR) * 16);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int lv = l + k * TPR;
+        valid[k] = row_ok && lv < cn && !failed;
+        xr[k] = valid[k] ? *reinterpret_cast<const uint4*>(sb + lv * 16)
+                         : make_uint4(kFill, kFill, kFill, kFill);
+      }
     }
 
     // ---- thread-level reduction (registers) ----
@@ -404,16 +415,9 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
         if (trow >= 0 && trow < N) {  // capture x[target] if it is in this thread's vectors
           const int64_t tl = trow / E - cbase;  // target vector, relative to the slot
           if (tl >= 0 && tl < cn && int(tl) % TPR == l) {
-            const int kk = int(tl) / TPR, ee = int(trow % E);
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-              if (k != kk) continue;
-              float f[E];
-              V::unpack(xr[k], f);
-#pragma unroll
-              for (int e = 0; e < E; ++e)
-                if (e == ee) xt = f[e];
-            }
+            // One element read from the slot (still held until the barrier
+            // below), rather than a select over every element in registers.
+            xt = V::load1(sb + tl * 16 + (trow % E) * int64_t(sizeof(T)));
             own_t = true;
           }
         }
@@ -421,11 +425,21 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
       // Streamed pairs start from the running maximum, so a chunk with no
       // elements for this thread leaves the pair unchanged.
       float m = (OP == kXent || TWO_PASS) ? run_m : kNegInf;
+      // Cross-entropy: the maximum as a tree and four independent accumulator
+      // pairs (short dependency chains).  Softmax keeps one chain of each: it
+      // also holds the exponentials for the finish, and the extra registers
+      // would cost a resident CTA.
+      constexpr bool kShortChains = (OP == kXent);
+      if constexpr (kShortChains) {
+        m = fmaxf(m, V::template max_all<VPT>(xr));
+      } else {
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) m = V::max_into(m, xr[k]);
+        for (int k = 0; k < VPT; ++k) m = V::max_into(m, xr[k]);
+      }
       const float mb = (m == kNegInf) ? 0.f : m * kLog2e;
       const float2 l2e = make_float2(kLog2e, kLog2e), nmb = make_float2(-mb, -mb);
-      float2 acc = make_float2(0.f, 0.f);
+      float2 a4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         float f[E];
@@ -438,9 +452,12 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
             ef[k * E + e] = ev.x;
             ef[k * E + e + 1] = ev.y;
           }
-          acc = add2(acc, ev);
+          const int c = kShortChains ? ((k * E + e) / 2) & 3 : 0;
+          a4[c] = add2(a4[c], ev);
         }
       }
+      const float2 acc =
+          kShortChains ? add2(add2(a4[0], a4[1]), add2(a4[2], a4[3])) : a4[0];
       if constexpr (OP == kSoftmax && !TWO_PASS) {
         tm = m;
         pm = m;

@@ -388,28 +388,27 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
           const int64_t it = row * N + trow - F0;  // slot element of the target
           if (it >= s_lo && it < s_hi) {
             const int vi = int(it / E) - vb;
-            if (vi % TPR == l) {
-              const int kk = vi / TPR, ee = int(it % E);
-#pragma unroll
-              for (int k = 0; k < VPT; ++k) {
-                if (k != kk) continue;
-                float f[E];
-                V::unpack(xr[k], f);
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                  if (e == ee) xt = f[e];
-              }
+            if (vi % TPR == l) {  // one element read from the slot
+              xt = V::load1(sb + vi * 16 + int(it % E) * int(sizeof(T)));
               own_t = true;
             }
           }
         }
       }
       float m = (OP == kXent) ? run_m : kNegInf;
+      // Cross-entropy: the maximum as a tree and four accumulator pairs
+      // (short dependency chains); softmax keeps one chain of each.
+      constexpr bool kShortChains = (OP == kXent);
+      if constexpr (kShortChains) {
+        m = fmaxf(m, V::template max_all<VPT>(xr));
+      } else {
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) m = V::max_into(m, xr[k]);
+        for (int k = 0; k < VPT; ++k) m = V::max_into(m, xr[k]);
+      }
       const float mb = (m == kNegInf) ? 0.f : m * kLog2e;
       const float2 l2e = make_float2(kLog2e, kLog2e), nmb = make_float2(-mb, -mb);
-      float2 acc = make_float2(0.f, 0.f);
+      float2 a4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         float f[E];
@@ -417,9 +416,12 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
 #pragma unroll
         for (int e = 0; e < E; e += 2) {
           const float2 t = fma2(make_float2(f[e], f[e + 1]), l2e, nmb);
-          acc = add2(acc, make_float2(exp2_approx(t.x), exp2_approx(t.y)));  // padding: 2^-inf = 0
+          const int c = kShortChains ? ((k * E + e) / 2) & 3 : 0;
+          a4[c] = add2(a4[c], make_float2(exp2_approx(t.x), exp2_approx(t.y)));  // padding: 2^-inf = 0
         }
       }
+      const float2 acc =
+          kShortChains ? add2(add2(a4[0], a4[1]), add2(a4[2], a4[3])) : a4[0];
       if constexpr (OP == kSoftmax) {
         tm = m;
         pm = m;
