@@ -259,7 +259,7 @@ const Choice kLayerNormTable[] = {
 };
 const Choice kSoftmaxTable[] = {
     {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 3},       {128, 256, 32, 4, 1, 3},
-    {256, 256, 64, 4, 1, 2},     {512, 256, 128, 4, 1, 1},     {1024, 256, 256, 4, 1, 1},
+    {256, 256, 64, 4, 1, 2},     {512, 128, 128, 4, 1, 1},     {1024, 256, 256, 4, 1, 1},
     {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 16, 4, 2},  {32768, 256, 256, 16, 8, 1},  {65536, 256, 256, 16, 16, 1},
 };
