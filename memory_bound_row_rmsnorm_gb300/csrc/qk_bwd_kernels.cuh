@@ -47,8 +47,15 @@ struct BwdArgs {
   int* status;
 };
 
+// Residency requests for the launch bounds (0: none): cross-entropy's
+// 8-vector plans hold three CTAs per SM.
+template <int OP, int THREADS, int VPT>
+constexpr int bwd_min_blocks() {
+  return (OP == kXentBwd && THREADS == 256 && VPT == 8) ? 3 : 0;
+}
+
 template <int OP, typename T, int THREADS, int TPR, int VPT, bool CLUSTER>
-__global__ void __launch_bounds__(THREADS) bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(THREADS, (bwd_min_blocks<OP, THREADS, VPT>())) bwd_kernel(const BwdArgs a) {
   using V = Vec16<T>;
   constexpr int E = V::kElems;
   constexpr int NIN = (OP == kXentBwd) ? 1 : 2;  // input matrices per item
@@ -100,6 +107,25 @@ __global__ void __launch_bounds__(THREADS) bwd_kernel(const BwdArgs a) {
     cluster_sync_all();
   } else {
     __syncthreads();
+  }
+  // The first item of every input into L2 while the previous kernel in the
+  // stream finishes (a hint; the copies into shared memory follow the wait).
+  if (!CLUSTER && tid == 0 && q_total > 0) {
+    int64_t off, bytes;
+    if (K > 1) {
+      off = int64_t(cid) * NV * 16;
+      bytes = min(int64_t(S) * CH, NV) * 16;
+    } else {
+      const int64_t r0 = int64_t(cid) * R;
+      off = r0 * NV * 16;
+      bytes = min(int64_t(R), M - r0) * NV * 16;
+    }
+    const void* in[2] = {a.in0, a.in1};
+#pragma unroll
+    for (int i = 0; i < NIN; ++i)
+      for (int64_t o = 0; o < bytes; o += 32768)
+        bulk_prefetch_l2(static_cast<const unsigned char*>(in[i]) + off + o,
+                         uint32_t(min(int64_t(32768), bytes - o)));
   }
   grid_dependency_wait();
   allow_dependent_launch();
@@ -199,6 +225,19 @@ __global__ void __launch_bounds__(THREADS) bwd_kernel(const BwdArgs a) {
     if (j == 0 && OP != kSoftmaxBwd) {
       rs = s_next, gs = g_next, trow = t_next;
       prefetch(item + ncl);
+    }
+    // Cross-entropy: the thread holding x[target] in this slot reads it once
+    // here (the slot is refilled after the barrier below) and rewrites that
+    // one output element after its vector store.
+    int64_t tl = -1;       // target vector, relative to the slot
+    bool own_t = false;
+    float xt = 0.f;
+    if constexpr (OP == kXentBwd) {
+      if (row_ok && !failed && trow >= 0 && trow < N) {
+        tl = trow / E - cbase;
+        own_t = tl >= 0 && tl < cn && int(tl) % TPR == l;
+        if (own_t) xt = V::load1(sb + tl * 16 + (trow % E) * int64_t(sizeof(T)));
+      }
     }
     bool valid[VPT];
 #pragma unroll
@@ -337,26 +376,26 @@ __global__ void __launch_bounds__(THREADS) bwd_kernel(const BwdArgs a) {
       const float gv = ignored ? 0.f : (tok ? gs : __int_as_float(0x7fc00000));
       const float zf = fmaf(2.f * a.z_loss, rs, 1.f);
       const float lb = rs * kLog2e;
-      const int64_t tl = tok ? trow / E - cbase : -1;  // target vector, relative to the slot
-      const int te = int(trow & (E - 1));
+      const float2 zf2 = make_float2(zf, zf), gv2 = make_float2(gv, gv);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!valid[k]) continue;
         float f[E], o[E];
         V::unpack_fresh(xa[k], f);
-        const bool tvec = (int64_t(l + k * TPR) == tl);
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
+        for (int e = 0; e < E; e += 2) {  // (exp(x - lse) (1 + 2 z lse)) dloss
           const float2 t = fma2(make_float2(f[e], f[e + 1]), make_float2(kLog2e, kLog2e),
                                 make_float2(-lb, -lb));
-          float p0 = exp2_approx(t.x) * zf, p1 = exp2_approx(t.y) * zf;
-          if (tvec && te == e) p0 -= 1.f;
-          if (tvec && te == e + 1) p1 -= 1.f;
-          const float2 v = mul2(make_float2(p0, p1), make_float2(gv, gv));
+          const float2 v =
+              mul2(mul2(make_float2(exp2_approx(t.x), exp2_approx(t.y)), zf2), gv2);
           o[e] = v.x;
           o[e + 1] = v.y;
         }
         og[l + k * TPR] = V::pack(o);
+      }
+      if (own_t) {  // the target element: the same terms, minus the one-hot 1
+        const float p = exp2_approx(fmaf(xt, kLog2e, -lb)) * zf - 1.f;
+        V::store1(reinterpret_cast<T*>(og + tl) + (trow % E), p * gv);
       }
     }
   }

@@ -147,6 +147,14 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
       : "memory");
 }
 
+// Hint: pull [src, src + bytes) from HBM into L2 (both 16-byte multiples).
+// It returns nothing to the SM, so it may be issued before the kernel that
+// writes those bytes has finished: L2 is where every write lands, and the
+// copies into shared memory that read the data later come after the wait.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Thread-block cluster / DSMEM
 // ---------------------------------------------------------------------------

@@ -33,6 +33,8 @@
 #include "qk_device.cuh"
 #include "qk_internal.h"
 
+#include <type_traits>
+
 namespace qk {
 
 constexpr int64_t kCopyBytes = 32768;  // largest single bulk copy issued
@@ -73,8 +75,19 @@ __device__ __forceinline__ void merge_partials(const float2* p, int n, float& m,
 // slice is streamed through the ring twice in chunks -- the first pass
 // accumulates the reduction, the second re-reads each chunk and writes its
 // outputs with the row's totals (three HBM passes instead of two).
+// Residency requests for the launch bounds (0: none).  A few 128-thread plans
+// sit just under an occupancy step; these keep the register allocator there.
+template <int OP, typename T, int THREADS, int VPT, bool CLUSTER, bool TWO_PASS>
+constexpr int row_min_blocks() {
+  if (THREADS != 128 || VPT != 4 || CLUSTER || TWO_PASS) return 0;
+  if (OP == kSoftmax) return std::is_same<T, float>::value ? 10 : 8;
+  if (OP == kRmsNorm) return std::is_same<T, float>::value ? 8 : 0;
+  return 0;
+}
+
 template <int OP, typename T, int THREADS, int TPR, int VPT, bool CLUSTER, bool TWO_PASS = false>
-__global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, T, THREADS, VPT, CLUSTER, TWO_PASS>()))
+    row_kernel(const RowArgs a) {
   using V = Vec16<T>;
   constexpr int E = V::kElems;       // elements per 16-byte vector
   constexpr int NW = THREADS / 32;   // warps per CTA
@@ -138,8 +151,25 @@ __global__ void __launch_bounds__(THREADS) row_kernel(const RowArgs a) {
   } else {
     __syncthreads();
   }
-  // Everything above touched only shared memory; from here on global memory
-  // is read, which the previous kernel in the stream may still be writing.
+  // While the previous kernel in the stream finishes, bring this CTA's first
+  // item (the slots of its first ring fill) into L2, so that HBM is not idle
+  // between the two kernels.  (Not for clusters: their launches are long and
+  // measured a point or two slower with it.)
+  if (!CLUSTER && tid == 0 && q_total > 0) {
+    int64_t off, bytes;
+    if (K > 1 || kChunked) {  // the first chunks of the row
+      off = int64_t(cid) * NV * 16;
+      bytes = min(int64_t(S) * CH, nv) * 16;
+    } else {
+      const int64_t r0 = int64_t(cid) * R;
+      off = r0 * NV * 16;
+      bytes = min(int64_t(R), M - r0) * NV * 16;
+    }
+    for (int64_t o = 0; o < bytes; o += kCopyBytes)
+      bulk_prefetch_l2(xg + off + o, uint32_t(min(kCopyBytes, bytes - o)));
+  }
+  // Everything above touched only shared memory (and L2, by hint); from here
+  // on global memory is read, which the previous kernel may still be writing.
   grid_dependency_wait();
   allow_dependent_launch();
 

@@ -109,6 +109,22 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
   } else {
     __syncthreads();
   }
+  // The aligned range of the first step into L2 while the previous kernel in
+  // the stream finishes (a hint; the copies into shared memory follow the wait).
+  if (!CLUSTER && tid == 0 && q_total > 0) {
+    const int64_t L = (K > 1) ? int64_t(cid) * N : int64_t(cid) * R * N;
+    const int64_t H = (K > 1) ? min(L + N, L + CHE) : min(M, (int64_t(cid) + 1) * R) * N;
+    const uintptr_t lo = (xaddr + uintptr_t(L * ES)) & ~uintptr_t(15);
+    const uintptr_t hi = (xaddr + uintptr_t(H * ES) + 15) & ~uintptr_t(15);
+    const int64_t bytes = H > L ? int64_t(hi - lo) : 0;
+#pragma unroll
+    for (int in = 0; in < NIN; ++in) {
+      const uintptr_t s_in = in == 0 ? lo : lo - xaddr + reinterpret_cast<uintptr_t>(a.x2);
+      for (int64_t o = 0; o < bytes; o += kCopyBytes)
+        bulk_prefetch_l2(reinterpret_cast<const void*>(s_in + uintptr_t(o)),
+                         uint32_t(min(kCopyBytes, bytes - o)));
+    }
+  }
   grid_dependency_wait();
   allow_dependent_launch();
 
@@ -263,6 +279,19 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         g_zf = fmaf(2.f * a.z_loss, lse, 1.f);
         g_lb = lse * kLog2e;
       }
+      // The thread holding x[target] reads it from the slot before it is
+      // refilled, and rewrites that one output element after its vector.
+      int64_t it_t = -1;  // slot element of the target
+      bool own_t = false;
+      float xt = 0.f;
+      if (row_ok && !failed && g_t >= 0 && g_t < N) {
+        it_t = row * N + g_t - F0;
+        if (it_t >= s_lo && it_t < s_hi) {
+          const int vi = int(it_t / E) - vb;
+          own_t = vi % TPR == l;
+          if (own_t) xt = V::load1(sb + vi * 16 + int(it_t % E) * ES);
+        }
+      }
       if (__syncthreads_or(failed)) {  // the slot is free: every thread holds its vectors
         abort = true;
         break;
@@ -278,7 +307,6 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
       } else {
         ++j;
       }
-      const int64_t it_t = row * N + g_t - F0;  // slot element of the target (if in range)
       unsigned char* yb = static_cast<unsigned char*>(a.y);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -288,11 +316,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         float f[E], o[E];
         V::unpack_fresh(xr[k], f);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          float pe = exp2_approx(fmaf(f[e], kLog2e, -g_lb)) * g_zf;
-          if (int64_t(i0 + e) == it_t) pe -= 1.f;
-          o[e] = pe * g_gv;
-        }
+        for (int e = 0; e < E; ++e) o[e] = (exp2_approx(fmaf(f[e], kLog2e, -g_lb)) * g_zf) * g_gv;
         unsigned char* dst = yb + (F0 + i0) * ES;  // 16-byte aligned: dlogits has the logits' alignment
         if (lo == 0 && hi == E) {
           *reinterpret_cast<uint4*>(dst) = V::pack(o);
@@ -301,6 +325,10 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
           for (int e = 0; e < E; ++e)
             if (e >= lo && e < hi) V::store1(dst + e * ES, o[e]);
         }
+      }
+      if (own_t) {  // the target element, minus the one-hot 1
+        const float p = exp2_approx(fmaf(xt, kLog2e, -g_lb)) * g_zf - 1.f;
+        V::store1(yb + (F0 + it_t) * ES, p * g_gv);
       }
       continue;
     }
