@@ -408,12 +408,27 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   if (st != QK_OK) return st;
   if (occ <= 0) return QK_ERR_UNSUPPORTED;
 
+  // Short launches (fewer than four items for each resident CTA) spend most
+  // of their time waiting for their first loads: give each CTA a ring of
+  // three slots, if that costs no resident CTA.  (Softmax fp32 1024 x 4096:
+  // 70 % -> 75 %; 2048 x 4096: 76 % -> 97 %.)
+  int64_t smem_used = smem;
+  if (!ov.on && !two_pass && k == 1 && cl == 1 && slots < 3 &&
+      p->num_items < 4 * int64_t(occ) * d.sms) {
+    const int64_t smem3 = kSmemHeader + 3 * int64_t(nin) * slot_bytes + param_bytes;
+    int occ3 = 0;
+    if (smem3 <= d.smem_optin && occupancy(dev, *ke, int(smem3), 0, &occ3) == QK_OK && occ3 >= occ) {
+      slots = 3;
+      smem_used = smem3;
+    }
+  }
+
   p->kernel = ke;
   p->cluster = cl;
   p->slots = slots;
   p->chunks = k;
   p->slot_bytes = slot_bytes;
-  p->smem = int(smem);
+  p->smem = int(smem_used);
   // Persistent grid: every resident CTA (or cluster) once, at most one per item.
   int64_t units = cl > 1 ? int64_t(occ) : int64_t(occ) * d.sms;
   if (ov.on && ov.plan.grid > 0) units = std::min<int64_t>(units, std::max(1, ov.plan.grid / cl));
