@@ -27,6 +27,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -384,6 +385,40 @@ def cpu_oracle_rate(op, dtype, M, N, sigma, budget_s: float, seed: int = 4242):
     return nbytes / el / 1e12, cores, sample, el
 
 
+def cpu_single_core_rate(op, dtype, N, sigma, budget_s: float, seed: int = 4243):
+    """The same oracle on one thread of the host (the per-core rate)."""
+    import oracle
+
+    lib = oracle.library()
+    rows = 64
+    d = oracle_inputs(op, dtype, rows, N, sigma, seed)
+    oracle_call(oracle, lib, op, d, slice(0, rows))  # warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_call(oracle, lib, op, d, slice(0, rows))
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return min_bytes(op, dtype, rows, N) * reps / el / 1e12
+
+
+def cpu_model() -> str:
+    """The host CPU's name as the kernel reports it (x86 and Arm layouts)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model Name", "Hardware"):
+        for line in info.splitlines():
+            if line.split(":")[0].strip() == key:
+                return line.split(":", 1)[1].strip()
+    parts = sorted({line.split(":", 1)[1].strip() for line in info.splitlines()
+                    if line.split(":")[0].strip() == "CPU part"})
+    return f"{platform.machine()} (CPU part {', '.join(parts)})" if parts else platform.machine()
+
+
 def run_reference(args, op, dtype, M, N, sigma):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -422,7 +457,7 @@ def run_reference(args, op, dtype, M, N, sigma):
                    "rows_per_step": rows},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -583,7 +618,9 @@ def main():
     cpu = None
     if ws == 1 and args.cpu_seconds > 0:
         rate, cores, sample, _ = cpu_oracle_rate(op, dtype, M, N, sigma, args.cpu_seconds)
-        cpu = {"value": rate, "unit": "TB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        one = cpu_single_core_rate(op, dtype, N, sigma, min(2.0, args.cpu_seconds / 5))
+        cpu = {"value": rate, "unit": "TB/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "single_core_value": one, "cpu_model": cpu_model()}
 
     line = {
         "metric": METRIC,
