@@ -442,16 +442,20 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
 // step copies the aligned range around its elements, so a row group must hold
 // ceil((15 + slice bytes) / 16) vectors: one more than the aligned row when
 // it is misaligned, hence row groups of 5 (or 9) vectors a thread.  Row groups
-// from 8 to 256 threads of 5 vectors, then 256 x 9, then the smallest cluster
+// from 8 to 256 threads of 5 or 9 vectors (the smallest that holds the row),
+// then the smallest cluster
 // of 256 x 9 CTAs (256 x 8 when the slice fits: fewer registers) for softmax / RMSNorm /
 // LayerNorm; cross-entropy streams longer rows in equal chunks of at most 2303
 // vectors.
 struct ShiftChoice {
   int threads, row_threads, vec_per_thread, slots;
 };
+// In order of capacity (row_threads x vec_per_thread vectors): the first that
+// holds the row is the one with the least padding.
 constexpr ShiftChoice kShiftTable[] = {
-    {256, 8, 5, 2},   {256, 16, 5, 2},  {256, 32, 5, 2}, {256, 64, 5, 2},
-    {256, 128, 5, 2}, {256, 256, 5, 2}, {256, 256, 9, 1},
+    {256, 8, 5, 2},   {256, 16, 5, 2},  {256, 16, 9, 2},  {256, 32, 5, 2},
+    {256, 32, 9, 2},  {256, 64, 5, 2},  {256, 64, 9, 2},  {256, 128, 5, 2},
+    {256, 128, 9, 2}, {256, 256, 5, 2}, {256, 256, 9, 1},
 };
 int64_t span_vectors(int64_t elems, int es) { return (15 + elems * es + 15) / 16; }
 
@@ -461,9 +465,14 @@ qk_status plan_shifted(int dev, const DeviceInfo& d, int op, int dt, int64_t M, 
   const int last = kinds - 1;
   const bool streams = (op == kXent || op == kOpXentBwd);  // no row reduction to keep
   int pick = -1, cl = 1, k = 1;
-  for (int i = 0; i <= last && pick < 0; ++i)
-    if (span_vectors(N, es) <= int64_t(kShiftTable[i].row_threads) * kShiftTable[i].vec_per_thread)
-      pick = i;
+  // LayerNorm and softmax backward hold two CTAs per SM at 9 vectors a thread
+  // (counts, or a second input): their narrow row groups stay at 5 vectors.
+  const bool narrow9 = !(op == kOpLayerNorm || op == kOpSoftmaxBwd);
+  for (int i = 0; i <= last && pick < 0; ++i) {
+    const ShiftChoice& c = kShiftTable[i];
+    if (c.vec_per_thread == 9 && c.row_threads < 256 && !narrow9) continue;
+    if (span_vectors(N, es) <= int64_t(c.row_threads) * c.vec_per_thread) pick = i;
+  }
   if (pick < 0 && streams) {  // stream the row in chunks of (cap - 1) vectors
     pick = last;
     const int64_t che = (int64_t(kShiftTable[pick].row_threads) * kShiftTable[pick].vec_per_thread - 1) *

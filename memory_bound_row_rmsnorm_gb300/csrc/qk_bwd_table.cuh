@@ -39,7 +39,8 @@ const KernelEntry kBwdTable[] = {
     // unaligned rows whose dlogits share the logits' alignment (path 6)
     QK_SHIFT_GRAD(256, 8, 5),   QK_SHIFT_GRAD(256, 16, 5),  QK_SHIFT_GRAD(256, 32, 5),
     QK_SHIFT_GRAD(256, 64, 5),  QK_SHIFT_GRAD(256, 128, 5), QK_SHIFT_GRAD(256, 256, 5),
-    QK_SHIFT_GRAD(256, 256, 9),
+    QK_SHIFT_GRAD(256, 16, 9),  QK_SHIFT_GRAD(256, 32, 9),  QK_SHIFT_GRAD(256, 64, 9),
+    QK_SHIFT_GRAD(256, 128, 9), QK_SHIFT_GRAD(256, 256, 9),
 #else
     QK_BWD_DIRECT(128, 4, false),  QK_BWD_DIRECT(256, 8, false),  QK_BWD_DIRECT(512, 16, false),
     QK_BWD_DIRECT(512, 16, true),

@@ -65,6 +65,12 @@ const KernelEntry kTable[] = {
     QK_SHIFT(256, 64, 5, false),
     QK_SHIFT(256, 128, 5, false),
     QK_SHIFT(256, 256, 5, false),
+#if QK_OP != 3  // LayerNorm at 9 vectors keeps two CTAs per SM: its narrow groups stay at 5
+    QK_SHIFT(256, 16, 9, false),
+    QK_SHIFT(256, 32, 9, false),
+    QK_SHIFT(256, 64, 9, false),
+    QK_SHIFT(256, 128, 9, false),
+#endif
     QK_SHIFT(256, 256, 9, false),
 #if QK_OP != 2
     QK_SHIFT(256, 256, 8, true),

@@ -55,7 +55,6 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
   constexpr int WPG = TPR / 32;
   constexpr int GW = TPR < 32 ? TPR : 32;
   constexpr int R = THREADS / TPR;
-  constexpr int64_t CH = int64_t(TPR) * VPT;   // slot vectors a row group holds
   constexpr int NIN = (OP == kSoftmaxGrad) ? 2 : 1;  // input matrices per slot (y and dy)
   constexpr int RED = (OP == kSoftmaxGrad) ? kRmsNorm : OP;  // softmax backward reduces a plain sum
   static_assert((TPR % 32 == 0 || 32 % TPR == 0) && THREADS % TPR == 0 && TPR >= 4, "row groups");
@@ -77,8 +76,8 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
   const int S = a.slots;
   const int64_t K = a.chunks;  // chunks per row slice (cross-entropy streaming), else 1
   // Elements of one chunk of a streamed row (a.chunk_elems): the row in K
-  // equal parts, each at most (CH - 1) * E elements so that its aligned copy
-  // fits CH vectors.
+  // equal parts, each at most (TPR * VPT - 1) * E elements so that its
+  // aligned copy fits the TPR * VPT vectors of a row group.
 
   uint32_t C = 1, rank = 0, cid = blockIdx.x, ncl = gridDim.x;
   if constexpr (CLUSTER) {

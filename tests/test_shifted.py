@@ -37,10 +37,11 @@ def shifted_copy(t, elems, fill=None):
 
 
 # Lengths around every plan boundary of the shifted kernel (row groups of
-# 8 ... 256 threads of 5 vectors, 256 x 9, clusters of 2 ... 16, streamed
+# 8 ... 256 threads of 5 or 9 vectors, clusters of 2 ... 16, streamed
 # cross-entropy in equal chunks).
-SHIFT_N = [1, 5, 9, 60, 123, 153, 251, 311, 313, 627, 1003, 1263, 2045, 2547, 4097, 5111,
-           9209, 10227, 16385, 18415, 18419, 32761, 50257, 65537, 131071, 250001]
+SHIFT_N = [1, 5, 9, 60, 123, 153, 251, 311, 313, 571, 573, 627, 1003, 1143, 1149, 1263, 2045,
+           2295, 2301, 2547, 4097, 4599, 4605, 5111, 9207, 9209, 10227, 16385, 18415, 18419,
+           32761, 50257, 65537, 131071, 250001]
 
 
 @pytest.mark.parametrize("N", SHIFT_N)
