@@ -507,7 +507,12 @@ qk_status plan_shifted(int dev, const DeviceInfo& d, int op, int dt, int64_t M, 
     param_bytes = param_slice_bytes(slice) * (op == kOpLayerNorm ? 2 : 1);
   }
   const int nin = op == kOpSoftmaxBwd ? 2 : 1;  // y and dy share each slot
-  int slots = c.slots;
+  // Forward cross-entropy keeps nothing of a row but its running pair, so the
+  // 256 x 9 groups take a second slot to overlap the next chunk's copy with
+  // this one (16384 x 50257 bf16: 80 % -> 95 %); the operators that hold the
+  // row in registers measured slower with it (softmax, RMSNorm, and the
+  // backward, whose stores share the SM's bandwidth).
+  int slots = op == kXent ? std::max(c.slots, 2) : c.slots;
   while (slots > 1 && kSmemHeader + int64_t(slots) * nin * slot_bytes + param_bytes > d.smem_optin)
     --slots;
   const int64_t smem = kSmemHeader + int64_t(slots) * nin * slot_bytes + param_bytes;
