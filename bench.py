@@ -362,7 +362,10 @@ def cpu_oracle_rate(op, dtype, M, N, sigma, budget_s: float, seed: int = 4242):
 
     cores = os.cpu_count() or 1
     lib = oracle.library()
-    rows = min(M, max(cores * 16, 256))
+    # enough rows per thread that each call spends its time in the C oracle,
+    # not in the Python around it (ctypes releases the GIL only inside the
+    # call); at most 2^27 elements held in float64
+    rows = min(M, max(cores * 128, 256), max(cores, (1 << 27) // N))
     d = oracle_inputs(op, dtype, rows, N, sigma, seed)
     parts = [p for p in np.array_split(np.arange(rows), cores) if p.size]
 
