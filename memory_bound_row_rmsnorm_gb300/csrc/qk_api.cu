@@ -249,12 +249,13 @@ const Choice kRmsNormTable[] = {
     {16384, 256, 256, 8, 8, 3},  {32768, 256, 256, 8, 16, 2},  {65536, 512, 512, 8, 16, 2},
 };
 // LayerNorm: from a sweep of every compiled configuration on GB300 (M = 16384,
-// N = 256 ... 262144, fp32 and bf16).  Its parameters not held in registers
-// take shared memory, so long rows keep fewer ring slots than RMSNorm.
+// N = 256 ... 262144, fp32 and bf16; rows of 512 and 2048 vectors again at
+// 8192-32768 rows).  Its parameters not held in registers take shared memory,
+// so long rows keep fewer ring slots than RMSNorm.
 const Choice kLayerNormTable[] = {
     {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 2},       {128, 256, 32, 4, 1, 2},
-    {256, 256, 32, 8, 1, 3},     {512, 128, 128, 4, 1, 2},     {1024, 128, 128, 8, 1, 1},
-    {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {256, 256, 32, 8, 1, 3},     {512, 256, 128, 4, 1, 2},     {1024, 128, 128, 8, 1, 1},
+    {2048, 512, 512, 4, 1, 2},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 8, 8, 2},  {32768, 512, 512, 8, 8, 1},   {65536, 512, 512, 8, 16, 2},
 };
 const Choice kSoftmaxTable[] = {
