@@ -22,8 +22,11 @@
 //   * RMSNorm / LayerNorm parameters: the columns a thread meets change from
 //     row to row, so each CTA stages its slice of w (and b) in shared memory
 //     once and the finish reads them element by element.
-//   * LayerNorm partials carry their element counts through the block level
-//     (a second small buffer), since they no longer follow from the geometry.
+//   * LayerNorm rows held by one CTA take two passes over the registers: the
+//     row sum, then the squared deviations from the row mean, each a plain sum
+//     through the warp and block levels (a second barrier).  Rows split over a
+//     cluster merge (count, mean, M2) partials instead, their counts carried
+//     through the block level in a second small buffer.
 // Cited: QbitAI article on QuACK, section "硬件感知的加载与存储策略" (asynchronous
 // GMEM->SMEM staging of the row, vectorised SMEM->register loads) and section
 // "硬件感知的归约策略" (thread, warp, block and cluster reduction).
@@ -65,7 +68,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + 8 * kMaxSlots);
-  float* cnt_red = reinterpret_cast<float*>(smem + 384);   // [2][16] LayerNorm warp counts
+  float* cnt_red = reinterpret_cast<float*>(smem + 384);   // [2][16] LayerNorm warp counts or M2 partials
   float2* red = reinterpret_cast<float2*>(smem + 512);
   float2* xbuf = reinterpret_cast<float2*>(smem + 768);
   unsigned char* ring = smem + kSmemHeader;
@@ -359,6 +362,19 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         }
       }
       ps = acc.x + acc.y;
+    } else if constexpr (OP == kLayerNorm && !CLUSTER) {
+      // First of two passes over the registers: the row sum (padding is 0).
+      // The squared deviations from the row mean follow the block reduction.
+      float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;
+        float f[E];
+        V::unpack(xr[k], f);
+#pragma unroll
+        for (int e = 0; e < E; e += 2) s2 = add2(s2, make_float2(f[e], f[e + 1]));
+      }
+      ps = s2.x + s2.y;
     } else if constexpr (OP == kLayerNorm) {
       float2 s2 = make_float2(0.f, 0.f);
       int cnt = 0;
@@ -464,7 +480,9 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
     // ---- warp butterfly; warp partials to the block buffer ----
     const bool row_end = (j == K - 1);
     if (row_end) {
-      if constexpr (OP == kLayerNorm) {
+      if constexpr (OP == kLayerNorm && !CLUSTER) {
+        ps = group_sum<GW>(ps);  // the row group's sum, through the barrier below
+      } else if constexpr (OP == kLayerNorm) {
         group_welford<GW>(pn, pm, ps);
         if (WPG > 1 && lane == 0) cnt_red[ibit * 16 + warp] = pn;
       } else {
@@ -495,7 +513,51 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
     if (!row_end) continue;
 
     // ---- block reduction over the warps of this row group ----
-    if constexpr (WPG > 1) {
+    if constexpr (OP == kLayerNorm && !CLUSTER) {
+      // The mean from the row sum (warp partials added in a fixed order), then
+      // the second pass: squared deviations from it, summed the same way.
+      float tot = ps;
+      if constexpr (WPG > 1) {
+        tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < WPG; ++w) tot += red[row_ibit * 16 + g * WPG + w].y;
+      }
+      const float mu = tot * a.inv_n;
+      const float2 nmu = make_float2(-mu, -mu);
+      float qd = 0.f;
+      float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;
+        const int i0 = (vb + l + k * TPR) * E;
+        const int lo = max(0, s_lo - i0), hi = min(E, s_hi - i0);
+        float f[E];
+        V::unpack(xr[k], f);
+        if (lo == 0 && hi == E) {  // a whole vector: packed
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            const float2 d = add2(make_float2(f[e], f[e + 1]), nmu);
+            q2 = fma2(d, d, q2);
+          }
+        } else {  // a partial vector at an end of the window
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float d = f[e] - mu;
+            if (e >= lo && e < hi) qd = fmaf(d, d, qd);
+          }
+        }
+      }
+      float m2 = group_sum<GW>(qd + (q2.x + q2.y));
+      if constexpr (WPG > 1) {
+        if (lane == 0) cnt_red[row_ibit * 16 + warp] = m2;
+        __syncthreads();
+        m2 = 0.f;
+#pragma unroll
+        for (int w = 0; w < WPG; ++w) m2 += cnt_red[row_ibit * 16 + g * WPG + w];
+      }
+      pm = mu;
+      ps = m2;
+    } else if constexpr (WPG > 1) {
       if constexpr (OP == kLayerNorm) {  // butterfly of width WPG; lane l takes warp l % WPG
         const int w = row_ibit * 16 + g * WPG + lane % WPG;
         pm = red[w].x;
