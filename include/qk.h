@@ -35,8 +35,15 @@
  *    otherwise).  The fast path additionally wants 16-byte aligned x, y, w and
  *    N * sizeof(dtype) a multiple of 16.  Other forward inputs take a shifted
  *    ring kernel when y has x's alignment modulo 16 (rows start anywhere inside
- *    a 16-byte vector) and a masked element kernel otherwise; both give the
- *    same results as the fast path.
+ *    a 16-byte vector) and a masked element kernel otherwise; both compute the
+ *    same definitions within the same tolerances as the fast path (the order
+ *    of their fp32 sums differs, so the last bits can).
+ *  - Launches are stream-ordered with programmatic dependent launch: a kernel
+ *    may start, and prefetch the first rows it will read into L2, while the
+ *    previous kernel on the stream is still running, but it reads its inputs
+ *    and writes its outputs only after that kernel has completed, so one call
+ *    may consume another's output (or overwrite its input) with no extra
+ *    synchronisation.
  *  - Accumulation is float32; bf16 outputs are rounded to nearest even once.
  */
 #ifndef QK_H_
