@@ -1,0 +1,105 @@
+"""Every plan the host tables can choose has a compiled kernel, for both
+dtypes -- checked without a GPU, from the plan tables in qk_api.cu and the
+kernel instantiations that the built libqk.so holds (its symbol table).  A
+table entry without its kernel would only surface on a GPU, as
+QK_ERR_UNSUPPORTED for the shapes that pick it."""
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+API = os.path.join(ROOT, "memory_bound_row_rmsnorm_gb300", "csrc", "qk_api.cu")
+DTYPES = ("float", "__nv_bfloat16")
+# template operator codes (qk_internal.h enum Op, qk_bwd_kernels.cuh enum BwdOp)
+ROW_OPS = {"kRmsNormTable": 1, "kSoftmaxTable": 0, "kXentTable": 2, "kLayerNormTable": 3}
+BWD_OPS = {"kSoftmaxBwdTable": 10, "kRmsNormBwdTable": 11, "kXentBwdTable": 12}
+SHIFT_OPS = {0: "softmax", 1: "rmsnorm", 2: "xent", 3: "layernorm", 4: "xent backward", 5: "softmax backward"}
+
+
+@pytest.fixture(scope="module")
+def kernels():
+    if shutil.which("nm") is None:
+        pytest.skip("nm is not available")
+    from memory_bound_row_rmsnorm_gb300 import build
+    lib = build.build()
+    out = subprocess.run(["nm", "-C", lib], capture_output=True, text=True, check=True).stdout
+    names = set()
+    for m in re.finditer(r"qk::(\w+_kernel)<([^>]*)>\(qk::\w+\)", out):
+        args = tuple(a.strip() for a in m.group(2).split(","))
+        names.add((m.group(1),) + args)
+    assert names, "no kernel symbols found in libqk.so"
+    return names
+
+
+def table(name):
+    text = open(API).read()
+    m = re.search(r"\b" + name + r"\[\]\s*=\s*\{(.*?)\n\};", text, re.S)
+    assert m, name
+    return [tuple(x.strip() for x in e.split(",")) for e in re.findall(r"\{([^{}]*)\}", m.group(1))]
+
+
+def b(v):
+    return "true" if v else "false"
+
+
+@pytest.mark.parametrize("name", sorted(ROW_OPS))
+def test_forward_tables(kernels, name):
+    rows = table(name)
+    assert rows
+    for max_nv, th, tpr, vpt, cl, slots in rows:
+        for dt in DTYPES:
+            key = ("row_kernel", str(ROW_OPS[name]), dt, th, tpr, vpt, b(int(cl) > 1), "false")
+            assert key in kernels, f"{name} entry {max_nv}: no {key}"
+
+
+@pytest.mark.parametrize("name", sorted(BWD_OPS))
+def test_backward_tables(kernels, name):
+    rows = table(name)
+    assert rows
+    for max_nv, th, tpr, vpt, cl, slots in rows:
+        for dt in DTYPES:
+            key = ("bwd_kernel", str(BWD_OPS[name]), dt, th, tpr, vpt, b(int(cl) > 1))
+            assert key in kernels, f"{name} entry {max_nv}: no {key}"
+
+
+def test_two_pass_kernels(kernels):
+    """Rows beyond a cluster's capacity (softmax, RMSNorm, LayerNorm): 256 x 8
+    two-pass kernels, alone and clustered."""
+    for op in (0, 1, 3):
+        for dt in DTYPES:
+            for cl in ("false", "true"):
+                assert ("row_kernel", str(op), dt, "256", "256", "8", cl, "true") in kernels
+
+
+def test_shifted_table(kernels):
+    """Unaligned rows: every row group of the shifted table for the operators
+    that use it (LayerNorm and softmax backward skip the narrow 9-vector
+    groups), and the clusters of 256 x 8 or 9 for the operators that split
+    rows."""
+    rows = table("kShiftTable")
+    assert rows
+    for op in SHIFT_OPS:
+        narrow9 = op not in (3, 5)
+        for th, tpr, vpt, slots in rows:
+            if vpt == "9" and int(tpr) < 256 and not narrow9:
+                continue
+            for dt in DTYPES:
+                key = ("shifted_kernel", str(op), dt, th, tpr, vpt, "false")
+                assert key in kernels, f"{SHIFT_OPS[op]}: no {key}"
+        if op in (0, 1, 3, 5):
+            for vpt in ("8", "9"):
+                for dt in DTYPES:
+                    assert ("shifted_kernel", str(op), dt, "256", "256", vpt, "true") in kernels
+
+
+def test_tables_are_ordered():
+    """The planner takes the first entry that holds the row, so the forward and
+    backward tables grow in max_nv and the shifted table in capacity."""
+    for name in list(ROW_OPS) + list(BWD_OPS):
+        caps = [int(r[0]) if r[0] != "kStream" else 1 << 62 for r in table(name)]
+        assert caps == sorted(caps) and len(set(caps)) == len(caps), name
+    caps = [int(r[1]) * int(r[2]) for r in table("kShiftTable")]
+    assert caps == sorted(caps), caps
