@@ -199,7 +199,8 @@ def test_backward_benchmark_shapes(op, dtype, M, N):
 
 # ---- masked path: rows whose length or start is not a multiple of 16 bytes ----
 
-MASKED_N = [1, 3, 7, 101, 513, 2047, 2049, 5001, 8191, 8193, 20001, 131071]
+MASKED_N = [1, 3, 7, 101, 513, 571, 1143, 2047, 2049, 2295, 4605, 5001, 8191, 8193, 9207, 20001,
+            131071]
 
 
 @pytest.mark.parametrize("N", MASKED_N)

@@ -56,7 +56,7 @@ def test_shifted_lengths(op, dtype, N):
     check_against_oracle(op, dtype, inp, out, what=f"shifted {dtype} {M}x{N} plan {plan['path']}")
 
 
-@pytest.mark.parametrize("N", [7, 1001, 20001])
+@pytest.mark.parametrize("N", [7, 571, 1001, 1143, 2295, 4097, 4605, 9207, 20001])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_shifted_layernorm(dtype, N):
     full = tln.full_check(dtype, 5, N, seed=10100 + N)
