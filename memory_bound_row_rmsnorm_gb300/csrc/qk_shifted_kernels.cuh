@@ -665,13 +665,13 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
             // LayerNorm 42 % -> 46 % with this).
             const int64_t c0 = cbase + i0;
             const int sh = int(c0 & 7);
+            // (With sh = 0 the window is the first vector alone; the index
+            // below then reads it twice rather than a vector past the slice.)
             const uint4* wv = reinterpret_cast<const uint4*>(wsm) + (c0 >> 3);
-            const uint4 w0 = wv[0];
-            V::unpack(bf16_window(w0, sh ? wv[1] : w0, sh), w);
+            V::unpack(bf16_window(wv[0], wv[sh ? 1 : 0], sh), w);
             if constexpr (OP == kLayerNorm) {
               const uint4* bv = reinterpret_cast<const uint4*>(bsm) + (c0 >> 3);
-              const uint4 b0 = bv[0];
-              V::unpack(bf16_window(b0, sh ? bv[1] : b0, sh), bb);
+              V::unpack(bf16_window(bv[0], bv[sh ? 1 : 0], sh), bb);
             }
           } else {
 #pragma unroll
