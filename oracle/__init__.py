@@ -66,9 +66,9 @@ def bind(path: str):
     lib.oracle_rmsnorm_bwd.restype = None
     lib.oracle_xent_bwd.argtypes = [dp, lp, dp, dp, dp, i64, i64]
     lib.oracle_xent_bwd.restype = None
-    lib.oracle_xent_fwd_ex.argtypes = [dp, lp, dp, dp, dp, i64, i64, i64, ctypes.c_double]
+    lib.oracle_xent_fwd_ex.argtypes = [dp, lp, dp, dp, dp, i64, i64, ctypes.c_int, i64, ctypes.c_double]
     lib.oracle_xent_fwd_ex.restype = None
-    lib.oracle_xent_bwd_ex.argtypes = [dp, lp, dp, dp, dp, i64, i64, i64, ctypes.c_double]
+    lib.oracle_xent_bwd_ex.argtypes = [dp, lp, dp, dp, dp, i64, i64, ctypes.c_int, i64, ctypes.c_double]
     lib.oracle_xent_bwd_ex.restype = None
     lib.oracle_layernorm_fwd.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64, ctypes.c_double]
     lib.oracle_layernorm_fwd.restype = None
@@ -170,12 +170,17 @@ def xent_bwd(x, target, lse, dloss, lib=None) -> np.ndarray:
     return dx
 
 
-NO_IGNORE = -(2 ** 63)  # an ignore index no target can equal
+def _ignore_args(ignore_index):
+    """(has_ignore, ignore_index) for the C oracle: None means no row is
+    ignored.  The index passed with the flag off is INT64_MIN, the value a
+    sentinel would use, so an oracle that tested the index alone would be
+    caught by the extreme-target pins."""
+    return (0, -(2 ** 63)) if ignore_index is None else (1, int(ignore_index))
 
 
-def xent_fwd_ex(x, target, ignore_index: int = NO_IGNORE, z: float = 0.0, lib=None):
-    """Cross-entropy with an ignore index and a z-loss term; returns
-    (loss [M], lse [M], mean over the rows not ignored)."""
+def xent_fwd_ex(x, target, ignore_index=None, z: float = 0.0, lib=None):
+    """Cross-entropy with an ignore index (None: no row is ignored) and a
+    z-loss term; returns (loss [M], lse [M], mean over the rows not ignored)."""
     lib = lib or library()
     x = _f64(x)
     M, N = x.shape
@@ -184,11 +189,11 @@ def xent_fwd_ex(x, target, ignore_index: int = NO_IGNORE, z: float = 0.0, lib=No
     lse = np.empty(M, dtype=np.float64)
     mean = np.empty(1, dtype=np.float64)
     lib.oracle_xent_fwd_ex(_ptr(x), _ptr(t, ctypes.c_int64), _ptr(loss), _ptr(lse), _ptr(mean), M, N,
-                           int(ignore_index), float(z))
+                           *_ignore_args(ignore_index), float(z))
     return loss, lse, float(mean[0])
 
 
-def xent_bwd_ex(x, target, lse, dloss, ignore_index: int = NO_IGNORE, z: float = 0.0, lib=None):
+def xent_bwd_ex(x, target, lse, dloss, ignore_index=None, z: float = 0.0, lib=None):
     """dlogits of xent_fwd_ex's per-row loss, given the forward lse and dloss [M]."""
     lib = lib or library()
     x, lse, dloss = _f64(x), _f64(lse), _f64(dloss)
@@ -196,7 +201,7 @@ def xent_bwd_ex(x, target, lse, dloss, ignore_index: int = NO_IGNORE, z: float =
     t = np.ascontiguousarray(target, dtype=np.int64)
     dx = np.empty_like(x)
     lib.oracle_xent_bwd_ex(_ptr(x), _ptr(t, ctypes.c_int64), _ptr(lse), _ptr(dloss), _ptr(dx), M, N,
-                           int(ignore_index), float(z))
+                           *_ignore_args(ignore_index), float(z))
     return dx
 
 

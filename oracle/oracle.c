@@ -183,8 +183,11 @@ void oracle_xent_bwd(const double *x, const int64_t *target, const double *lse,
 
 /* ------------------------------------------------------------------------
  * Cross-entropy variants (ignore index, z-loss, mean over rows).
- *   loss_i = lse_i - x_{i,t_i} + z * lse_i^2      for t_i != ignore_index,
- *   loss_i = 0                                    for t_i == ignore_index,
+ * A row is ignored when has_ignore is nonzero and t_i == ignore_index; with
+ * has_ignore == 0 no row is ignored, whatever its target (no target value
+ * stands for "none", so INT64_MIN is an ordinary out-of-range target).
+ *   loss_i = lse_i - x_{i,t_i} + z * lse_i^2      for a row not ignored,
+ *   loss_i = 0                                    for an ignored row,
  *   mean   = sum of loss_i over the rows not ignored / their number
  *            (NaN when every row is ignored: 0 / 0);
  *   dx_ij  = dloss_i * ((1 + 2 z lse_i) exp(x_ij - lse_i) - [j == t_i]),
@@ -192,7 +195,8 @@ void oracle_xent_bwd(const double *x, const int64_t *target, const double *lse,
  * A target that is neither ignored nor inside [0, N) gives NaN, as before.
  * ------------------------------------------------------------------------ */
 void oracle_xent_fwd_ex(const double *x, const int64_t *target, double *loss, double *lse,
-                        double *mean, int64_t M, int64_t N, int64_t ignore_index, double z)
+                        double *mean, int64_t M, int64_t N, int has_ignore, int64_t ignore_index,
+                        double z)
 {
     double total = 0.0;
     int64_t counted = 0;
@@ -210,7 +214,7 @@ void oracle_xent_fwd_ex(const double *x, const int64_t *target, double *loss, do
         double l = m + log(s);
         int64_t t = target[i];
         double li;
-        if (t == ignore_index) {
+        if (has_ignore && t == ignore_index) {
             li = 0.0;
         } else {
             li = (t >= 0 && t < N) ? l - xi[t] + z * l * l : NAN;
@@ -225,7 +229,7 @@ void oracle_xent_fwd_ex(const double *x, const int64_t *target, double *loss, do
 
 void oracle_xent_bwd_ex(const double *x, const int64_t *target, const double *lse,
                         const double *dloss, double *dx, int64_t M, int64_t N,
-                        int64_t ignore_index, double z)
+                        int has_ignore, int64_t ignore_index, double z)
 {
     for (int64_t i = 0; i < M; ++i) {
         const double *xi = x + i * N;
@@ -233,7 +237,7 @@ void oracle_xent_bwd_ex(const double *x, const int64_t *target, const double *ls
         int64_t t = target[i];
 
         for (int64_t j = 0; j < N; ++j) {
-            if (t == ignore_index) {
+            if (has_ignore && t == ignore_index) {
                 di[j] = 0.0;
             } else if (t >= 0 && t < N) {
                 double p = exp(xi[j] - lse[i]);

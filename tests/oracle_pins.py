@@ -468,6 +468,27 @@ def pin_xent_ex_reduces_to_plain(lib):
     assert math.isnan(all_ignored), "xent ex: the mean of no rows is NaN"
 
 
+def pin_xent_ex_no_sentinel_target(lib):
+    """Without an ignore index no target value is special: the extreme int64
+    targets are out of range and give NaN exactly as in the plain loss, and
+    with that value as the ignore index the same row is ignored."""
+    rng = _rng(32)
+    x = rng.normal(size=(4, 9))
+    t = np.array([-(2 ** 63), 3, 2 ** 63 - 1, 0], dtype=np.int64)
+    loss0, lse0 = oracle.xent_fwd(x, t, lib)
+    assert np.isnan(loss0[[0, 2]]).all() and np.isfinite(loss0[[1, 3]]).all(), "xent: extreme targets"
+    loss, lse, _ = oracle.xent_fwd_ex(x, t, lib=lib)
+    assert np.isnan(loss[[0, 2]]).all(), "xent ex: INT64_MIN / INT64_MAX targets are out of range"
+    _close(loss[[1, 3]], loss0[[1, 3]], 1e-15, "xent ex: in-range rows beside extreme targets")
+    g = np.ones(4)
+    dx = oracle.xent_bwd_ex(x, t, lse, g, lib=lib)
+    assert np.isnan(dx[[0, 2]]).all() and np.isfinite(dx[[1, 3]]).all(), "xent ex bwd: extreme targets"
+    loss_i = oracle.xent_fwd_ex(x, t, ignore_index=-(2 ** 63), lib=lib)[0]
+    assert loss_i[0] == 0.0 and np.isnan(loss_i[2]), "xent ex: INT64_MIN as the ignore index"
+    dx_i = oracle.xent_bwd_ex(x, t, lse, g, ignore_index=-(2 ** 63), lib=lib)
+    assert np.all(dx_i[0] == 0.0) and np.isnan(dx_i[2]).all(), "xent ex bwd: INT64_MIN as the ignore index"
+
+
 def pin_xent_ex_bwd_finite_differences(lib):
     rng = _rng(31)
     x = rng.normal(0, 1.5, size=(4, 6))

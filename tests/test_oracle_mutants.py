@@ -51,8 +51,12 @@ MUTANTS = [
     ("xent ex: ignored rows counted in the mean", "            total += li;\n            counted += 1;\n        }",
      "            total += li;\n        }\n        counted += 1;"),
     ("xent ex bwd: z-loss gradient factor 1 + z lse", "(1.0 + 2.0 * z * lse[i])", "(1.0 + z * lse[i])"),
-    ("xent ex bwd: ignored rows not zeroed", "            if (t == ignore_index) {\n                di[j] = 0.0;",
-     "            if (t == ignore_index) {\n                di[j] = dloss[i];"),
+    ("xent ex bwd: ignored rows not zeroed", "            if (has_ignore && t == ignore_index) {\n                di[j] = 0.0;",
+     "            if (has_ignore && t == ignore_index) {\n                di[j] = dloss[i];"),
+    ("xent ex: the ignore index is a sentinel", "        if (has_ignore && t == ignore_index) {\n            li = 0.0;",
+     "        if (t == ignore_index) {\n            li = 0.0;"),
+    ("xent ex bwd: the ignore index is a sentinel", "            if (has_ignore && t == ignore_index) {\n                di[j] = 0.0;",
+     "            if (t == ignore_index) {\n                di[j] = 0.0;"),
     ("layernorm: sample variance", "double var = sq / (double)N;", "double var = sq / (double)(N - 1);"),
     ("layernorm: mean not subtracted in the variance", "sq += (xi[j] - mu) * (xi[j] - mu);", "sq += xi[j] * xi[j];"),
     ("layernorm: eps outside the root", "double r = 1.0 / sqrt(var + eps);", "double r = 1.0 / (sqrt(var) + eps);"),
