@@ -45,6 +45,13 @@
  *    may consume another's output (or overwrite its input) with no extra
  *    synchronisation.
  *  - Accumulation is float32; bf16 outputs are rounded to nearest even once.
+ *  - Per-device state (the device's properties, kernel attributes, occupancy
+ *    answers, the device addresses of the status word and of the
+ *    no-allocation scratch array) is set up by the first call made on each
+ *    device and kept until the process exits.  A cudaDeviceReset() of a device
+ *    after the library's first call on it is not supported: the cached
+ *    addresses and kernel attributes no longer match the new context, so
+ *    calls on that device may fail to launch or touch stale addresses.
  */
 #ifndef QK_H_
 #define QK_H_
@@ -219,7 +226,10 @@ QK_API qk_status qk_rmsnorm_bwd(const void* x, const void* w, const float* rstd,
  * (qk_rmsnorm_bwd_workspace_size) exceeds 16 MiB return QK_ERR_UNSUPPORTED.
  *
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * that device current); make that first call before any stream capture.  The
+ * address is kept for the life of the process: after a cudaDeviceReset() of
+ * that device it is stale, so do not call this entry point on a device that
+ * was reset after its first call (see the per-device state note at the top).
  * Every call on a device shares the one array: calls whose kernels overlap on
  * the GPU (for example on two streams) race on it and must be serialised by
  * the caller.  Nothing in it needs clearing between calls: each call writes
@@ -244,17 +254,21 @@ QK_API qk_status qk_xent_bwd(const void* logits, const int64_t* targets, const f
 /*
  * Cross-entropy variants.  Options of qk_xent_fwd_ex / qk_xent_bwd_ex (NULL
  * means the plain operator: no ignore index, no z-loss):
- *   ignore_index  rows whose target equals it get loss 0 and zero gradient and
- *                 are left out of the mean (QK_NO_IGNORE_INDEX: none);
- *   z_loss        coefficient z of the term z * lse^2 added to each row's loss
- *                 (a penalty on the log-partition function; 0: none).
+ *   has_ignore_index  nonzero: rows whose target equals ignore_index get loss 0
+ *                     and zero gradient and are left out of the mean.  Zero:
+ *                     no row is ignored, and every target outside [0, N) --
+ *                     INT64_MIN and INT64_MAX included -- gives NaN as in
+ *                     qk_xent_fwd; ignore_index is then not read.
+ *   ignore_index      the target value of ignored rows (any int64).
+ *   z_loss            coefficient z of the term z * lse^2 added to each row's
+ *                     loss (a penalty on the log-partition function; 0: none).
  * The article names cross-entropy loss only; these are the common training
  * variants of the same per-row definition, added in its epilogue.
  */
-#define QK_NO_IGNORE_INDEX INT64_MIN
 typedef struct {
-  int64_t ignore_index;
+  int32_t has_ignore_index;
   float z_loss;
+  int64_t ignore_index;
 } qk_xent_options;
 
 /*

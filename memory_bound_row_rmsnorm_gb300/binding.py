@@ -37,7 +37,6 @@ _EXPORTS = (
     "qk_rmsnorm_bwd_workspace_size", "qk_xent_bwd", "qk_rmsnorm_bwd_noalloc",
     "qk_xent_fwd_ex", "qk_xent_bwd_ex", "qk_layernorm_fwd",
 )
-QK_NO_IGNORE_INDEX = -(2 ** 63)
 
 
 class QkError(RuntimeError):
@@ -47,7 +46,8 @@ class QkError(RuntimeError):
 
 
 class qk_xent_options(ctypes.Structure):
-    _fields_ = [("ignore_index", ctypes.c_int64), ("z_loss", ctypes.c_float)]
+    _fields_ = [("has_ignore_index", ctypes.c_int32), ("z_loss", ctypes.c_float),
+                ("ignore_index", ctypes.c_int64)]
 
 
 class qk_plan(ctypes.Structure):
@@ -66,6 +66,9 @@ _lib = None
 def load_library(path: str = LIBRARY):
     """Load libqk.so (once) and declare its signatures; raises if it is missing."""
     global _lib
+    lib = _lib
+    if lib is not None:  # every call after the first: no lock
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -193,7 +196,7 @@ def _options(ignore_index, z_loss):
     if ignore_index is None and not z_loss:
         return None
     return ctypes.byref(qk_xent_options(
-        QK_NO_IGNORE_INDEX if ignore_index is None else int(ignore_index), float(z_loss)))
+        0 if ignore_index is None else 1, float(z_loss), 0 if ignore_index is None else int(ignore_index)))
 
 
 def qk_xent_fwd_ex(logits, targets, loss, lse, mean_loss, M: int, N: int, dtype: int,

@@ -899,7 +899,8 @@ qk_status qk_layernorm_fwd(const void* x, const void* w, const void* b, void* y,
 qk_status qk_xent_fwd_ex(const void* logits, const int64_t* targets, float* loss, float* lse,
                          float* mean_loss, int64_t M, int64_t N, qk_dtype dtype,
                          const qk_xent_options* options, void* stream) {
-  const int64_t ignore = options != nullptr ? options->ignore_index : QK_NO_IGNORE_INDEX;
+  const int has_ignore = options != nullptr && options->has_ignore_index != 0;
+  const int64_t ignore = has_ignore ? options->ignore_index : 0;
   const float z = options != nullptr ? options->z_loss : 0.f;
   qk_status st = check_sizes(kXent, dtype, M, N);
   if (st != QK_OK) return st;
@@ -925,6 +926,7 @@ qk_status qk_xent_fwd_ex(const void* logits, const int64_t* targets, float* loss
   a.M = M;
   a.N = N;
   a.ignore_index = ignore;
+  a.has_ignore = has_ignore;
   a.z_loss = z;
   const bool fast = aligned16(logits) && (N * int64_t(es)) % 16 == 0;
   st = run(kXent, dtype, a, row_path(fast, true), stream);
@@ -939,7 +941,7 @@ qk_status qk_xent_fwd_ex(const void* logits, const int64_t* targets, float* loss
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const float* lp = loss;
-  if (cudaLaunchKernelEx(&cfg, xent_mean_kernel<0>, lp, targets, M, ignore, mean_loss) !=
+  if (cudaLaunchKernelEx(&cfg, xent_mean_kernel<0>, lp, targets, M, has_ignore, ignore, mean_loss) !=
       cudaSuccess) {
     cudaGetLastError();
     return QK_ERR_LAUNCH;
@@ -1058,7 +1060,8 @@ qk_status qk_rmsnorm_bwd(const void* x, const void* w, const float* rstd, const 
 qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float* lse,
                          const float* dloss, void* dlogits, int64_t M, int64_t N, qk_dtype dtype,
                          const qk_xent_options* options, void* stream) {
-  const int64_t ignore = options != nullptr ? options->ignore_index : QK_NO_IGNORE_INDEX;
+  const int has_ignore = options != nullptr && options->has_ignore_index != 0;
+  const int64_t ignore = has_ignore ? options->ignore_index : 0;
   const float z = options != nullptr ? options->z_loss : 0.f;
   qk_status st = check_sizes(kOpXentBwd, dtype, M, N);
   if (st != QK_OK) return st;
@@ -1086,6 +1089,7 @@ qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float
     r.M = M;
     r.N = N;
     r.ignore_index = ignore;
+    r.has_ignore = has_ignore;
     r.z_loss = z;
     st = run(kOpXentBwd, dtype, r, kPathShifted, stream);
     if (st != QK_ERR_UNSUPPORTED) return st;
@@ -1099,6 +1103,7 @@ qk_status qk_xent_bwd_ex(const void* logits, const int64_t* targets, const float
   a.M = M;
   a.N = N;
   a.ignore_index = ignore;
+  a.has_ignore = has_ignore;
   a.z_loss = z;
   return run_bwd(kOpXentBwd, dtype, a, nullptr, 0, fast, stream);
 }

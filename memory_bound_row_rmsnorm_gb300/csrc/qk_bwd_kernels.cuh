@@ -38,7 +38,8 @@ struct BwdArgs {
   int64_t N;
   float inv_n;          // 1 / N
   float z_loss;         // x-entropy: z-loss coefficient (gradient factor 1 + 2 z lse)
-  int64_t ignore_index; // x-entropy: rows with this target get zero gradient
+  int64_t ignore_index; // x-entropy: rows with this target get zero gradient (when has_ignore)
+  int32_t has_ignore;   // x-entropy: nonzero when ignore_index is in use
   int32_t chunks;       // ring steps per row (streamed x-entropy rows), else 1
   int32_t slots;        // ring slots per CTA
   uint32_t slot_bytes;  // bytes of ONE input's item in a slot (multiple of 128)
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, (bwd_min_blocks<OP, THREADS, VPT>()))
         og[l + k * TPR] = V::pack(o);
       }
     } else {  // cross-entropy: dloss * (exp(x - lse) - onehot)
-      const bool ignored = (trow == a.ignore_index);
+      const bool ignored = a.has_ignore && trow == a.ignore_index;
       const bool tok = trow >= 0 && trow < N;
       // zero row if ignored, NaN row for a bad target; the z-loss term scales
       // the softmax part by 1 + 2 z lse
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(THREADS) bwd_direct_kernel(const BwdArgs a) {
       const float lse = __ldg(a.lse + row);
       const float gr = a.dloss != nullptr ? __ldg(a.dloss + row) : 1.f;
       const int64_t t = __ldg(a.target + row);
-      const bool ignored = (t == a.ignore_index), tok = t >= 0 && t < N;
+      const bool ignored = a.has_ignore && t == a.ignore_index, tok = t >= 0 && t < N;
       const float gv = ignored ? 0.f : (tok ? gr : __int_as_float(0x7fc00000));
       const float zf = fmaf(2.f * a.z_loss, lse, 1.f);
       const float lb = lse * kLog2e;

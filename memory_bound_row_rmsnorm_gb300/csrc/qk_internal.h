@@ -29,7 +29,8 @@ struct RowArgs {
   float eps;
   float inv_n;          // 1 / N, rounded once on the host (RMSNorm mean)
   float z_loss;         // cross-entropy: coefficient of z * lse^2 added to the loss (0: none)
-  int64_t ignore_index; // cross-entropy: rows with this target give loss 0 (INT64_MIN: none)
+  int64_t ignore_index; // cross-entropy: rows with this target give loss 0 (when has_ignore)
+  int32_t has_ignore;   // cross-entropy: nonzero when ignore_index is in use (no target value means "none")
   int32_t chunks;       // ring slots one row slice spans (streamed rows), else 1
   int64_t chunk_elems;  // shifted kernel, streamed rows: elements of one chunk, ceil(N / chunks)
   int32_t slots;        // ring slots per CTA

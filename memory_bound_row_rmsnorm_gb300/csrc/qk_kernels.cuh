@@ -763,7 +763,7 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, T, THREADS, VPT, 
       }
     } else {
       const bool leader = (l == 0 && rank == 0);
-      const bool ignored = (trow == a.ignore_index);
+      const bool ignored = a.has_ignore && trow == a.ignore_index;
       if (leader || own_t) {  // only the threads that write need the logarithm
         const float lse = pm + logf(ps);
         if (leader) {
@@ -975,7 +975,7 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
     }
   } else {
     const float lse = pm + logf(ps);
-    const bool ignored = (trow == a.ignore_index);
+    const bool ignored = a.has_ignore && trow == a.ignore_index;
     if (tid == 0 && rank == 0) {
       if (a.lse != nullptr) a.lse[row] = lse;
       if (ignored) {
@@ -989,13 +989,14 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
   if constexpr (CLUSTER) cluster_sync_all();
 }
 
-// Mean of the per-row losses over the rows whose target is not ignore_index
-// (NaN when there are none): one CTA, each thread summing a fixed strided
+// Mean of the per-row losses over the rows not ignored (with has_ignore, those
+// whose target is not ignore_index; NaN when there are none): one CTA, each thread summing a fixed strided
 // subset in order, then a fixed-shape tree -- deterministic.
 template <int kUnused = 0>
 __global__ void __launch_bounds__(1024) xent_mean_kernel(const float* __restrict__ loss,
                                                          const int64_t* __restrict__ target,
-                                                         int64_t M, int64_t ignore_index,
+                                                         int64_t M, int has_ignore,
+                                                         int64_t ignore_index,
                                                          float* __restrict__ mean) {
   __shared__ float ssum[1024];
   __shared__ int64_t scnt[1024];
@@ -1005,7 +1006,7 @@ __global__ void __launch_bounds__(1024) xent_mean_kernel(const float* __restrict
   float acc = 0.f;
   int64_t cnt = 0;
   for (int64_t i = tid; i < M; i += 1024) {
-    if (target[i] != ignore_index) {
+    if (!(has_ignore && target[i] == ignore_index)) {
       acc += loss[i];
       ++cnt;
     }

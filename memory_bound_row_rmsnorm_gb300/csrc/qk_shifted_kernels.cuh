@@ -286,13 +286,13 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
 
     // ---- cross-entropy backward: no reduction, every step writes its chunk ----
     // dlogits = dloss * ((1 + 2 z lse) exp(x - lse) - onehot(t)); a row whose
-    // target is ignore_index gets 0, one with a target outside [0, N) NaN.
+    // target is the ignore index (if any) gets 0, one with a target outside [0, N) NaN.
     if constexpr (OP == kXentGrad) {
       if (j == 0 && row_ok) {
         const float lse = __ldg(a.lse + row);
         g_t = __ldg(a.target + row);
         const float gr = a.dloss != nullptr ? __ldg(a.dloss + row) : 1.f;
-        const bool ignored = (g_t == a.ignore_index), tok = g_t >= 0 && g_t < N;
+        const bool ignored = a.has_ignore && g_t == a.ignore_index, tok = g_t >= 0 && g_t < N;
         g_gv = ignored ? 0.f : (tok ? gr : __int_as_float(0x7fc00000));
         g_zf = fmaf(2.f * a.z_loss, lse, 1.f);
         g_lb = lse * kLog2e;
@@ -615,7 +615,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
     unsigned char* yb = static_cast<unsigned char*>(a.y);
     if constexpr (OP == kXent) {
       const bool leader = (l == 0 && rank == 0);
-      const bool ignored = (trow == a.ignore_index);
+      const bool ignored = a.has_ignore && trow == a.ignore_index;
       if (leader || own_t) {
         const float lse = pm + logf(ps);
         if (leader) {

@@ -170,15 +170,15 @@ def test_backward_forced_plans(op, dtype, pi):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_xent_backward_bad_targets_and_default_dloss(dtype):
-    case = make_case("xent", dtype, 6, 1024, seed=8000)
-    case["targets"] = torch.tensor([-1, 1024, 0, 1023, 2 ** 40, 5], dtype=torch.int64)
+    case = make_case("xent", dtype, 8, 1024, seed=8000)
+    case["targets"] = torch.tensor([-1, 1024, 0, 1023, 2 ** 40, 5, -(2 ** 63), 2 ** 63 - 1], dtype=torch.int64)
     d = {k: v.to(DEV) for k, v in case.items()}
     dx = torch.empty_like(d["x"])
-    qb.qk_xent_bwd(d["x"], d["targets"], d["lse"], None, dx, 6, 1024, DT[dtype])  # dloss = 1
+    qb.qk_xent_bwd(d["x"], d["targets"], d["lse"], None, dx, 8, 1024, DT[dtype])  # dloss = 1
     torch.cuda.synchronize()
-    case["dloss"] = torch.ones(6)
+    case["dloss"] = torch.ones(8)
     check("xent", dtype, case, {"dx": dx}, "bad targets, dloss = 1")
-    assert torch.isnan(dx[[0, 1, 4]]).all() and torch.isfinite(dx[[2, 3, 5]]).all()
+    assert torch.isnan(dx[[0, 1, 4, 6, 7]]).all() and torch.isfinite(dx[[2, 3, 5]]).all()
 
 
 def test_rmsnorm_backward_is_deterministic():
@@ -278,15 +278,15 @@ def test_backward_masked_in_place(op, dtype):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_xent_backward_masked_bad_targets(dtype):
     N = 1001
-    case = make_case("xent", dtype, 6, N, seed=9700)
-    case["targets"] = torch.tensor([-1, N, 0, N - 1, 2 ** 40, 5], dtype=torch.int64)
+    case = make_case("xent", dtype, 8, N, seed=9700)
+    case["targets"] = torch.tensor([-1, N, 0, N - 1, 2 ** 40, 5, -(2 ** 63), 2 ** 63 - 1], dtype=torch.int64)
     d = {k: v.to(DEV) for k, v in case.items()}
     dx = torch.empty_like(d["x"])
-    qb.qk_xent_bwd(d["x"], d["targets"], d["lse"], None, dx, 6, N, DT[dtype])  # dloss = 1
+    qb.qk_xent_bwd(d["x"], d["targets"], d["lse"], None, dx, 8, N, DT[dtype])  # dloss = 1
     torch.cuda.synchronize()
-    case["dloss"] = torch.ones(6)
+    case["dloss"] = torch.ones(8)
     check("xent", dtype, case, {"dx": dx}, "masked, bad targets, dloss = 1")
-    assert torch.isnan(dx[[0, 1, 4]]).all() and torch.isfinite(dx[[2, 3, 5]]).all()
+    assert torch.isnan(dx[[0, 1, 4, 6, 7]]).all() and torch.isfinite(dx[[2, 3, 5]]).all()
 
 
 def test_masked_rows_beyond_the_limit_are_refused():

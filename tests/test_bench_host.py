@@ -71,3 +71,44 @@ def test_peaks():
     assert peak > 1000 and isinstance(source, str)
     assert bench.NOMINAL_HBM_GBS == 7900.0
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_clock_windows_by_timestamp():
+    """Samples carry nvidia-smi's timestamp; a window keeps only its own."""
+    import datetime
+    cs = bench.ClockSampler(0)
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    def line(dt_s, mhz, cap="Not Active"):
+        ts = (base + datetime.timedelta(seconds=dt_s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, 0, {mhz}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+    cs.lines = [line(0.0, 1500), line(0.1, 2070), line(0.2, 2070, "Active"), line(0.3, 1000)]
+    t = base.timestamp()
+    w = cs.summary(t + 0.05, t + 0.25)
+    assert w["samples"] == 2 and w["sm_mhz"] == 2070 and w["reasons"] == ["sw_power_cap"]
+    assert cs.summary()["samples"] == 4
+    assert cs.summary(t + 5, t + 6)["samples"] == 0
+
+
+def test_rotating_sets_and_kernel_counts():
+    L2 = bench.L2_BYTES
+    assert bench.n_sets(4 * L2) == 1 and bench.n_sets(10 * L2) == 1
+    assert bench.n_sets(L2) == 4 and bench.n_sets(4 * L2 - 1) == 2
+    for b in (1, 10 ** 6, L2 // 3, 2 * L2):  # together they pass 4x L2
+        assert bench.n_sets(b) * b >= 4 * L2
+    assert bench.kernels_per_step("rmsnorm_bwd") == 2
+    assert all(bench.kernels_per_step(op) == 1 for op in ("softmax", "rmsnorm", "xent", "layernorm"))
+
+
+def test_sweep_summary():
+    cs = bench.ClockSampler(0)
+    pts = []
+    for N, f in ((1024, 0.4), (4096, 0.9), (16384, 0.8), (65536, 0.95)):
+        pts.append({"op": "softmax", "dtype": "f32", "M": 8192, "N": N, "frac": f, "frac_stream": f - 0.1,
+                    "TBps": f * 6.8, "clocks": {"sm_mhz": 2070}})
+    s = bench.sweep_summary(pts, (0.0, 1.0), cs)
+    k = s["per_kernel"]["softmax_f32"]
+    assert k["points"] == 4 and k["points_N_ge_4096"] == 3
+    assert k["min_frac_N_ge_4096"] == 0.8 and k["worst"]["N"] == 16384
+    assert k["median_frac_N_ge_4096"] == 0.9
+    assert s["points_N_ge_4096_at_or_above_0.85"] == 2 and s["points_N_ge_4096"] == 3
+    assert len(s["points"]) == 4 and s["points"][0][:4] == ["softmax", "f32", 8192, 1024]

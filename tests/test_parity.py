@@ -278,17 +278,52 @@ def test_rmsnorm_zero_and_constant_rows(dtype):
     assert abs(out["rstd"][0].item() - EPS ** -0.5) <= 1e-5 * EPS ** -0.5
 
 
+INT64_MIN, INT64_MAX = -(2 ** 63), 2 ** 63 - 1
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("N", [10, 4096, 131072])
 def test_xent_targets_out_of_range(dtype, N):
-    M = 6
+    """Every target outside [0, N) gives NaN, the extreme int64 values too
+    (no target value stands for "no ignore index").  N = 10 takes the
+    shifted kernel, 4096 the ring, 131072 the streamed ring."""
+    M = 8
     inp = syn.make_inputs("xent", dtype, M, N, 800, "cpu")
-    inp["targets"] = torch.tensor([-1, N, 0, N - 1, 2 ** 40, -(2 ** 40)], dtype=torch.int64)
+    inp["targets"] = torch.tensor([-1, N, 0, N - 1, 2 ** 40, -(2 ** 40), INT64_MIN, INT64_MAX],
+                                  dtype=torch.int64)
     out = run_gpu("xent", {k: v.to(DEV) for k, v in inp.items()}, dtype)
     check_against_oracle("xent", dtype, inp, out, what="targets out of range")
     loss = out["loss"].cpu()
-    assert torch.isnan(loss[[0, 1, 4, 5]]).all() and torch.isfinite(loss[[2, 3]]).all()
+    assert torch.isnan(loss[[0, 1, 4, 5, 6, 7]]).all() and torch.isfinite(loss[[2, 3]]).all()
     assert torch.isfinite(out["lse"]).all()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("N", [10, 4096, 131072, 4101])
+def test_xent_extreme_targets_through_the_variants(dtype, N):
+    """qk_xent_fwd_ex without an ignore index treats INT64_MIN / INT64_MAX
+    as out of range (NaN); with INT64_MIN as the ignore index that row is
+    ignored (loss 0, left out of the mean) and INT64_MAX is still NaN."""
+    M = 8
+    inp = syn.make_inputs("xent", dtype, M, N, 810, "cpu")
+    t = torch.tensor([INT64_MIN, 3, INT64_MAX, 0, N - 1, 1, INT64_MIN, 2], dtype=torch.int64)
+    inp["targets"] = t
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    x64 = to_f64(inp["x"])
+    for ignore in (None, INT64_MIN):
+        loss = torch.full((M,), float("nan"), dtype=torch.float32, device=DEV)
+        lse = torch.full((M,), float("nan"), dtype=torch.float32, device=DEV)
+        qb.qk_xent_fwd_ex(d["x"], d["targets"], loss, lse, None, M, N, DT_CODE[dtype], ignore_index=ignore)
+        torch.cuda.synchronize()
+        ref_loss, ref_lse, _ = oracle.xent_fwd_ex(x64, t.numpy(), ignore_index=ignore)
+        check_scalars(to_f64(lse), ref_lse, f"xent ex lse, ignore {ignore}")
+        check_scalars(to_f64(loss), ref_loss, f"xent ex loss, ignore {ignore}",
+                      denom=loss_denominator(ref_loss, ref_lse))
+        got = loss.cpu()
+        if ignore is None:
+            assert torch.isnan(got[[0, 2, 6]]).all()
+        else:
+            assert (got[[0, 6]] == 0).all() and torch.isnan(got[2])
 
 
 def test_xent_constant_row_is_log_n():

@@ -1,9 +1,11 @@
 """Parity at the benchmark workloads' full sizes, in the launch configuration
 bench.py times (the library's default plan), and on the M x N sweep grid.
 
-The matrices are too large for the oracle to check whole, so 64 seeded rows
-(always including the first and the last) are compared element by element,
-and every row is checked against properties that hold at any size:
+Matrices of at most 2^27 elements (softmax 1024 x 4096, RMSNorm 16384 x 4096)
+are compared with the oracle element by element on every row, in blocks of
+rows.  Larger ones are compared on 256 seeded rows (always including the
+first and the last), and every row is checked against properties that hold
+at any size:
   softmax   every entry finite and >= 0, each row sums to 1;
   RMSNorm   rstd finite, 0 < rstd <= eps^-1/2, mean_j (y_ij / w_j)^2 = ms_i/(ms_i+eps) ~ 1;
   x-entropy lse finite and in [max_j x_ij, max_j x_ij + ln N], loss = lse - x_t >= 0.
@@ -34,9 +36,18 @@ def library():
     torch.cuda.empty_cache()
 
 
+WHOLE_MATRIX_ELEMENTS = 1 << 27  # up to this size every row goes to the oracle
+SAMPLED_ROWS = 256
+ORACLE_BLOCK_ELEMENTS = 1 << 22  # rows handed to the oracle at a time
+
+
 def sample_rows(M, seed):
+    """SAMPLED_ROWS seeded rows, the first and the last among them."""
     rng = np.random.default_rng(seed)
-    rows = set(rng.choice(M, size=min(M, 62), replace=False).tolist()) | {0, M - 1}
+    rows = set(rng.choice(M, size=min(M, SAMPLED_ROWS - 2), replace=False).tolist()) | {0, M - 1}
+    extra = iter(rng.permutation(M).tolist())
+    while len(rows) < min(M, SAMPLED_ROWS):
+        rows.add(next(extra))
     return torch.tensor(sorted(rows), dtype=torch.int64)
 
 
@@ -63,18 +74,28 @@ def whole_matrix_properties(op, dtype, inp, out, N):
         assert (loss >= -1e-6).all()
 
 
-def check_workload(op, dtype, M, N, sigma, seed):
-    inp = syn.make_inputs(op, dtype, M, N, seed, DEV, sigma)
-    out = run_gpu(op, inp, dtype)
-    rows = sample_rows(M, seed)
-    idx = rows.to(DEV)
+def check_rows_against_oracle(op, dtype, inp, out, idx, what):
+    """The oracle on rows `idx` (a device index tensor) of the inputs."""
     inp_rows = {"x": inp["x"].index_select(0, idx).cpu()}
     if op == "rmsnorm":
         inp_rows["w"] = inp["w"].cpu()
     if op == "xent":
         inp_rows["targets"] = inp["targets"].index_select(0, idx).cpu()
     out_rows = {k: v.index_select(0, idx) for k, v in out.items()}
-    check_against_oracle(op, dtype, inp_rows, out_rows, what=f"{op} {dtype} {M}x{N} sampled rows")
+    check_against_oracle(op, dtype, inp_rows, out_rows, what=what)
+
+
+def check_workload(op, dtype, M, N, sigma, seed):
+    inp = syn.make_inputs(op, dtype, M, N, seed, DEV, sigma)
+    out = run_gpu(op, inp, dtype)
+    if M * N <= WHOLE_MATRIX_ELEMENTS:
+        block = max(1, ORACLE_BLOCK_ELEMENTS // N)
+        for r0 in range(0, M, block):
+            idx = torch.arange(r0, min(M, r0 + block), device=DEV)
+            check_rows_against_oracle(op, dtype, inp, out, idx, f"{op} {dtype} {M}x{N} rows {r0}+")
+    else:
+        idx = sample_rows(M, seed).to(DEV)
+        check_rows_against_oracle(op, dtype, inp, out, idx, f"{op} {dtype} {M}x{N} sampled rows")
     whole_matrix_properties(op, dtype, inp, out, N)
     del inp, out
     torch.cuda.empty_cache()

@@ -99,3 +99,49 @@ def test_backward(dtype, N, z):
     scale = np.abs(to_f64(g))[:, None] * (np.abs(1 + 2 * z * lse32)[:, None] * p + onehot)
     check_scaled(to_f64(dx), ref, scale, dtype, f"xent bwd ex z={z}")
     assert torch.all(dx.cpu()[t == -100] == 0)
+
+
+@pytest.mark.parametrize("ignore", [None, -(2 ** 63)])
+@pytest.mark.parametrize("N", [1024, 1001, 131072])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_extreme_targets_forward_mean_and_backward(dtype, N, ignore):
+    """INT64_MIN and INT64_MAX targets: out of range (NaN loss, NaN gradient
+    row) when no ignore index is given; with INT64_MIN as the ignore index,
+    those rows give loss 0, a zero gradient and stay out of the mean, while
+    INT64_MAX rows are still NaN.  Ring (1024), shifted (1001) and streamed
+    (131072) rows."""
+    M = 6
+    x = syn.normal_rows(M, N, dtype, 40 + N, "cpu", sigma=2 ** 0.5)
+    t = torch.tensor([-(2 ** 63), 5, 2 ** 63 - 1, 0, N - 1, -(2 ** 63)], dtype=torch.int64)
+    ref_loss, ref_lse, ref_mean = oracle.xent_fwd_ex(to_f64(x), t.numpy(), ignore_index=ignore)
+    xd, td = x.to(DEV), t.to(DEV)
+    loss = torch.full((M,), float("nan"), device=DEV)
+    lse = torch.full((M,), float("nan"), device=DEV)
+    mean = torch.full((1,), 0.0, device=DEV)
+    qb.qk_xent_fwd_ex(xd, td, loss, lse, mean, M, N, DT[dtype], ignore_index=ignore)
+    torch.cuda.synchronize()
+    assert qb.qk_get_device_status() == qb.QK_OK
+    check_scalars(to_f64(lse), ref_lse, "lse")
+    check_scalars(to_f64(loss), ref_loss, "loss", denom=loss_denominator(ref_loss, ref_lse))
+    # INT64_MAX is never ignored, so the mean over the rows not ignored is NaN either way
+    assert math.isnan(mean.item()) and math.isnan(ref_mean)
+    g = syn.uniform_weight(M, "f32", 9, "cpu", lo=0.25, hi=2.0)
+    ref = oracle.xent_bwd_ex(to_f64(x), t.numpy(), ref_lse, to_f64(g), ignore_index=ignore)
+    dx = torch.full_like(xd, float("nan"))
+    qb.qk_xent_bwd_ex(xd, td, torch.from_numpy(ref_lse).float().to(DEV), g.to(DEV), dx, M, N, DT[dtype],
+                      ignore_index=ignore)
+    torch.cuda.synchronize()
+    assert qb.qk_get_device_status() == qb.QK_OK
+    lse32 = to_f64(torch.from_numpy(ref_lse).float())
+    tn = t.numpy()
+    onehot = np.zeros((M, N))
+    ok = (tn >= 0) & (tn < N)
+    onehot[np.arange(M)[ok], tn[ok]] = 1.0
+    scale = np.abs(to_f64(g))[:, None] * (np.exp(to_f64(x) - lse32[:, None]) + onehot)
+    check_scaled(to_f64(dx), ref, scale, dtype, f"xent bwd ex, extreme targets, ignore {ignore}")
+    got = dx.cpu()
+    assert torch.isnan(got[2]).all()
+    if ignore is None:
+        assert torch.isnan(got[[0, 5]]).all() and torch.isnan(loss.cpu()[[0, 2, 5]]).all()
+    else:
+        assert (got[[0, 5]] == 0).all() and (loss.cpu()[[0, 5]] == 0).all()
