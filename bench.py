@@ -9,9 +9,23 @@ every input once, write every output once) divided by the device time.
 
 Timing: W warm-up steps, then K steps between CUDA events on the launching
 stream, with a barrier and synchronize on both sides; the max over ranks is
-taken.  Input/output sets rotate over more than 4x the L2 size, so no step
-finds its data in L2.  SM clocks and throttle reasons are sampled with
-nvidia-smi during the timed region.
+taken.  The K steps are issued twice, in two timed regions: once as a CUDA
+graph of the K calls, replayed once (the headline: no host launch overhead
+between steps, as a launch-bound loop is issued in production), and once call
+by call from Python (reported beside it).  Inputs are larger than 4x the L2
+size, or input/output sets rotate over more than that, so no step finds its
+data in L2.  SM clocks and throttle reasons are sampled with nvidia-smi for
+the whole run; each entry reports the samples taken from its warm-up to the
+end of a 0.3 s hold of the same steps, untimed, right after its timed regions
+(a K-step region of tens of microseconds is shorter than the sampling period).
+
+With one GPU the line also carries, at the same K and W:
+  per_workload  the other named workloads (softmax 1024 x 4096 fp32,
+                cross-entropy 8192 x 131072 bf16, softmax 16384 x 131072 fp32)
+                and the backward / LayerNorm workloads, each with its roofline;
+  sweep         the M x N sweep (3 operators x fp32/bf16 x M x N), per
+                operator and dtype the min and median fraction of peak over
+                N >= 4096 and the worst point, and every point.
 
 Multi-GPU (torchrun, one rank per GPU): rows are independent, so each rank
 processes its own batch of the same shape (weak scaling, no collective on the
@@ -116,9 +130,11 @@ def recorded_traffic(workload: str, plan: dict):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    """nvidia-smi sampling of SM clock and throttle reasons while running.
+    Each sample carries nvidia-smi's own timestamp, so a summary can be taken
+    over the samples of one time window (host wall clock, time.time())."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -128,15 +144,20 @@ class ClockSampler:
         self.lines = []
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        cmd = ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        # line-buffered output through a pipe when stdbuf is there, so that
+        # every sample reaches the reader as it is taken
+        for prefix in (["stdbuf", "-oL"], []):
+            try:
+                self.proc = subprocess.Popen(prefix + cmd, stdout=subprocess.PIPE,
+                                             stderr=subprocess.DEVNULL, text=True)
+                break
+            except Exception:
+                self.proc = None
+        if self.proc is not None:
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
-        except Exception:
-            self.proc = None
         return self
 
     def _read(self):
@@ -152,12 +173,30 @@ class ClockSampler:
                 self.proc.kill()
             self._t.join(timeout=2)
 
-    def summary(self):
+    @staticmethod
+    def _stamp(field: str):
+        """Seconds since the epoch of an nvidia-smi timestamp (local time), or None."""
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(field.strip(), fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
+    def summary(self, t0: float | None = None, t1: float | None = None):
+        """Median SM clock, max clock, throttle reasons and sample count, over
+        every sample or over those stamped inside [t0, t1]."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
+            ts = self._stamp(parts[0]) if parts else None
+            if ts is not None:
+                parts = parts[1:]
             if len(parts) < 9:
+                continue
+            if t0 is not None and (ts is None or ts < t0 or ts > t1):
                 continue
             try:
                 sm.append(float(parts[1]))
@@ -466,8 +505,169 @@ def run_reference(args, op, dtype, M, N, sigma):
     print(json.dumps(line), flush=True)
 
 
+HOLD_S = 0.3  # untimed hold after each entry's timed regions, so that its clock record has samples
+ALL_WORKLOADS = {**syn.WORKLOADS, **syn.BWD_WORKLOADS, **syn.NEXT_WORKLOADS}
+
+
+def n_sets(set_bytes: int) -> int:
+    """Input/output sets to rotate over so that no step finds its data in L2:
+    one when a set alone is over 4x L2, else enough to pass 4x L2 together."""
+    return 1 if set_bytes >= 4 * L2_BYTES else max(2, math.ceil(4 * L2_BYTES / set_bytes))
+
+
+def kernels_per_step(op: str) -> int:
+    """Kernels of the library one call launches (RMSNorm backward: the ring
+    kernel, then the fixed-order sum of the dw partials)."""
+    return 2 if op == "rmsnorm_bwd" else 1
+
+
+def hold(qb, op, dtype, sets, M, N, stream, dev, seconds: float, per_launch_ms: float):
+    """Keeps issuing the same steps, untimed, for about `seconds`, in batches
+    of ~20 ms of GPU work so the queue stays short and the hold ends on time."""
+    batch = int(max(8, min(4096, 20.0 / max(per_launch_ms, 1e-3))))
+    t_end, i = time.time() + seconds, 0
+    while time.time() < t_end:
+        for _ in range(batch):
+            inp, out = sets[i % len(sets)]
+            launch(qb, op, dtype, inp, out, M, N, stream)
+            i += 1
+        torch.cuda.synchronize(dev)
+
+
+def time_entry(qb, op, dtype, M, N, sigma, K, W, dev, stream, seed=77, hold_s=HOLD_S,
+               modes=("graph", "stream")):
+    """W warm-up steps, then K steps timed once per launch mode, then an untimed
+    hold.  Returns ({mode: ms per step}, (start of the warm-up, end of the
+    hold), {"t0", "t1"} of the timed regions), the times from time.time()."""
+    sb = min_bytes(op, dtype, M, N)
+    sets = [make_set(op, dtype, M, N, sigma, seed + i, dev) for i in range(n_sets(sb))]
+    torch.cuda.synchronize(dev)
+    t_start = time.time()
+    for i in range(W):
+        launch(qb, op, dtype, *sets[i % len(sets)], M, N, stream)
+    torch.cuda.synchronize(dev)
+    ms = {}
+    t0 = time.time()
+    for mode in modes:
+        e0, e1 = timed_launches(qb, op, dtype, sets, M, N, K, stream, mode == "graph", dev)
+        torch.cuda.synchronize(dev)
+        ms[mode] = e0.elapsed_time(e1) / K
+    t1 = time.time()
+    if hold_s > 0:
+        hold(qb, op, dtype, sets, M, N, stream, dev, hold_s, min(ms.values()))
+    t_end = time.time()
+    st = qb.qk_get_device_status(stream)
+    if st != qb.QK_OK:
+        raise RuntimeError(f"device status after {op} {dtype} {M}x{N}: {qb.qk_status_string(st)}")
+    del sets
+    torch.cuda.empty_cache()
+    return ms, (t_start, t_end), {"t0": t0, "t1": t1}
+
+
+def tbs_of(op, dtype, M, N, ms: float) -> float:
+    return min_bytes(op, dtype, M, N) / (ms * 1e-3) / 1e12
+
+
+def roofline(op, dtype, M, N, ms, peak, peak_src, traffic=None) -> dict:
+    """The HBM roofline of one call: algorithmic bytes over its device time."""
+    b = min_bytes(op, dtype, M, N)
+    gbs = b / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+            "traffic": traffic, "peak_source": peak_src, "bytes_per_launch": b,
+            "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": gbs / NOMINAL_HBM_GBS}
+
+
+def workload_entry(qb, name, K, W, dev, stream, peak, peak_src) -> dict:
+    """One named workload at K steps: graph and call-by-call rates, roofline and
+    the launch plan; "clocks" holds the entry's time window until the sampler
+    has stopped (finish_clocks)."""
+    op, dtype, M, N, sigma = ALL_WORKLOADS[name]
+    ms, window, _ = time_entry(qb, op, dtype, M, N, sigma, K, W, dev, stream)
+    code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
+    plan = qb.qk_get_plan(OP_CODES[op], code, M, N)
+    g, s = ms["graph"], ms["stream"]
+    return {
+        "workload": name, "op": op, "dtype": dtype, "M": M, "N": N, "steps": K, "warmup": W,
+        "ms_per_step": g, "value": tbs_of(op, dtype, M, N, g), "unit": "TB/s", "launch": "cuda_graph",
+        "stream": {"ms_per_step": s, "value": tbs_of(op, dtype, M, N, s),
+                   "frac": tbs_of(op, dtype, M, N, s) * 1e3 / peak},
+        "roofline": roofline(op, dtype, M, N, g, peak, peak_src, recorded_traffic(name, plan)),
+        "gpu_launches": K * kernels_per_step(op), "clocks": window, "plan": plan,
+    }
+
+
+def finish_clocks(entries: list, sampler) -> None:
+    """Replaces each entry's time window by the clock summary of its samples."""
+    for e in entries:
+        t0, t1 = e["clocks"]
+        e["clocks"] = dict(sampler.summary(t0, t1), window="warm-up, both timed regions and a 0.3 s hold")
+
+
+def sweep_points(qb, ops, dtypes, Ms, Ns, K, W, dev, stream, peak) -> list:
+    """Every point of the M x N grid at K steps (graph and call by call); each
+    record keeps the times of its timed regions for finish_sweep_clocks."""
+    points = []
+    for op in ops:
+        for dtype in dtypes:
+            code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
+            for M in Ms:
+                for N in Ns:
+                    if N > qb.qk_max_row_elements(OP_CODES[op], code):
+                        continue  # longer rows than this operator takes
+                    ms, _, t = time_entry(qb, op, dtype, M, N, 1.0, K, W, dev, stream,
+                                          seed=2000 + N, hold_s=0.0)
+                    rec = {"op": op, "dtype": dtype, "M": M, "N": N, "steps": K,
+                           "TBps": tbs_of(op, dtype, M, N, ms["graph"]),
+                           "frac": tbs_of(op, dtype, M, N, ms["graph"]) * 1e3 / peak,
+                           "frac_stream": tbs_of(op, dtype, M, N, ms["stream"]) * 1e3 / peak,
+                           "ms": ms["graph"], "ms_stream": ms["stream"],
+                           "plan": qb.qk_get_plan(OP_CODES[op], code, M, N), **t}
+                    points.append(rec)
+    return points
+
+
+def finish_sweep_clocks(points: list, sampler, out=None) -> None:
+    """Each point's clock samples: those within 0.15 s of its timed regions."""
+    for p in points:
+        p["clocks"] = sampler.summary(p.pop("t0") - 0.15, p.pop("t1") + 0.15)
+        if out is not None:
+            out.write(json.dumps(p) + "\n")
+
+
+def sweep_summary(points: list, t_window, sampler) -> dict:
+    """Per operator and dtype: min and median fraction of peak over N >= 4096,
+    and the worst point; every point as [op, dtype, M, N, frac, frac call by
+    call, median SM MHz of its samples]."""
+    groups = {}
+    for p in points:
+        groups.setdefault(f"{p['op']}_{p['dtype']}", []).append(p)
+    per = {}
+    for key, ps in groups.items():
+        ge = [p for p in ps if p["N"] >= 4096] or ps
+        worst = min(ge, key=lambda p: p["frac"])
+        per[key] = {"points": len(ps), "points_N_ge_4096": len(ge),
+                    "min_frac_N_ge_4096": worst["frac"],
+                    "median_frac_N_ge_4096": statistics.median(p["frac"] for p in ge),
+                    "min_frac_stream_N_ge_4096": min(p["frac_stream"] for p in ge),
+                    "median_frac_stream_N_ge_4096": statistics.median(p["frac_stream"] for p in ge),
+                    "worst": {"M": worst["M"], "N": worst["N"], "frac": worst["frac"],
+                              "TBps": worst["TBps"]}}
+    ge_all = [p for p in points if p["N"] >= 4096]
+    return {
+        "grid": {"M": sorted({p["M"] for p in points}), "N": sorted({p["N"] for p in points}),
+                 "ops": sorted({p["op"] for p in points}), "dtypes": sorted({p["dtype"] for p in points})},
+        "launch": "cuda_graph (frac) and call by call (frac_stream)",
+        "per_kernel": per,
+        "points_N_ge_4096_at_or_above_0.85": sum(p["frac"] >= 0.85 for p in ge_all),
+        "points_N_ge_4096": len(ge_all),
+        "clocks": sampler.summary(*t_window),
+        "points": [[p["op"], p["dtype"], p["M"], p["N"], round(p["frac"], 4), round(p["frac_stream"], 4),
+                    p["clocks"]["sm_mhz"]] for p in points],
+    }
+
+
 def run_sweep(args, path):
-    """Every point of the M x N sweep grid (3 operators x fp32/bf16 x M x N),
+    """Every point of the M x N sweep grid (--sweep-ops x fp32/bf16 x M x N),
     timed with the library's default plan, one JSON line per point into
     `path`; the summary line goes to stdout."""
     from memory_bound_row_rmsnorm_gb300 import binding as qb
@@ -480,53 +680,25 @@ def run_sweep(args, path):
     peak, peak_src = measured_peak()
     sweep_m = [int(v) for v in args.sweep_m.split(",")] if args.sweep_m else list(syn.SWEEP_M)
     sweep_n = [int(v) for v in args.sweep_n.split(",")] if args.sweep_n else list(syn.SWEEP_N)
-    points = []
+    with ClockSampler(0) as sampler:
+        t0 = time.time()
+        points = sweep_points(qb, args.sweep_ops.split(","), ("f32", "bf16"), sweep_m, sweep_n,
+                              args.steps, args.warmup, dev, stream, peak)
+        t1 = time.time()
+        time.sleep(0.3)  # let the sampler's last lines arrive
     with open(path, "w") as fout:
-        for op in args.sweep_ops.split(","):
-            for dtype in ("f32", "bf16"):
-                for M in sweep_m:
-                    for N in sweep_n:
-                        code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
-                        if N > qb.qk_max_row_elements(OP_CODES[op], code):
-                            continue  # longer rows than this operator takes
-                        sb = min_bytes(op, dtype, M, N)
-                        nsets = max(2, math.ceil(4 * L2_BYTES / sb))
-                        sets = [make_set(op, dtype, M, N, 1.0, 77 + i, dev) for i in range(nsets)]
-                        K = int(max(5, min(args.steps, 8e9 / sb)))
-                        for i in range(max(3, min(args.warmup, 20))):
-                            launch(qb, op, dtype, *sets[i % nsets], M, N, stream)
-                        torch.cuda.synchronize(dev)
-                        e0, e1 = timed_launches(qb, op, dtype, sets, M, N, K, stream, args.graph, dev)
-                        torch.cuda.synchronize(dev)
-                        if qb.qk_get_device_status(stream) != qb.QK_OK:
-                            raise RuntimeError("device status reports a failure")
-                        ms = e0.elapsed_time(e1) / K
-                        tbs = sb / (ms * 1e-3) / 1e12
-                        code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
-                        opc = OP_CODES[op]
-                        rec = {"op": op, "dtype": dtype, "M": M, "N": N, "TBps": tbs,
-                               "frac": tbs * 1e3 / peak, "frac_of_nominal": tbs * 1e3 / NOMINAL_HBM_GBS,
-                               "ms": ms, "steps": K,
-                               "launch": "cuda_graph" if args.graph else "stream",
-                               "plan": qb.qk_get_plan(opc, code, M, N)}
-                        fout.write(json.dumps(rec) + "\n")
-                        fout.flush()
-                        points.append(rec)
-                        del sets
-                        torch.cuda.empty_cache()
-    ge = [p for p in points if p["N"] >= 4096] or points
-    print(json.dumps({"sweep": path, "points": len(points), "peak_gbs": peak, "peak_source": peak_src,
-                      "min_frac_N_ge_4096": min(p["frac"] for p in ge),
-                      "median_frac_N_ge_4096": statistics.median(p["frac"] for p in ge)}))
+        finish_sweep_clocks(points, sampler, fout)
+    summ = sweep_summary(points, (t0, t1), sampler)
+    summ.pop("points")
+    print(json.dumps({"sweep": path, "peak_gbs": peak, "peak_source": peak_src, **summ}))
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(syn.WORKLOADS) + sorted(syn.BWD_WORKLOADS) + sorted(syn.NEXT_WORKLOADS))
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(ALL_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -534,17 +706,17 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: total CPU time budget of the timed steps")
     ap.add_argument("--sweep-ops", default="softmax,rmsnorm,xent",
-                    help="operators of --sweep (also softmax_bwd, rmsnorm_bwd, xent_bwd, layernorm)")
-    ap.add_argument("--sweep-m", help="comma-separated row counts of --sweep (default: the sweep grid)")
-    ap.add_argument("--sweep-n", help="comma-separated row lengths of --sweep (default: the sweep grid)")
-    ap.add_argument("--graph", action="store_true",
-                    help="issue the timed steps as one CUDA-graph replay (no host launch overhead)")
+                    help="operators of the sweep (also softmax_bwd, rmsnorm_bwd, xent_bwd, layernorm)")
+    ap.add_argument("--sweep-m", help="comma-separated row counts of the sweep (default: the sweep grid)")
+    ap.add_argument("--sweep-n", help="comma-separated row lengths of the sweep (default: the sweep grid)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the per-workload block and the sweep summary of the default line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.sweep:
         run_sweep(args, args.sweep)
         return
-    op, dtype, M, N, sigma = {**syn.WORKLOADS, **syn.BWD_WORKLOADS, **syn.NEXT_WORKLOADS}[args.workload]
+    op, dtype, M, N, sigma = ALL_WORKLOADS[args.workload]
 
     if args.impl == "reference":
         run_reference(args, op, dtype, M, N, sigma)
@@ -566,16 +738,19 @@ def main():
     if ws > 1:
         dist.barrier()
     qb.load_library()
+    peak, peak_src = measured_peak()
+    sampler = ClockSampler(local).__enter__()
 
     # rotating input/output sets: > 4x L2 in total
     set_bytes = min_bytes(op, dtype, M, N)
-    nsets = max(2, math.ceil(4 * L2_BYTES / set_bytes))
+    nsets = n_sets(set_bytes)
     sets = [make_set(op, dtype, M, N, sigma, rank_seed(rank, i), dev) for i in range(nsets)]
     stream = torch.cuda.current_stream(dev)
     code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
-    opcode = OP_CODES[op]
-    plan = qb.qk_get_plan(opcode, code, M, N)
+    plan = qb.qk_get_plan(OP_CODES[op], code, M, N)
+    torch.cuda.synchronize(dev)
 
+    t_start = time.time()
     for i in range(args.warmup):
         inp, out = sets[i % nsets]
         launch(qb, op, dtype, inp, out, M, N, stream)
@@ -584,39 +759,62 @@ def main():
         raise RuntimeError("device status reports a failure after warm-up")
 
     K = args.steps
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clocks:
-        start, stop = timed_launches(qb, op, dtype, sets, M, N, K, stream, args.graph, dev)
+    elapsed = {}
+    for mode in ("graph", "stream"):  # the same K steps, as one graph replay, then call by call
+        if ws > 1:
+            dist.barrier()
         torch.cuda.synchronize(dev)
-    if ws > 1:
-        dist.barrier()
-    elapsed_ms = start.elapsed_time(stop)
-    if ws > 1:
-        elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
+        start, stop = timed_launches(qb, op, dtype, sets, M, N, K, stream, mode == "graph", dev)
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            dist.barrier()
+        ms = start.elapsed_time(stop)
+        elapsed[mode] = max_over_ranks(ms, dist, dev) if ws > 1 else ms
+    hold(qb, op, dtype, sets, M, N, stream, dev, HOLD_S, elapsed["graph"] / K)
+    t_end = time.time()
     status = qb.qk_get_device_status(stream)
     if status != qb.QK_OK:
         raise RuntimeError(f"device status: {qb.qk_status_string(status)}")
 
-    per_launch_s = elapsed_ms / 1e3 / K
-    bytes_per_launch = set_bytes
-    value = whole_job_tbs(bytes_per_launch, ws, K, elapsed_ms)
-    peak, peak_src = measured_peak()
-    achieved_gbs = bytes_per_launch / per_launch_s / 1e9
-    traffic = recorded_traffic(args.workload, plan)
+    elapsed_ms = elapsed["graph"]
+    value = whole_job_tbs(set_bytes, ws, K, elapsed_ms)
+    stream_value = whole_job_tbs(set_bytes, ws, K, elapsed["stream"])
+    line_roofline = roofline(op, dtype, M, N, elapsed_ms / K, peak, peak_src,
+                             recorded_traffic(args.workload, plan))
 
     # ---- end to end: pinned host buffers, copies inside the timed region ----
-    e2e_ms, E, h2d, d2h = e2e_pipelined(qb, op, dtype, sets[:2], M, N, max(3, args.e2e_steps), dev)
+    e2e_sets = sets[:2] if nsets >= 2 else sets + [make_set(op, dtype, M, N, sigma, rank_seed(rank, 1), dev)]
+    e2e_ms, E, h2d, d2h = e2e_pipelined(qb, op, dtype, e2e_sets, M, N, max(3, args.e2e_steps), dev)
     if ws > 1:
         e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e_value = whole_job_tbs(set_bytes, ws, E, e2e_ms)
+    del sets, e2e_sets
+    torch.cuda.empty_cache()
 
     if rank != 0:
+        sampler.__exit__(None, None, None)
         if ws > 1:
             dist.barrier()
             dist.destroy_process_group()
         return
+
+    per_workload, points, sweep_window = None, None, None
+    if ws == 1 and not args.no_extras:
+        per_workload = [workload_entry(qb, name, K, args.warmup, dev, stream, peak, peak_src)
+                        for name in list(syn.WORKLOADS) + list(syn.BWD_WORKLOADS) + list(syn.NEXT_WORKLOADS)
+                        if name != args.workload]
+        t0 = time.time()
+        points = sweep_points(qb, ("softmax", "rmsnorm", "xent"), ("f32", "bf16"), syn.SWEEP_M, syn.SWEEP_N,
+                              K, args.warmup, dev, stream, peak)
+        sweep_window = (t0, time.time())
+    time.sleep(0.3)  # let the sampler's last lines arrive
+    sampler.__exit__(None, None, None)
+    clocks = sampler.summary(t_start, t_end)
+    sweep = None
+    if per_workload is not None:
+        finish_clocks(per_workload, sampler)
+        finish_sweep_clocks(points, sampler)
+        sweep = sweep_summary(points, sweep_window, sampler)
 
     cpu = None
     if ws == 1 and args.cpu_seconds > 0:
@@ -639,20 +837,24 @@ def main():
         "dtype": "f32" if dtype == "f32" else "bf16 in/out, f32 accumulate",
         "data": "synthetic",
         "config": {"workload": args.workload, "op": op, "M": M, "N": N, "input_dtype": dtype,
-                   "rows_per_gpu": M, "launch": "cuda_graph" if args.graph else "stream",
-                   "l2": f"{nsets} rotating input/output sets "
+                   "rows_per_gpu": M, "launch": "cuda_graph: the K calls captured once, replayed once",
+                   "l2": f"{nsets} rotating input/output set(s) "
                    f"({nsets * set_bytes / 2**20:.0f} MiB) > 4x L2", "plan": plan},
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": achieved_gbs / peak, "traffic": traffic, "peak_source": peak_src,
-                     "bytes_per_launch": bytes_per_launch, "nominal_peak": NOMINAL_HBM_GBS,
-                     "frac_of_nominal": achieved_gbs / NOMINAL_HBM_GBS},
+        "stream": {"value": stream_value, "unit": "TB/s", "ms_per_step": elapsed["stream"] / K,
+                   "frac": stream_value * 1e3 / ws / peak,
+                   "how": "the same K steps issued call by call from Python, in their own timed region"},
+        "roofline": line_roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": E,
                 "how": "pinned host buffers; copy-in, call, copy-out every step, pipelined over 3 streams"},
-        "gpu_launches": K,
-        "clocks": clocks.summary(),
+        "gpu_launches": K * kernels_per_step(op),
+        "clocks": dict(clocks, window="warm-up, both timed regions and a 0.3 s hold of the same steps"),
     }
+    if per_workload is not None:
+        line["per_workload"] = per_workload
+    if sweep is not None:
+        line["sweep"] = sweep
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
