@@ -316,7 +316,8 @@ QK_API int64_t qk_max_row_elements(qk_op op, qk_dtype dtype);
  *
  *   path            1 = TMA ring (aligned fast path), 2 = masked direct path,
  *                   3 = backward ring, 4 = two-pass ring (rows beyond 1 MiB;
- *                   an override with path 4 forces it for any row).
+ *                   an override with path 4 forces it for any row),
+ *                   5 = masked backward, 6 = shifted ring (unaligned rows).
  *   threads         threads per CTA.
  *   row_threads     threads that share one row inside a CTA (rows per CTA
  *                   step = threads / row_threads).

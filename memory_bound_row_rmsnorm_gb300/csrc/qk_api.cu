@@ -264,9 +264,20 @@ const Choice kSoftmaxTable[] = {
     {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 16, 4, 2},  {32768, 256, 256, 16, 8, 1},  {65536, 256, 256, 16, 16, 1},
 };
+// bf16 softmax: rows of 8192 elements (1024 vectors) in 128-thread CTAs of
+// 8 vectors a thread, which keep four CTAs per SM where 256 x 4 keeps three
+// (85-98 % of peak against 80-90 % at 2048-32768 rows).
+const Choice kSoftmaxBf16Table[] = {
+    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 3},       {128, 256, 32, 4, 1, 3},
+    {256, 256, 64, 4, 1, 2},     {512, 128, 128, 4, 1, 1},     {1024, 128, 128, 8, 1, 1},
+    {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {16384, 256, 256, 16, 4, 2},  {32768, 256, 256, 16, 8, 1},  {65536, 256, 256, 16, 16, 1},
+};
+// Cross-entropy rows of 1024 vectors stream from two slots (fp32 4096 and
+// bf16 8192 elements: +3 to +10 points over one slot at 4096-32768 rows).
 const Choice kXentTable[] = {
     {32, 256, 8, 4, 1, 1},       {64, 256, 8, 8, 1, 2},        {128, 256, 16, 8, 1, 2},
-    {256, 256, 32, 8, 1, 2},     {512, 256, 64, 8, 1, 2},      {1024, 128, 128, 8, 1, 1},
+    {256, 256, 32, 8, 1, 2},     {512, 256, 64, 8, 1, 2},      {1024, 128, 128, 8, 1, 2},
     {2048, 256, 256, 8, 1, 2},   {kStream, 256, 256, 4, 1, 2},  // 16 KB chunks
 };
 
@@ -291,13 +302,19 @@ const Choice kXentBwdTable[] = {
 };
 
 // Chooses the ring kernel (fast path) for a row of NV 16-byte vectors.
-qk_status choose_ring(int op, int64_t NV, int* th, int* tpr, int* vpt, int* cl, int* k,
+qk_status choose_ring(int op, int dt, int64_t NV, int* th, int* tpr, int* vpt, int* cl, int* k,
                       int* slots) {
 #define QK_TABLE(T) t = T, n = int(sizeof(T) / sizeof(Choice))
   const Choice* t;
   int n;
   switch (op) {
-    case kSoftmax: QK_TABLE(kSoftmaxTable); break;
+    case kSoftmax:
+      if (dt == QK_BF16) {
+        QK_TABLE(kSoftmaxBf16Table);
+      } else {
+        QK_TABLE(kSoftmaxTable);
+      }
+      break;
     case kRmsNorm: QK_TABLE(kRmsNormTable); break;
     case kXent: QK_TABLE(kXentTable); break;
     case kOpSoftmaxBwd: QK_TABLE(kSoftmaxBwdTable); break;
@@ -326,7 +343,35 @@ bool wants_two_pass(int op, int64_t NV) {
          NV > int64_t(kMaxCluster) * kRingMaxVectorsPerCta;
 }
 
-qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p) {
+// Short launches: items per resident CTA below which the planner raises a
+// one-row-per-slot launch to 3 ring slots (t3) or 2 (t2), when that costs no
+// resident CTA.  From sweeps of 1-3 slots over 1024-32768 rows and rows of
+// 256-16384 elements: a launch of few items per CTA waits mostly on its
+// first loads, one of many items streams best from the table's slots.
+struct SlotBands {
+  int t3, t2;
+};
+SlotBands slot_bands(int op) {
+  if (op == kRmsNorm || op == kOpLayerNorm) return {8, 0};
+  if (op == kSoftmax) return {4, 8};
+  return {4, 0};
+}
+
+// Alternative kernel for short launches (fewer than 8 items per resident CTA
+// of the table's plan): fp32 softmax rows of 4096 elements in 128-thread CTAs
+// of 8 vectors a thread, with 3 ring slots below 4 items per CTA and 2 above
+// (1024 x 4096: 86 % -> 88 %; 4096 x 4096: 90 % -> 92 %); the 256 x 4 plan
+// beats it by 1-2 points from 8192 rows on.
+bool short_alternative(int op, int dt, int64_t NV, bool very_short, Choice* c) {
+  if (op == kSoftmax && dt == QK_F32 && NV > 512 && NV <= 1024) {
+    *c = Choice{1024, 128, 128, 8, 1, very_short ? 3 : 2};
+    return true;
+  }
+  return false;
+}
+
+qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int64_t N, Plan* p,
+                    const Choice* alt = nullptr) {
   const int E = 16 / elem_size(dt);
   const int64_t NV = N / E;
   int th, tpr, vpt, cl, k;
@@ -363,8 +408,11 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
     } else {
       return QK_ERR_UNSUPPORTED;
     }
+  } else if (alt != nullptr) {
+    th = alt->threads, tpr = alt->row_threads, vpt = alt->vec_per_thread;
+    cl = alt->cluster, slots = alt->slots, k = 1;
   } else {
-    qk_status st = choose_ring(op, NV, &th, &tpr, &vpt, &cl, &k, &slots);
+    qk_status st = choose_ring(op, dt, NV, &th, &tpr, &vpt, &cl, &k, &slots);
     if (st != QK_OK) return st;
   }
   const KernelEntry* ke =
@@ -408,19 +456,36 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   st = occupancy(dev, *ke, int(smem), cl > 1 ? cl : 0, &occ);
   if (st != QK_OK) return st;
   if (occ <= 0) return QK_ERR_UNSUPPORTED;
+  // CTAs per SM the launch can hold (clusters: resident clusters' CTAs over the SMs)
+  const int64_t ctas_per_sm = cl > 1 ? std::max<int64_t>(1, int64_t(occ) * cl / std::max(1, d.sms)) : occ;
 
-  // Short launches (fewer than four items for each resident CTA) spend most
-  // of their time waiting for their first loads: give each CTA a ring of
-  // three slots, if that costs no resident CTA.  (Softmax fp32 1024 x 4096:
-  // 70 % -> 75 %; 2048 x 4096: 76 % -> 97 %.)
+  // Short launches spend most of their time waiting for their first loads:
+  // below the operator's bands of items per resident CTA, give each CTA a
+  // ring of three (or two) slots, if that costs no resident CTA.  (Softmax
+  // fp32 1024 x 4096: 70 % -> 75 %; 2048 x 4096: 76 % -> 97 %; RMSNorm bf16
+  // 16384 x 1024: 90 % -> 98 %.)
+  const bool short_ok = !ov.on && !two_pass && k == 1 && cl == 1;
+  const int64_t resident = ctas_per_sm * d.sms;
+  if (short_ok && alt == nullptr && p->num_items < 8 * resident) {
+    Choice c;
+    if (short_alternative(op, dt, NV, p->num_items < 4 * resident, &c) &&
+        !(c.threads == th && c.row_threads == tpr && c.vec_per_thread == vpt))
+      return plan_ring(dev, d, op, dt, M, N, p, &c);  // its slots as given
+  }
   int64_t smem_used = smem;
-  if (!ov.on && !two_pass && k == 1 && cl == 1 && slots < 3 &&
-      p->num_items < 4 * int64_t(occ) * d.sms) {
-    const int64_t smem3 = kSmemHeader + 3 * int64_t(nin) * slot_bytes + param_bytes;
-    int occ3 = 0;
-    if (smem3 <= d.smem_optin && occupancy(dev, *ke, int(smem3), 0, &occ3) == QK_OK && occ3 >= occ) {
-      slots = 3;
-      smem_used = smem3;
+  const SlotBands band = slot_bands(op);
+  const int want = !short_ok || alt != nullptr               ? 0
+                   : p->num_items < band.t3 * resident ? 3
+                   : p->num_items < band.t2 * resident ? 2
+                                                       : 0;
+  for (int s = want; s > slots; --s) {
+    const int64_t smem_s = kSmemHeader + int64_t(s) * nin * slot_bytes + param_bytes;
+    int occ_s = 0;
+    if (smem_s <= d.smem_optin && occupancy(dev, *ke, int(smem_s), 0, &occ_s) == QK_OK &&
+        occ_s >= occ) {
+      slots = s;
+      smem_used = smem_s;
+      break;
     }
   }
 
@@ -434,7 +499,7 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   int64_t units = cl > 1 ? int64_t(occ) : int64_t(occ) * d.sms;
   if (ov.on && ov.plan.grid > 0) units = std::min<int64_t>(units, std::max(1, ov.plan.grid / cl));
   units = std::min<int64_t>(units, p->num_items);
-  p->ctas_per_sm = cl > 1 ? std::max(1, occ * cl / std::max(1, d.sms)) : occ;
+  p->ctas_per_sm = int(ctas_per_sm);
   p->grid = units * cl;
   return QK_OK;
 }
@@ -769,7 +834,7 @@ qk_status run_bwd(int op, int dt, BwdArgs a, float* dw, size_t workspace_bytes, 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(unsigned((a.N + 31) / 32), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(kDwReduceThreads, 1, 1);
   cfg.stream = static_cast<cudaStream_t>(stream);
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -601,27 +601,47 @@ __global__ void __launch_bounds__(THREADS) bwd_direct_kernel(const BwdArgs a) {
 }
 
 // dw[j] = sum over the partial rows p of partial[p][j], in a fixed order:
-// 32 columns per CTA (one per lane), 8 warps each summing every 8th row,
-// then the 8 warp sums in index order.
+// 32 columns per CTA (one per lane, a 128-byte line per warp and row), 32
+// warps each summing every 32nd row in row order, then the 32 warp sums in
+// index order.  The partial rows were just written by the ring kernel and sit
+// in L2; what bounds this kernel is how many of those lines are in flight, so
+// each warp issues the loads of up to 16 of its rows before it adds them (a
+// few hundred partial rows: every load of a warp in one round trip).  The sum
+// keeps the plain row order: the same bits as a one-row-at-a-time loop.
 // (A template so that every translation unit may include this header.)
+constexpr int kDwReduceThreads = 1024;
 template <int kUnused = 0>
-__global__ void __launch_bounds__(256) dw_reduce_kernel(const float* __restrict__ partial,
-                                                        float* __restrict__ dw, int64_t rows,
-                                                        int64_t N) {
-  __shared__ float part[8][33];
+__global__ void __launch_bounds__(kDwReduceThreads) dw_reduce_kernel(const float* __restrict__ partial,
+                                                                     float* __restrict__ dw, int64_t rows,
+                                                                     int64_t N) {
+  constexpr int NW = kDwReduceThreads / 32;
+  __shared__ float part[NW][33];
   grid_dependency_wait();
   allow_dependent_launch();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t col = int64_t(blockIdx.x) * 32 + lane;
   float acc = 0.f;
-  if (col < N)
-    for (int64_t r = warp; r < rows; r += 8) acc += partial[r * N + col];
+  if (col < N) {
+    constexpr int kDepth = 16;  // rows of one warp whose loads are in flight together
+    const float* p = partial + col;
+    for (int64_t base = warp; base < rows; base += int64_t(kDepth) * NW) {
+      float v[kDepth];
+#pragma unroll
+      for (int u = 0; u < kDepth; ++u) {
+        const int64_t r = base + int64_t(u) * NW;
+        v[u] = r < rows ? __ldcg(p + r * N) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kDepth; ++u)
+        if (base + int64_t(u) * NW < rows) acc += v[u];
+    }
+  }
   part[warp][lane] = acc;
   __syncthreads();
   if (warp == 0 && col < N) {
     float s = part[0][lane];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) s += part[w][lane];
+    for (int w = 1; w < NW; ++w) s += part[w][lane];
     dw[col] = s;
   }
 }

@@ -60,7 +60,8 @@ constexpr int kMaxCluster = 16;
 // One compiled kernel.  `path` 1: TMA ring kernel (threads, row_threads,
 // vec_per_thread); path 2: masked direct kernel (threads, elems_per_thread);
 // path 3: backward ring kernel (as path 1); path 4: two-pass ring kernel for
-// rows longer than a cluster holds (as path 1).
+// rows longer than a cluster holds (as path 1); path 5: masked backward
+// kernel; path 6: shifted ring kernel (unaligned rows).
 struct KernelEntry {
   int path;
   int threads;
