@@ -12,9 +12,11 @@ stream, with a barrier and synchronize on both sides; the max over ranks is
 taken.  The K steps are issued twice, in two timed regions: once as a CUDA
 graph of the K calls, replayed once (the headline: no host launch overhead
 between steps, as a launch-bound loop is issued in production), and once call
-by call from Python (reported beside it).  Before each start event a spin
+by call from Python (reported beside it).  Before each timed region a spin
 kernel holds the stream for ~0.5 ms, so that the calls are enqueued before
-the GPU reaches the start event and the events measure device time only.  Inputs are larger than 4x the L2
+the GPU reaches the start event; in the graph the two events are nodes
+recorded right before the first call and after the last, so the events
+measure device time only.  Inputs are larger than 4x the L2
 size, or input/output sets rotate over more than that, so no step finds its
 data in L2.  SM clocks and throttle reasons are sampled with nvidia-smi for
 the whole run; each entry reports the samples taken from its warm-up to the
@@ -299,8 +301,11 @@ def timed_launches(qb, op, dtype, sets, M, N, K, stream, graph: bool, dev):
     """Enqueues K steps (rotating over `sets`) between two CUDA events on
     `stream` and returns (start, stop).  With graph=True the K calls are first
     captured into one CUDA graph (the library's launches, recorded once) and
-    the graph is replayed, which removes host launch overhead between steps.
-    Either way a head start (head_start) precedes the start event."""
+    the graph is replayed, which removes host launch overhead between steps;
+    the two events are then nodes of the graph itself, recorded right before
+    the first call and right after the last, so that the graph's own launch
+    is not counted.  Either way a head start (head_start) precedes the
+    timed region."""
     nsets = len(sets)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if not graph:
@@ -311,18 +316,20 @@ def timed_launches(qb, op, dtype, sets, M, N, K, stream, graph: bool, dev):
             launch(qb, op, dtype, inp, out, M, N, stream)
         stop.record(stream)
         return start, stop
+    start = torch.cuda.Event(enable_timing=True, external=True)
+    stop = torch.cuda.Event(enable_timing=True, external=True)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         cs = torch.cuda.current_stream(dev)
+        start.record(cs)
         for i in range(K):
             inp, out = sets[i % nsets]
             launch(qb, op, dtype, inp, out, M, N, cs)
+        stop.record(cs)
     g.replay()  # first replay uploads the graph
     torch.cuda.synchronize(dev)
     head_start(stream)
-    start.record(stream)
     g.replay()
-    stop.record(stream)
     timed_launches.keep = g  # the graph must outlive the replay
     return start, stop
 
@@ -728,12 +735,19 @@ def main():
     ap.add_argument("--sweep-n", help="comma-separated row lengths of the sweep (default: the sweep grid)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload block and the sweep summary of the default line")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="run the workload with this many rows instead of its own M (small cases for "
+                         "multi-metric profiler captures); the line then names the reduced shape")
+    ap.add_argument("--hold", type=float, default=HOLD_S,
+                    help="seconds of untimed steps after the timed regions (clock samples)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.sweep:
         run_sweep(args, args.sweep)
         return
     op, dtype, M, N, sigma = ALL_WORKLOADS[args.workload]
+    if args.rows > 0:
+        M = args.rows
 
     if args.impl == "reference":
         run_reference(args, op, dtype, M, N, sigma)
@@ -787,7 +801,8 @@ def main():
             dist.barrier()
         ms = start.elapsed_time(stop)
         elapsed[mode] = max_over_ranks(ms, dist, dev) if ws > 1 else ms
-    hold(qb, op, dtype, sets, M, N, stream, dev, HOLD_S, elapsed["graph"] / K)
+    if args.hold > 0:
+        hold(qb, op, dtype, sets, M, N, stream, dev, args.hold, elapsed["graph"] / K)
     t_end = time.time()
     status = qb.qk_get_device_status(stream)
     if status != qb.QK_OK:
@@ -797,7 +812,7 @@ def main():
     value = whole_job_tbs(set_bytes, ws, K, elapsed_ms)
     stream_value = whole_job_tbs(set_bytes, ws, K, elapsed["stream"])
     line_roofline = roofline(op, dtype, M, N, elapsed_ms / K, peak, peak_src,
-                             recorded_traffic(args.workload, plan))
+                             recorded_traffic(args.workload, plan) if args.rows <= 0 else None)
 
     # ---- end to end: pinned host buffers, copies inside the timed region ----
     e2e_sets = sets[:2] if nsets >= 2 else sets + [make_set(op, dtype, M, N, sigma, rank_seed(rank, 1), dev)]
@@ -853,8 +868,8 @@ def main():
         "vs_baseline": None,
         "dtype": "f32" if dtype == "f32" else "bf16 in/out, f32 accumulate",
         "data": "synthetic",
-        "config": {"workload": args.workload, "op": op, "M": M, "N": N, "input_dtype": dtype,
-                   "rows_per_gpu": M, "launch": "cuda_graph: the K calls captured once, replayed once",
+        "config": {"workload": args.workload if args.rows <= 0 else f"{args.workload} at {M} rows",
+                   "op": op, "M": M, "N": N, "input_dtype": dtype, "rows_per_gpu": M, "launch": "cuda_graph: the K calls captured once, replayed once",
                    "l2": f"{nsets} rotating input/output set(s) "
                    f"({nsets * set_bytes / 2**20:.0f} MiB) > 4x L2", "plan": plan},
         "stream": {"value": stream_value, "unit": "TB/s", "ms_per_step": elapsed["stream"] / K,

@@ -181,6 +181,39 @@ def test_xent_backward_bad_targets_and_default_dloss(dtype):
     assert torch.isnan(dx[[0, 1, 4, 6, 7]]).all() and torch.isfinite(dx[[2, 3, 5]]).all()
 
 
+@pytest.mark.parametrize("dtype,M,N", [("bf16", 4096, 4096), ("f32", 300, 16384), ("bf16", 2000, 1024)])
+def test_rmsnorm_backward_graph_replays(dtype, M, N):
+    """RMSNorm backward (the ring kernel and the fixed-order dw sum) captured
+    into a CUDA graph and replayed with new data copied into the same buffers
+    before each replay: every replay gives the oracle's dx and dw.  The
+    workspace starts as random bytes (it is scratch)."""
+    code = DT[dtype]
+    cases = [make_case("rmsnorm", dtype, M, N, seed=9150 + i) for i in range(3)]
+    d = {k: v.to(DEV) for k, v in cases[0].items()}
+    dx = torch.empty_like(d["x"])
+    dw = torch.empty((N,), dtype=torch.float32, device=DEV)
+    nbytes = qb.qk_rmsnorm_bwd_workspace_size(M, N, code)
+    ws = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # one eager call first: plan, attributes, occupancy
+        qb.qk_rmsnorm_bwd(d["x"], d["w"], d["rstd"], d["dy"], dx, dw, ws, nbytes, M, N, code, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        qb.qk_rmsnorm_bwd(d["x"], d["w"], d["rstd"], d["dy"], dx, dw, ws, nbytes, M, N, code,
+                          torch.cuda.current_stream())
+    for i, case in enumerate(cases):
+        for k in d:
+            d[k].copy_(case[k].to(DEV))
+        dx.fill_(float("nan"))
+        dw.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert qb.qk_get_device_status() == qb.QK_OK
+        check("rmsnorm", dtype, case, {"dx": dx, "dw": dw}, f"graph replay {i}")
+
+
 def test_rmsnorm_backward_is_deterministic():
     case = make_case("rmsnorm", "bf16", 4096, 4096, seed=9000)
     a = run_gpu("rmsnorm", "bf16", case)
