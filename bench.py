@@ -93,7 +93,8 @@ def min_bytes(op: str, dtype: str, M: int, N: int) -> int:
 
 
 # The device code of the kernels (the launch plan is compared separately).
-KERNEL_SOURCES = ("qk_device.cuh", "qk_kernels.cuh", "qk_kernel_table.cuh", "qk_internal.h")
+KERNEL_SOURCES = ("qk_device.cuh", "qk_kernels.cuh", "qk_kernel_table.cuh", "qk_internal.h",
+                  "qk_bwd_kernels.cuh", "qk_bwd_table.cuh")
 
 
 def kernel_source_hash() -> str:
