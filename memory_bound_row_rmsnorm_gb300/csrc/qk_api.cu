@@ -275,9 +275,12 @@ const Choice kSoftmaxBf16Table[] = {
 };
 // Cross-entropy rows of 1024 vectors stream from two slots (fp32 4096 and
 // bf16 8192 elements: +3 to +10 points over one slot at 4096-32768 rows).
+// Rows of 512 vectors (bf16 4096, fp32 2048 elements) take one warp a row,
+// 16 vectors a lane, in 128-thread CTAs: bf16 16384 x 4096 90 % -> 100 %,
+// 32768 x 4096 97 % -> 103 %; fp32 8192 x 2048 89 % -> 93 %.
 const Choice kXentTable[] = {
     {32, 256, 8, 4, 1, 1},       {64, 256, 8, 8, 1, 2},        {128, 256, 16, 8, 1, 2},
-    {256, 256, 32, 8, 1, 2},     {512, 256, 64, 8, 1, 2},      {1024, 128, 128, 8, 1, 2},
+    {256, 256, 32, 8, 1, 2},     {512, 128, 32, 16, 1, 2},     {1024, 128, 128, 8, 1, 2},
     {2048, 256, 256, 8, 1, 2},   {kStream, 256, 256, 4, 1, 2},  // 16 KB chunks
 };
 
@@ -357,14 +360,23 @@ SlotBands slot_bands(int op) {
   return {4, 0};
 }
 
-// Alternative kernel for short launches (fewer than 8 items per resident CTA
-// of the table's plan): fp32 softmax rows of 4096 elements in 128-thread CTAs
-// of 8 vectors a thread, with 3 ring slots below 4 items per CTA and 2 above
-// (1024 x 4096: 86 % -> 88 %; 4096 x 4096: 90 % -> 92 %); the 256 x 4 plan
-// beats it by 1-2 points from 8192 rows on.
+// Alternative kernels for short launches (fewer than 8 items per resident CTA
+// of the table's plan):
+//  * fp32 softmax rows of 4096 elements in 128-thread CTAs of 8 vectors a
+//    thread, with 3 ring slots below 4 items per CTA and 2 above (1024 x 4096:
+//    86 % -> 88 %; 4096 x 4096: 90 % -> 92 %); the 256 x 4 plan beats it by
+//    1-2 points from 8192 rows on;
+//  * cross-entropy rows of 512 vectors below 4 items per CTA: two 64-thread
+//    rows of 8 vectors a thread per 128-thread CTA, six CTAs per SM (bf16
+//    2048 x 4096: 36 % -> 53 %, 4096 x 4096 64 % -> 68 %; fp32 2048 x 2048
+//    40 % -> 56 %).
 bool short_alternative(int op, int dt, int64_t NV, bool very_short, Choice* c) {
   if (op == kSoftmax && dt == QK_F32 && NV > 512 && NV <= 1024) {
     *c = Choice{1024, 128, 128, 8, 1, very_short ? 3 : 2};
+    return true;
+  }
+  if (op == kXent && NV > 256 && NV <= 512 && very_short) {
+    *c = Choice{512, 128, 64, 8, 1, 2};
     return true;
   }
   return false;

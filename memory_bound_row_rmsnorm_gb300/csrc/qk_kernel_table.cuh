@@ -46,6 +46,10 @@ const KernelEntry kTable[] = {
     QK_RING(512, 512, 2, false),
     QK_RING(512, 512, 4, false),
     QK_RING(512, 512, 8, false),
+#if QK_OP == 2  // cross-entropy: 128-thread CTAs of two 64-thread rows (finer items for short launches)
+    QK_RING(128, 64, 8, false),
+    QK_RING(128, 32, 16, false),
+#endif
 #if QK_OP != 2  // cross-entropy streams long rows instead of splitting them
     QK_RING(256, 256, 4, true),
     QK_RING(256, 256, 8, true),
