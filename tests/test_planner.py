@@ -1,0 +1,101 @@
+"""The launch planner's documented rules, read back through qk_get_plan on the
+device (the occupancy answers come from the GPU), and the results of the
+plans those rules pick against the oracle:
+  * a one-chunk, unclustered launch of few items per resident CTA gets a
+    deeper ring: RMSNorm and LayerNorm three slots below 8 items per CTA,
+    softmax three below 4 and two below 8, the others three below 4 -- and
+    never at the cost of a resident CTA;
+  * fp32 softmax rows of 4096 switch to 128-thread CTAs of 8 vectors a thread
+    below 8 items per resident CTA; cross-entropy rows of 512 vectors to two
+    64-thread rows per CTA below 4;
+  * a launch of fewer than two items per resident CTA gives every CTA the
+    same number of items;
+  * cross-entropy rows of 512 vectors otherwise run one warp a row, 16
+    vectors a lane; bf16 softmax rows of 8192 elements 128 x 8 vectors."""
+import pytest
+import torch
+
+from memory_bound_row_rmsnorm_gb300 import binding as qb
+from memory_bound_row_rmsnorm_gb300 import synthetic as syn
+from test_parity import DEV, check_against_oracle, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+OP = {"softmax": qb.QK_OP_SOFTMAX, "rmsnorm": qb.QK_OP_RMSNORM, "xent": qb.QK_OP_XENT,
+      "layernorm": qb.QK_OP_LAYERNORM}
+DT = {"f32": qb.QK_F32, "bf16": qb.QK_BF16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for the gpu tests")
+    from memory_bound_row_rmsnorm_gb300 import build
+    build.build()
+    qb.load_library()
+    torch.cuda.set_device(0)
+
+
+def plan(op, dtype, M, N):
+    return qb.qk_get_plan(OP[op], DT[dtype], M, N)
+
+
+def items(p, M):
+    return -(-M // (p["threads"] // p["row_threads"]))
+
+
+def resident(p):
+    return p["ctas_per_sm"] * torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("op,dtype,N", [("rmsnorm", "bf16", 1024), ("rmsnorm", "f32", 8192),
+                                        ("layernorm", "f32", 2048), ("softmax", "bf16", 4096)])
+def test_ring_depth_follows_items_per_cta(op, dtype, N):
+    long_ = plan(op, dtype, 1 << 20, N)  # many items per CTA: the table's slots
+    for M in (256, 1024, 4096, 16384, 65536):
+        p = plan(op, dtype, M, N)
+        assert p["ctas_per_sm"] == long_["ctas_per_sm"], "a deeper ring never costs a resident CTA"
+        ipc = items(p, M) / resident(p)
+        t3, t2 = (8, 0) if op in ("rmsnorm", "layernorm") else (4, 8)
+        if ipc < t3:  # three slots unless that would cost a resident CTA
+            assert p["slots"] >= long_["slots"]
+        if t3 <= ipc < t2:  # softmax: two slots (one more 8-16 KiB slot costs no CTA here)
+            assert p["slots"] >= 2, (M, p)
+        if ipc >= max(t3, t2):
+            assert p["slots"] == long_["slots"], (M, p, long_)
+
+
+def test_short_softmax_rows_of_4096_use_the_128_thread_kernel():
+    short = plan("softmax", "f32", 1024, 4096)
+    long_ = plan("softmax", "f32", 65536, 4096)
+    assert (short["threads"], short["row_threads"], short["vec_per_thread"], short["slots"]) == (128, 128, 8, 3)
+    assert (long_["threads"], long_["row_threads"], long_["vec_per_thread"], long_["slots"]) == (256, 256, 4, 1)
+    mid = plan("softmax", "f32", 4096, 4096)
+    assert (mid["threads"], mid["vec_per_thread"], mid["slots"]) == (128, 8, 2)
+
+
+def test_short_launches_give_every_cta_the_same_items():
+    p = plan("softmax", "f32", 1024, 4096)
+    assert 1024 % p["grid"] == 0 and 1024 // p["grid"] == 2, p
+    q = plan("softmax", "f32", 2048, 4096)  # three or more items per CTA: the full grid
+    assert q["grid"] == resident(q), q
+
+
+def test_cross_entropy_rows_of_512_vectors():
+    for dtype, N in (("bf16", 4096), ("f32", 2048)):
+        p = plan("xent", dtype, 16384, N)
+        assert (p["threads"], p["row_threads"], p["vec_per_thread"], p["slots"]) == (128, 32, 16, 2), p
+        s = plan("xent", dtype, 2048, N)
+        assert (s["threads"], s["row_threads"], s["vec_per_thread"]) == (128, 64, 8), s
+    b = plan("softmax", "bf16", 16384, 8192)
+    assert (b["threads"], b["row_threads"], b["vec_per_thread"]) == (128, 128, 8), b
+
+
+@pytest.mark.parametrize("op,dtype,M,N", [("softmax", "f32", 1024, 4096), ("softmax", "f32", 4096, 4096),
+                                          ("xent", "bf16", 2048, 4096), ("xent", "f32", 16384, 2048),
+                                          ("rmsnorm", "bf16", 2000, 1024), ("softmax", "bf16", 3000, 8192)])
+def test_the_chosen_plans_match_the_oracle(op, dtype, M, N):
+    """Every row against the oracle, on ragged row counts where it matters."""
+    inp = syn.make_inputs(op, dtype, M, N, 13000 + M, "cpu")
+    out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, dtype)
+    check_against_oracle(op, dtype, inp, out, what=f"planner {op} {dtype} {M}x{N}")
