@@ -258,6 +258,15 @@ const Choice kLayerNormTable[] = {
     {2048, 512, 512, 4, 1, 2},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 8, 8, 2},  {32768, 512, 512, 8, 8, 1},   {65536, 512, 512, 8, 16, 2},
 };
+// fp32 LayerNorm rows of 131072 elements (32768 vectors): clusters of 16
+// 256-thread CTAs with two ring slots, 83 % -> 93 % at 8192-16384 rows; bf16
+// rows of the same bytes measured 2 points slower that way and keep 512 x 8.
+const Choice kLayerNormF32Table[] = {
+    {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 2},       {128, 256, 32, 4, 1, 2},
+    {256, 256, 32, 8, 1, 3},     {512, 256, 128, 4, 1, 2},     {1024, 128, 128, 8, 1, 1},
+    {2048, 512, 512, 4, 1, 2},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {16384, 256, 256, 8, 8, 2},  {32768, 256, 256, 8, 16, 2},  {65536, 512, 512, 8, 16, 2},
+};
 const Choice kSoftmaxTable[] = {
     {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 3},       {128, 256, 32, 4, 1, 3},
     {256, 256, 64, 4, 1, 2},     {512, 128, 128, 4, 1, 1},     {1024, 256, 256, 4, 1, 1},
@@ -322,7 +331,13 @@ qk_status choose_ring(int op, int dt, int64_t NV, int* th, int* tpr, int* vpt, i
     case kXent: QK_TABLE(kXentTable); break;
     case kOpSoftmaxBwd: QK_TABLE(kSoftmaxBwdTable); break;
     case kOpRmsNormBwd: QK_TABLE(kRmsNormBwdTable); break;
-    case kOpLayerNorm: QK_TABLE(kLayerNormTable); break;
+    case kOpLayerNorm:
+      if (dt == QK_F32) {
+        QK_TABLE(kLayerNormF32Table);
+      } else {
+        QK_TABLE(kLayerNormTable);
+      }
+      break;
     default: QK_TABLE(kXentBwdTable); break;
   }
 #undef QK_TABLE

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 API = os.path.join(ROOT, "memory_bound_row_rmsnorm_gb300", "csrc", "qk_api.cu")
 DTYPES = ("float", "__nv_bfloat16")
 # template operator codes (qk_internal.h enum Op, qk_bwd_kernels.cuh enum BwdOp)
-ROW_OPS = {"kRmsNormTable": 1, "kSoftmaxTable": 0, "kSoftmaxBf16Table": 0, "kXentTable": 2, "kLayerNormTable": 3}
+ROW_OPS = {"kRmsNormTable": 1, "kSoftmaxTable": 0, "kSoftmaxBf16Table": 0, "kXentTable": 2, "kLayerNormTable": 3,
+           "kLayerNormF32Table": 3}
 BWD_OPS = {"kSoftmaxBwdTable": 10, "kRmsNormBwdTable": 11, "kXentBwdTable": 12}
 SHIFT_OPS = {0: "softmax", 1: "rmsnorm", 2: "xent", 3: "layernorm", 4: "xent backward", 5: "softmax backward"}
 
