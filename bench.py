@@ -305,11 +305,20 @@ def timed_launches(qb, op, dtype, sets, M, N, K, stream, graph: bool, dev):
     the graph is replayed, which removes host launch overhead between steps;
     the two events are then nodes of the graph itself, recorded right before
     the first call and right after the last, so that the graph's own launch
-    is not counted.  Either way a head start (head_start) precedes the
-    timed region."""
+    is not counted.  Either way one untimed pass over every set, in the
+    order the timed steps take them, comes first, so that each timed step's
+    set was last touched len(sets) steps earlier (none is still in L2 from an
+    earlier pass), and a head start (head_start) precedes the timed region."""
     nsets = len(sets)
+
+    def rotate():
+        for i in range(nsets):
+            inp, out = sets[i]
+            launch(qb, op, dtype, inp, out, M, N, stream)
+
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if not graph:
+        rotate()
         head_start(stream)
         start.record(stream)
         for i in range(K):
@@ -329,6 +338,7 @@ def timed_launches(qb, op, dtype, sets, M, N, K, stream, graph: bool, dev):
         stop.record(cs)
     g.replay()  # first replay uploads the graph
     torch.cuda.synchronize(dev)
+    rotate()
     head_start(stream)
     g.replay()
     timed_launches.keep = g  # the graph must outlive the replay
@@ -531,6 +541,13 @@ def run_reference(args, op, dtype, M, N, sigma):
 
 
 HOLD_S = 0.3  # untimed hold after each entry's timed regions, so that its clock record has samples
+# A K-step graph region shorter than this is timed once more, with enough steps
+# to last about LONG_TARGET_MS: the same kernel's rate once the region's one-off
+# costs (its first launch, which no earlier kernel overlaps; the event pair) are
+# spread over many calls.  Reported beside the K-step number, never instead of it.
+LONG_REGION_MS = 2.0
+LONG_TARGET_MS = 4.0
+LONG_MAX_STEPS = 2000
 ALL_WORKLOADS = {**syn.WORKLOADS, **syn.BWD_WORKLOADS, **syn.NEXT_WORKLOADS}
 
 
@@ -560,10 +577,13 @@ def hold(qb, op, dtype, sets, M, N, stream, dev, seconds: float, per_launch_ms: 
 
 
 def time_entry(qb, op, dtype, M, N, sigma, K, W, dev, stream, seed=77, hold_s=HOLD_S,
-               modes=("graph", "stream")):
+               modes=("graph", "stream"), long_region=False):
     """W warm-up steps, then K steps timed once per launch mode, then an untimed
     hold.  Returns ({mode: ms per step}, (start of the warm-up, end of the
-    hold), {"t0", "t1"} of the timed regions), the times from time.time()."""
+    hold), {"t0", "t1"} of the timed regions), the times from time.time().
+    With long_region, a graph region of K steps that lasts under
+    LONG_REGION_MS is timed once more with enough steps to last about
+    LONG_TARGET_MS: ms["graph_long"] = (steps, ms per step)."""
     sb = min_bytes(op, dtype, M, N)
     sets = [make_set(op, dtype, M, N, sigma, seed + i, dev) for i in range(n_sets(sb))]
     torch.cuda.synchronize(dev)
@@ -577,9 +597,15 @@ def time_entry(qb, op, dtype, M, N, sigma, K, W, dev, stream, seed=77, hold_s=HO
         e0, e1 = timed_launches(qb, op, dtype, sets, M, N, K, stream, mode == "graph", dev)
         torch.cuda.synchronize(dev)
         ms[mode] = e0.elapsed_time(e1) / K
+    per_step = min(ms.values())
+    if long_region and "graph" in ms and K * ms["graph"] < LONG_REGION_MS:
+        KL = min(LONG_MAX_STEPS, max(K, math.ceil(LONG_TARGET_MS / ms["graph"])))
+        e0, e1 = timed_launches(qb, op, dtype, sets, M, N, KL, stream, True, dev)
+        torch.cuda.synchronize(dev)
+        ms["graph_long"] = (KL, e0.elapsed_time(e1) / KL)
     t1 = time.time()
     if hold_s > 0:
-        hold(qb, op, dtype, sets, M, N, stream, dev, hold_s, min(ms.values()))
+        hold(qb, op, dtype, sets, M, N, stream, dev, hold_s, per_step)
     t_end = time.time()
     st = qb.qk_get_device_status(stream)
     if st != qb.QK_OK:
@@ -607,11 +633,11 @@ def workload_entry(qb, name, K, W, dev, stream, peak, peak_src) -> dict:
     the launch plan; "clocks" holds the entry's time window until the sampler
     has stopped (finish_clocks)."""
     op, dtype, M, N, sigma = ALL_WORKLOADS[name]
-    ms, window, _ = time_entry(qb, op, dtype, M, N, sigma, K, W, dev, stream)
+    ms, window, _ = time_entry(qb, op, dtype, M, N, sigma, K, W, dev, stream, long_region=True)
     code = qb.QK_F32 if dtype == "f32" else qb.QK_BF16
     plan = qb.qk_get_plan(OP_CODES[op], code, M, N)
     g, s = ms["graph"], ms["stream"]
-    return {
+    entry = {
         "workload": name, "op": op, "dtype": dtype, "M": M, "N": N, "steps": K, "warmup": W,
         "ms_per_step": g, "value": tbs_of(op, dtype, M, N, g), "unit": "TB/s", "launch": "cuda_graph",
         "stream": {"ms_per_step": s, "value": tbs_of(op, dtype, M, N, s),
@@ -619,6 +645,38 @@ def workload_entry(qb, name, K, W, dev, stream, peak, peak_src) -> dict:
         "roofline": roofline(op, dtype, M, N, g, peak, peak_src, recorded_traffic(name, plan)),
         "gpu_launches": K * kernels_per_step(op), "clocks": window, "plan": plan,
     }
+    if "graph_long" in ms:
+        entry["long_region"] = long_region_entry(op, dtype, M, N, *ms["graph_long"], peak)
+    return entry
+
+
+def long_region_entry(op, dtype, M, N, steps, ms_step, peak) -> dict:
+    return {"steps": steps, "ms_per_step": ms_step, "value": tbs_of(op, dtype, M, N, ms_step),
+            "frac": tbs_of(op, dtype, M, N, ms_step) * 1e3 / peak,
+            "how": "the same calls as one graph of this many steps (a region of about "
+                   f"{LONG_TARGET_MS:g} ms), timed after the K-step regions"}
+
+
+def region_floor_ms(dev, stream, reps: int = 5) -> float:
+    """Device time between the two events of an empty timed region (a graph
+    holding only the event pair, replayed after a head start): the part of
+    every graph-timed number that no kernel can remove.  Median of reps."""
+    ts = []
+    for _ in range(reps):
+        start = torch.cuda.Event(enable_timing=True, external=True)
+        stop = torch.cuda.Event(enable_timing=True, external=True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream(dev)
+            start.record(cs)
+            stop.record(cs)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        head_start(stream)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        ts.append(start.elapsed_time(stop))
+    return statistics.median(ts)
 
 
 def finish_clocks(entries: list, sampler) -> None:
@@ -802,6 +860,18 @@ def main():
             dist.barrier()
         ms = start.elapsed_time(stop)
         elapsed[mode] = max_over_ranks(ms, dist, dev) if ws > 1 else ms
+    long_steps = None
+    if elapsed["graph"] < LONG_REGION_MS:  # see LONG_REGION_MS
+        long_steps = min(LONG_MAX_STEPS, max(K, math.ceil(LONG_TARGET_MS * K / elapsed["graph"])))
+        if ws > 1:
+            dist.barrier()
+        start, stop = timed_launches(qb, op, dtype, sets, M, N, long_steps, stream, True, dev)
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            dist.barrier()
+        ms = start.elapsed_time(stop)
+        elapsed["graph_long"] = max_over_ranks(ms, dist, dev) if ws > 1 else ms
+    floor_ms = region_floor_ms(dev, stream)
     if args.hold > 0:
         hold(qb, op, dtype, sets, M, N, stream, dev, args.hold, elapsed["graph"] / K)
     t_end = time.time()
@@ -883,7 +953,12 @@ def main():
                 "how": "pinned host buffers; copy-in, call, copy-out every step, pipelined over 3 streams"},
         "gpu_launches": K * kernels_per_step(op),
         "clocks": dict(clocks, window="warm-up, both timed regions and a 0.3 s hold of the same steps"),
+        "region_floor_us": floor_ms * 1e3,
     }
+    if long_steps is not None:
+        line["long_region"] = long_region_entry(op, dtype, M, N, long_steps,
+                                                elapsed["graph_long"] / long_steps, peak)
+        line["long_region"]["value"] *= ws
     if per_workload is not None:
         line["per_workload"] = per_workload
     if sweep is not None:
