@@ -104,6 +104,10 @@ typedef enum {
  *   y      [M, N] dtype, written once.  y == x (exact aliasing) is allowed;
  *          any other overlap with x is QK_ERR_INVALID_ARG.
  *   M, N   rows and columns (any N on the aligned path; see qk_max_row_elements).
+ * Non-finite inputs (not part of the parity contract): a -inf entry gets
+ * probability 0 and the rest of its row is the softmax of the finite entries
+ * (masked logits); a row with no finite entry has no distribution (0/0) and
+ * gets NaN in every entry, as the definition gives; NaN and +inf propagate.
  */
 QK_API qk_status qk_softmax_fwd(const void* x, void* y, int64_t M, int64_t N, qk_dtype dtype,
                          void* stream);
@@ -162,6 +166,9 @@ QK_API qk_status qk_layernorm_fwd(const void* x, const void* w, const void* b, v
  *   loss    [M] float32, written once.
  *   lse     [M] float32, written once; may be NULL when not wanted.
  *   Any N >= 1 is supported.
+ * Non-finite logits: -inf entries drop out of the sum (masked logits); a
+ * -inf target logit gives loss = +inf; a row with no finite entry gives
+ * lse = -inf (the log of an empty sum) and loss = NaN.
  */
 QK_API qk_status qk_xent_fwd(const void* logits, const int64_t* targets, float* loss, float* lse,
                       int64_t M, int64_t N, qk_dtype dtype, void* stream);

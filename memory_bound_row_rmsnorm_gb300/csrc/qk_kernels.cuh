@@ -71,6 +71,16 @@ __device__ __forceinline__ void merge_partials(const float2* p, int n, float& m,
   }
 }
 
+// The softmax finish factor exp(m_t - M) / S of a thread whose own entries
+// have maximum m_t, in a row of maximum M and sum S = sum exp(x - M): 0 when
+// the thread holds only -inf entries (their probabilities are 0), NaN when the
+// whole row is -inf (S = 0: there is no distribution to normalise, and the
+// plain definition gives 0/0).
+__device__ __forceinline__ float softmax_scale(float tm, float pm, float ps) {
+  if (pm == kNegInf) return __int_as_float(0x7fc00000);
+  return (tm == kNegInf) ? 0.f : __fdividef(exp2_approx((tm - pm) * kLog2e), ps);
+}
+
 // TWO_PASS (softmax, RMSNorm, LayerNorm rows longer than a cluster holds): every row
 // slice is streamed through the ring twice in chunks -- the first pass
 // accumulates the reduction, the second re-reads each chunk and writes its
@@ -659,7 +669,8 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, T, THREADS, VPT, 
     if constexpr (TWO_PASS) {  // keep the totals for the second pass
       if constexpr (OP == kSoftmax) {
         tot_a = (pm == kNegInf) ? 0.f : pm * kLog2e;  // M log2 e
-        tot_b = __fdividef(1.f, ps);                  // 1 / S
+        // 1 / S, NaN for a row with no finite entry (as softmax_scale)
+        tot_b = (pm == kNegInf) ? __int_as_float(0x7fc00000) : __fdividef(1.f, ps);
       } else if constexpr (OP == kRmsNorm) {
         tot_a = rsqrtf(fmaf(ps, a.inv_n, a.eps));     // rstd
         if (l == 0 && rank == 0 && row_ok && a.rstd != nullptr) a.rstd[row] = tot_a;
@@ -677,7 +688,7 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, T, THREADS, VPT, 
     // ---- finish: outputs from registers, each stored once ----
     if (!row_ok) continue;
     if constexpr (OP == kSoftmax) {
-      const float scale = (tm == kNegInf) ? 0.f : __fdividef(exp2_approx((tm - pm) * kLog2e), ps);
+      const float scale = softmax_scale(tm, pm, ps);
       const float2 sc = make_float2(scale, scale);
       const float mb = (tm == kNegInf) ? 0.f : tm * kLog2e;
       uint4* yg = static_cast<uint4*>(a.y) + row * NV + cbase;
@@ -939,7 +950,7 @@ __global__ void __launch_bounds__(THREADS) direct_kernel(const RowArgs a) {
   }
 
   if constexpr (OP == kSoftmax) {
-    const float scale = (tm == kNegInf) ? 0.f : __fdividef(exp2_approx((tm - pm) * kLog2e), ps);
+    const float scale = softmax_scale(tm, pm, ps);
     T* yrow = static_cast<T*>(a.y) + row * N + e0;
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {

@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
     } else {
       float sa = 0.f, sb2 = 0.f;  // per-row factors of the finish
       if constexpr (OP == kSoftmax) {
-        sa = (tm == kNegInf) ? 0.f : __fdividef(exp2_approx((tm - pm) * kLog2e), ps);  // scale
+        sa = softmax_scale(tm, pm, ps);                                               // scale
         sb2 = (tm == kNegInf) ? 0.f : tm * kLog2e;                                    // m_t log2 e
       } else if constexpr (OP == kRmsNorm) {
         sa = rsqrtf(fmaf(ps, a.inv_n, a.eps));
