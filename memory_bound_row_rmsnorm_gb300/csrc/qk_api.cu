@@ -374,6 +374,18 @@ SlotBands slot_bands(int op) {
   if (op == kSoftmax) return {4, 8};
   return {4, 0};
 }
+// Backward launches below this many items per resident CTA take a ring of
+// three slots when that costs no resident CTA, else two when that costs at
+// most one CTA per SM, and keep the full grid.  A one-slot ring makes each CTA
+// load, reduce and write its items one after another, which a short launch
+// cannot hide (same-GPU A/B from graphs of 20-400 calls: softmax backward
+// fp32 1024 x 4096 82 % -> 95 %, 2048 x 4096 85 % -> 93 %, bf16 2048 x 4096
+// 85 % -> 98 %; cross-entropy backward fp32 4096 x 4096 85 % -> 97 %).
+// Three slots at the cost of a CTA measured worse (up to 6 points), and so
+// did the balanced short grid below for the two-input passes (softmax
+// backward bf16 1024 x 4096: 81 % on the full grid, 67 % balanced); at 9
+// items per CTA and more the table's ring was as good or better.
+constexpr int kBwdDeepRingItems = 8;
 
 // Alternative kernels for short launches (fewer than 8 items per resident CTA
 // of the table's plan):
@@ -484,11 +496,12 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   if (st != QK_OK) return st;
   if (occ <= 0) return QK_ERR_UNSUPPORTED;
   // CTAs per SM the launch can hold (clusters: resident clusters' CTAs over the SMs)
-  const int64_t ctas_per_sm = cl > 1 ? std::max<int64_t>(1, int64_t(occ) * cl / std::max(1, d.sms)) : occ;
+  int64_t ctas_per_sm = cl > 1 ? std::max<int64_t>(1, int64_t(occ) * cl / std::max(1, d.sms)) : occ;
 
   // Short launches spend most of their time waiting for their first loads:
   // below the operator's bands of items per resident CTA, give each CTA a
-  // ring of three (or two) slots, if that costs no resident CTA.  (Softmax
+  // ring of three (or two) slots, if that costs no resident CTA (backward
+  // launches: two slots may cost one, see kBwdDeepRingItems).  (Softmax
   // fp32 1024 x 4096: 70 % -> 75 %; 2048 x 4096: 76 % -> 97 %; RMSNorm bf16
   // 16384 x 1024: 90 % -> 98 %.)
   const bool short_ok = !ov.on && !two_pass && k == 1 && cl == 1;
@@ -501,17 +514,22 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   }
   int64_t smem_used = smem;
   const SlotBands band = slot_bands(op);
-  const int want = !short_ok || alt != nullptr               ? 0
-                   : p->num_items < band.t3 * resident ? 3
-                   : p->num_items < band.t2 * resident ? 2
-                                                       : 0;
+  const bool bwd = is_bwd(op);
+  const int want = !short_ok || alt != nullptr                               ? 0
+                   : bwd ? (p->num_items < kBwdDeepRingItems * resident ? 3 : 0)
+                   : p->num_items < band.t3 * resident                      ? 3
+                   : p->num_items < band.t2 * resident                      ? 2
+                                                                             : 0;
   for (int s = want; s > slots; --s) {
     const int64_t smem_s = kSmemHeader + int64_t(s) * nin * slot_bytes + param_bytes;
+    const int min_occ = (bwd && s == 2) ? std::max(1, occ - 1) : occ;  // see kBwdDeepRingItems
     int occ_s = 0;
     if (smem_s <= d.smem_optin && occupancy(dev, *ke, int(smem_s), 0, &occ_s) == QK_OK &&
-        occ_s >= occ) {
+        occ_s >= min_occ) {
       slots = s;
       smem_used = smem_s;
+      occ = occ_s;  // unclustered here: the grid below follows the new residency
+      ctas_per_sm = occ_s;
       break;
     }
   }
@@ -528,9 +546,11 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   units = std::min<int64_t>(units, p->num_items);
   // A launch of fewer than two items per CTA lasts as long as its busiest
   // CTA: give every CTA the same number (softmax fp32 1024 x 4096: 512 CTAs of
-  // two rows rather than 608 of one or two, 86 % -> 87 %; at three or more
-  // items per CTA the full grid measured better).
-  if (short_ok && p->num_items < 2 * units) {
+  // two rows rather than 608 of one or two, 86 % -> 87 %; cross-entropy
+  // backward fp32 1024 x 4096 +2 points).  At three or more items per CTA the
+  // full grid measured better, and so it did for the backward passes that
+  // load two matrices per item (softmax, RMSNorm; see kBwdDeepRingItems).
+  if (short_ok && nin == 1 && p->num_items < 2 * units) {
     const int64_t per = (p->num_items + units - 1) / units;
     units = (p->num_items + per - 1) / per;
   }

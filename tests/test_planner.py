@@ -11,10 +11,15 @@ plans those rules pick against the oracle:
   * a launch of fewer than two items per resident CTA gives every CTA the
     same number of items;
   * cross-entropy rows of 512 vectors otherwise run one warp a row, 16
-    vectors a lane; bf16 softmax rows of 8192 elements 128 x 8 vectors."""
+    vectors a lane; bf16 softmax rows of 8192 elements 128 x 8 vectors;
+  * a one-chunk, unclustered backward launch of fewer than 8 items per
+    resident CTA takes a ring of three slots if that costs no resident CTA,
+    else two if that costs at most one per SM; the passes with two inputs
+    per item (softmax, RMSNorm) keep the full grid."""
 import pytest
 import torch
 
+import test_backward as tb
 from memory_bound_row_rmsnorm_gb300 import binding as qb
 from memory_bound_row_rmsnorm_gb300 import synthetic as syn
 from test_parity import DEV, check_against_oracle, run_gpu
@@ -22,7 +27,8 @@ from test_parity import DEV, check_against_oracle, run_gpu
 pytestmark = pytest.mark.gpu
 
 OP = {"softmax": qb.QK_OP_SOFTMAX, "rmsnorm": qb.QK_OP_RMSNORM, "xent": qb.QK_OP_XENT,
-      "layernorm": qb.QK_OP_LAYERNORM}
+      "layernorm": qb.QK_OP_LAYERNORM, "softmax_bwd": qb.QK_OP_SOFTMAX_BWD,
+      "rmsnorm_bwd": qb.QK_OP_RMSNORM_BWD, "xent_bwd": qb.QK_OP_XENT_BWD}
 DT = {"f32": qb.QK_F32, "bf16": qb.QK_BF16}
 
 
@@ -99,3 +105,39 @@ def test_the_chosen_plans_match_the_oracle(op, dtype, M, N):
     inp = syn.make_inputs(op, dtype, M, N, 13000 + M, "cpu")
     out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, dtype)
     check_against_oracle(op, dtype, inp, out, what=f"planner {op} {dtype} {M}x{N}")
+
+
+@pytest.mark.parametrize("op,dtype,N", [("softmax_bwd", "f32", 4096), ("softmax_bwd", "bf16", 4096),
+                                        ("xent_bwd", "f32", 4096), ("xent_bwd", "bf16", 16384),
+                                        ("rmsnorm_bwd", "f32", 4096)])
+def test_backward_ring_depth_follows_items_per_cta(op, dtype, N):
+    long_ = plan(op, dtype, 1 << 20, N)  # many items per CTA: the table's ring
+    assert long_["cluster"] == 1 and long_["chunks"] == 1
+    for M in (1024, 2048, 4096, 8192, 16384, 65536):
+        p = plan(op, dtype, M, N)
+        assert p["ctas_per_sm"] >= long_["ctas_per_sm"] - 1, "at most one resident CTA for the deeper ring"
+        ipc = items(p, M) / (long_["ctas_per_sm"] * torch.cuda.get_device_properties(0).multi_processor_count)
+        if ipc < 8:  # each of these shapes has a deeper ring within one CTA per SM
+            assert p["slots"] > long_["slots"], (M, p, long_)
+            if p["ctas_per_sm"] < long_["ctas_per_sm"]:
+                assert p["slots"] == 2, (M, p, long_)
+            n, units = items(p, M), min(items(p, M), resident(p))
+            if op != "xent_bwd":  # two inputs per item: the full grid
+                assert p["grid"] == units, p
+            elif n < 2 * units:  # one input: every CTA the same number of items
+                per = -(-n // units)
+                assert p["grid"] == -(-n // per), p
+        else:
+            assert p["slots"] == long_["slots"] and p["ctas_per_sm"] == long_["ctas_per_sm"], (M, p, long_)
+
+
+@pytest.mark.parametrize("op,dtype,M,N", [("softmax", "f32", 1024, 4096), ("softmax", "bf16", 2048, 4096),
+                                          ("xent", "f32", 4096, 4096), ("xent", "bf16", 2048, 16384),
+                                          ("rmsnorm", "f32", 2048, 4096)])
+def test_the_chosen_backward_plans_match_the_oracle(op, dtype, M, N):
+    """The deeper-ring backward plans, every row against the oracle."""
+    p = plan(op + "_bwd", dtype, M, N)
+    assert p["slots"] >= 2, p
+    case = tb.make_case(op, dtype, M, N, 14000 + M)
+    out = tb.run_gpu(op, dtype, case)
+    tb.check(op, dtype, case, out, f"planner {op} bwd {dtype} {M}x{N}")
