@@ -251,11 +251,14 @@ const Choice kRmsNormTable[] = {
 // LayerNorm: from a sweep of every compiled configuration on GB300 (M = 16384,
 // N = 256 ... 262144, fp32 and bf16; rows of 512 and 2048 vectors again at
 // 8192-32768 rows).  Its parameters not held in registers take shared memory,
-// so long rows keep fewer ring slots than RMSNorm.
+// so long rows keep fewer ring slots than RMSNorm.  This table is bf16's; a
+// later sweep of 1-4 slots at 8192-32768 rows deepened its rows of 8192
+// elements to two slots (83-88 % -> 88-91 %) and of 16384 to three (94-97 %
+// -> 97-98 %).
 const Choice kLayerNormTable[] = {
     {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 2},       {128, 256, 32, 4, 1, 2},
-    {256, 256, 32, 8, 1, 3},     {512, 256, 128, 4, 1, 2},     {1024, 128, 128, 8, 1, 1},
-    {2048, 512, 512, 4, 1, 2},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
+    {256, 256, 32, 8, 1, 3},     {512, 256, 128, 4, 1, 2},     {1024, 128, 128, 8, 1, 2},
+    {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 8, 8, 2},  {32768, 512, 512, 8, 8, 1},   {65536, 512, 512, 8, 16, 2},
 };
 // fp32 LayerNorm rows of 131072 elements (32768 vectors): clusters of 16
@@ -301,9 +304,20 @@ const Choice kSoftmaxBwdTable[] = {
     {2048, 256, 256, 8, 1, 2}, {4096, 256, 256, 8, 2, 1}, {8192, 256, 256, 8, 4, 1},
     {16384, 256, 256, 8, 8, 1}, {32768, 256, 256, 8, 16, 1},
 };
+// RMSNorm backward: a ring depth per dtype from a sweep of 1-4 slots at
+// 8192-32768 rows.  fp32 rows of 2048 take four slots (three CTAs per SM
+// instead of five: 76 % -> 88 %, 86 % -> 95 %, 92 % -> 98 %; fewer CTAs also
+// means fewer dw partial rows to sum), bf16 rows of 8192 three (82 % -> 88 %,
+// 86 % -> 93 %, 90 % -> 97 %); the other rows measured best at two.
 const Choice kRmsNormBwdTable[] = {
     {32, 256, 32, 2, 1, 2},    {64, 256, 64, 2, 1, 2},    {128, 256, 64, 2, 1, 2},
-    {256, 256, 128, 2, 1, 2},  {512, 128, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 2},
+    {256, 256, 128, 2, 1, 2},  {512, 128, 128, 4, 1, 4},  {1024, 256, 256, 4, 1, 2},
+    {2048, 256, 256, 4, 2, 2}, {4096, 512, 512, 4, 2, 2}, {8192, 512, 512, 4, 4, 2},
+    {16384, 512, 512, 4, 8, 2}, {32768, 512, 512, 4, 16, 2},
+};
+const Choice kRmsNormBwdBf16Table[] = {
+    {32, 256, 32, 2, 1, 2},    {64, 256, 64, 2, 1, 2},    {128, 256, 64, 2, 1, 2},
+    {256, 256, 128, 2, 1, 2},  {512, 128, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 3},
     {2048, 256, 256, 4, 2, 2}, {4096, 512, 512, 4, 2, 2}, {8192, 512, 512, 4, 4, 2},
     {16384, 512, 512, 4, 8, 2}, {32768, 512, 512, 4, 16, 2},
 };
@@ -330,7 +344,13 @@ qk_status choose_ring(int op, int dt, int64_t NV, int* th, int* tpr, int* vpt, i
     case kRmsNorm: QK_TABLE(kRmsNormTable); break;
     case kXent: QK_TABLE(kXentTable); break;
     case kOpSoftmaxBwd: QK_TABLE(kSoftmaxBwdTable); break;
-    case kOpRmsNormBwd: QK_TABLE(kRmsNormBwdTable); break;
+    case kOpRmsNormBwd:
+      if (dt == QK_BF16) {
+        QK_TABLE(kRmsNormBwdBf16Table);
+      } else {
+        QK_TABLE(kRmsNormBwdTable);
+      }
+      break;
     case kOpLayerNorm:
       if (dt == QK_F32) {
         QK_TABLE(kLayerNormF32Table);

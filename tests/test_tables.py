@@ -16,7 +16,7 @@ DTYPES = ("float", "__nv_bfloat16")
 # template operator codes (qk_internal.h enum Op, qk_bwd_kernels.cuh enum BwdOp)
 ROW_OPS = {"kRmsNormTable": 1, "kSoftmaxTable": 0, "kSoftmaxBf16Table": 0, "kXentTable": 2, "kLayerNormTable": 3,
            "kLayerNormF32Table": 3}
-BWD_OPS = {"kSoftmaxBwdTable": 10, "kRmsNormBwdTable": 11, "kXentBwdTable": 12}
+BWD_OPS = {"kSoftmaxBwdTable": 10, "kRmsNormBwdTable": 11, "kRmsNormBwdBf16Table": 11, "kXentBwdTable": 12}
 SHIFT_OPS = {0: "softmax", 1: "rmsnorm", 2: "xent", 3: "layernorm", 4: "xent backward", 5: "softmax backward"}
 
 
