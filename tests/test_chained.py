@@ -36,27 +36,27 @@ def _nan(shape, dtype):
 def test_dependent_calls_on_one_stream(dtype, M, N):
     code = DT_CODE[dtype]
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-    rounds = 3
-    inp = [syn.make_inputs("layernorm", dtype, M, N, 12000 + 10 * r + N, "cpu") for r in range(rounds)]
-    z0 = [syn.make_inputs("softmax", dtype, M, N, 12500 + 10 * r + N, "cpu")["x"] for r in range(rounds)]
+    passes = 3
+    inp = [syn.make_inputs("layernorm", dtype, M, N, 12000 + 10 * r + N, "cpu") for r in range(passes)]
+    z0 = [syn.make_inputs("softmax", dtype, M, N, 12500 + 10 * r + N, "cpu")["x"] for r in range(passes)]
     g = torch.Generator().manual_seed(12100 + N)
     targets = torch.randint(0, N, (M,), generator=g, dtype=torch.int64)
     w, b, t = inp[0]["w"].to(DEV), inp[0]["b"].to(DEV), targets.to(DEV)
     # every buffer exists before the first launch of the chain
     X = [d["x"].to(DEV) for d in inp]
     Z = [z.to(DEV) for z in z0]
-    Y1 = [_nan((M, N), tdt) for _ in range(rounds)]
-    R1 = [_nan((M,), torch.float32) for _ in range(rounds)]
-    S2 = [_nan((M, N), tdt) for _ in range(rounds)]
-    loss = [_nan((M,), torch.float32) for _ in range(rounds)]
-    lse = [_nan((M,), torch.float32) for _ in range(rounds)]
-    Y4 = [_nan((M, N), tdt) for _ in range(rounds)]
-    mean4 = [_nan((M,), torch.float32) for _ in range(rounds)]
-    rstd4 = [_nan((M,), torch.float32) for _ in range(rounds)]
-    R6 = [_nan((M,), torch.float32) for _ in range(rounds)]
+    Y1 = [_nan((M, N), tdt) for _ in range(passes)]
+    R1 = [_nan((M,), torch.float32) for _ in range(passes)]
+    S2 = [_nan((M, N), tdt) for _ in range(passes)]
+    loss = [_nan((M,), torch.float32) for _ in range(passes)]
+    lse = [_nan((M,), torch.float32) for _ in range(passes)]
+    Y4 = [_nan((M, N), tdt) for _ in range(passes)]
+    mean4 = [_nan((M,), torch.float32) for _ in range(passes)]
+    rstd4 = [_nan((M,), torch.float32) for _ in range(passes)]
+    R6 = [_nan((M,), torch.float32) for _ in range(passes)]
     torch.cuda.synchronize()
 
-    for r in range(rounds):
+    for r in range(passes):
         qb.qk_rmsnorm_fwd(X[r], w, Y1[r], R1[r], M, N, EPS, code)    # a: reads X
         qb.qk_softmax_fwd(Y1[r], S2[r], M, N, code)                  # b: reads a's output
         qb.qk_softmax_fwd(Z[r], X[r], M, N, code)                    # c: overwrites what a read
@@ -67,8 +67,8 @@ def test_dependent_calls_on_one_stream(dtype, M, N):
     assert qb.qk_get_device_status() == qb.QK_OK
 
     w_cpu, b_cpu = inp[0]["w"], inp[0]["b"]
-    for r in range(rounds):
-        what = f"round {r} {dtype} {M}x{N}"
+    for r in range(passes):
+        what = f"pass {r} {dtype} {M}x{N}"
         check_against_oracle("rmsnorm", dtype, {"x": inp[r]["x"], "w": w_cpu},
                              {"y": Y1[r], "rstd": R1[r]}, what="a " + what)
         check_against_oracle("softmax", dtype, {"x": Y1[r].cpu()}, {"y": S2[r]}, what="b " + what)
