@@ -10,6 +10,12 @@ at any size:
   RMSNorm   rstd finite, 0 < rstd <= eps^-1/2, mean_j (y_ij / w_j)^2 = ms_i/(ms_i+eps) ~ 1;
   x-entropy lse finite and in [max_j x_ij, max_j x_ij + ln N], loss = lse - x_t >= 0.
 Outputs start as NaN, so a row the kernels never wrote fails.
+
+The backward workloads bench.py times, and the backward passes at the
+sweep's largest shape (2^33 elements), are checked the same way: dx on 256
+seeded rows against the oracle (each row of dx depends on its own row only),
+every row finite, and RMSNorm's dw, a sum over every row, against the same
+sum taken in float64 by PyTorch in blocks of rows.
 """
 import math
 
@@ -17,8 +23,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+import test_backward as tb
 from memory_bound_row_rmsnorm_gb300 import binding as qb
 from memory_bound_row_rmsnorm_gb300 import synthetic as syn
+from parity import check_scaled, to_f64
 from test_parity import DEV, DT_CODE, EPS, check_against_oracle, run_gpu
 
 pytestmark = pytest.mark.gpu
@@ -118,3 +127,53 @@ def test_sweep_grid(op, dtype, N):
 def test_sweep_largest_rows(M):
     """The largest M of the sweep at its longest row (up to 64 GiB moved)."""
     check_workload("softmax", "f32", M, syn.SWEEP_N[-1], 1.0, seed=3000 + M)
+
+
+def check_backward_workload(op, dtype, M, N, sigma, seed):
+    """One backward call at full size on the device (the saved forward
+    quantities are the generators' stand-ins of the right range), checked on
+    sampled rows against the oracle, every row for finiteness, and RMSNorm's
+    dw over all rows against a float64 column sum."""
+    base = op[:-len("_bwd")]
+    case = syn.make_inputs(op, dtype, M, N, seed, DEV, sigma)
+    out = tb.run_gpu(base, dtype, case)
+    dx = out["dx"]
+    for r0 in range(0, M, 1024):
+        assert torch.isfinite(dx[r0:r0 + 1024]).all(), f"{op} {M}x{N}: non-finite dx near row {r0}"
+    idx = sample_rows(M, seed).to(DEV)
+    rows = {k: (v.index_select(0, idx) if v.dim() == 2 or k in ("rstd", "lse", "dloss", "targets") else v).cpu()
+            for k, v in case.items()}
+    what = f"{op} {dtype} {M}x{N} sampled rows"
+    got = dx.index_select(0, idx)
+    if base in ("softmax", "xent"):
+        tb.check(base, dtype, rows, {"dx": got}, what)
+    else:
+        x, w, r, dy = (to_f64(rows[k]) for k in ("x", "w", "rstd", "dy"))
+        ref_dx, _ = oracle.rmsnorm_bwd(x, w, r, dy)  # dx rows are row-local; the dw of these rows is not dw
+        r2 = r[:, None]
+        scale = r2 * np.abs(dy) * w + np.abs(x) * r2 ** 3 * np.sum(np.abs(dy * w * x), axis=1, keepdims=True) / N
+        check_scaled(to_f64(got), ref_dx, scale, dtype, f"rmsnorm bwd dx {what}")
+        dw = torch.zeros(N, dtype=torch.float64, device=DEV)
+        dws = torch.zeros(N, dtype=torch.float64, device=DEV)
+        for r0 in range(0, M, 1024):
+            t = case["dy"][r0:r0 + 1024].double() * case["x"][r0:r0 + 1024].double()
+            t *= case["rstd"][r0:r0 + 1024].double()[:, None]
+            dw += t.sum(0)
+            dws += t.abs().sum(0)
+            del t
+        check_scaled(to_f64(out["dw"]), dw.cpu().numpy(), dws.cpu().numpy(), "f32", f"rmsnorm bwd dw {op} {M}x{N}")
+    del case, out, dx
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", sorted(syn.BWD_WORKLOADS))
+def test_backward_workload(name):
+    op, dtype, M, N, sigma = syn.BWD_WORKLOADS[name]
+    check_backward_workload(op, dtype, M, N, sigma, seed=1100)
+
+
+@pytest.mark.parametrize("op", ["softmax_bwd", "rmsnorm_bwd", "xent_bwd"])
+def test_backward_largest_sweep_shape(op):
+    """The sweep's largest backward shape, bf16 32768 x 262144: 2^33 elements
+    (16 GiB a matrix), so element offsets pass 2^32."""
+    check_backward_workload(op, "bf16", syn.SWEEP_M[-1], syn.SWEEP_N[-1], 1.0, seed=3300)
