@@ -215,21 +215,38 @@ def test_tensor_helper():
     check(inp, {"y": y2, "mean": None, "rstd": None}, "bf16", bias=False, what="no bias")
 
 
-def test_benchmark_workload_sampled_rows():
-    """The benchmark's LayerNorm workload at full size, default plan: 64 rows
-    against the oracle, and every row's statistics checked for sanity."""
+def check_rows(inp, out, dtype, idx, what):
+    inp_rows = {"x": inp["x"].index_select(0, idx).cpu(), "w": inp["w"].cpu(), "b": inp["b"].cpu()}
+    out_rows = {k: v.index_select(0, idx) for k, v in out.items()}
+    check(inp_rows, out_rows, dtype, what=what)
+
+
+def test_benchmark_workload_every_row():
+    """The benchmark's LayerNorm workload at full size (2^26 elements), default
+    plan: every row against the oracle, in blocks of rows."""
     M, N = 16384, 4096
     inp = syn.make_inputs("layernorm", "bf16", M, N, 1900, DEV)
     out = run_gpu(inp, "bf16")
-    rng = np.random.default_rng(1900)
-    rows = torch.tensor(sorted(set(rng.choice(M, 62, replace=False).tolist()) | {0, M - 1}))
-    idx = rows.to(DEV)
-    inp_rows = {"x": inp["x"].index_select(0, idx).cpu(), "w": inp["w"].cpu(), "b": inp["b"].cpu()}
-    out_rows = {k: v.index_select(0, idx) for k, v in out.items()}
-    check(inp_rows, out_rows, "bf16", what=f"{M}x{N} sampled rows")
-    assert torch.isfinite(out["y"]).all()
+    for r0 in range(0, M, 1024):
+        check_rows(inp, out, "bf16", torch.arange(r0, r0 + 1024, device=DEV), f"{M}x{N} rows {r0}+")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_largest_sweep_shape_sampled_rows(dtype):
+    """32768 rows of 262144 (1 MiB fp32 rows on clusters of 16; 2^33 elements):
+    256 seeded rows against the oracle, every row's statistics for sanity."""
+    M, N = 32768, 262144
+    inp = syn.make_inputs("layernorm", dtype, M, N, 1950, DEV)
+    out = run_gpu(inp, dtype)
+    rng = np.random.default_rng(1950)
+    rows = torch.tensor(sorted(set(rng.choice(M, 254, replace=False).tolist()) | {0, M - 1}))
+    check_rows(inp, out, dtype, rows.to(DEV), f"{M}x{N} sampled rows")
+    for r0 in range(0, M, 1024):
+        assert torch.isfinite(out["y"][r0:r0 + 1024]).all()
     assert (out["mean"].abs() <= 1.5).all()            # row offsets are in [-1, 1]
     assert ((out["rstd"] > 0.8) & (out["rstd"] < 1.25)).all()  # unit variance rows
+    del inp, out
+    torch.cuda.empty_cache()
 
 
 # Rows longer than a cluster holds stream through shared memory twice; the

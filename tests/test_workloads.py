@@ -129,6 +129,14 @@ def test_sweep_largest_rows(M):
     check_workload("softmax", "f32", M, syn.SWEEP_N[-1], 1.0, seed=3000 + M)
 
 
+@pytest.mark.parametrize("op,dtype", [("rmsnorm", "f32"), ("rmsnorm", "bf16"), ("xent", "f32"), ("xent", "bf16"),
+                                      ("softmax", "bf16")])
+def test_sweep_largest_shape(op, dtype):
+    """The sweep's largest shape, 32768 x 262144 (2^33 elements, element
+    offsets past 2^32), for the other operators and dtypes."""
+    check_workload(op, dtype, syn.SWEEP_M[-1], syn.SWEEP_N[-1], 1.0, seed=3100)
+
+
 def check_backward_workload(op, dtype, M, N, sigma, seed):
     """One backward call at full size on the device (the saved forward
     quantities are the generators' stand-ins of the right range), checked on
