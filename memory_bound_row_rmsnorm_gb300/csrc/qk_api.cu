@@ -406,6 +406,11 @@ SlotBands slot_bands(int op) {
 // backward bf16 1024 x 4096: 81 % on the full grid, 67 % balanced); at 9
 // items per CTA and more the table's ring was as good or better.
 constexpr int kBwdDeepRingItems = 8;
+// Forward launches of fewer than this many items per resident CTA (after the
+// rules above) take a third ring slot even when that costs up to a third of
+// the resident CTAs: with so few items every CTA's loads are in flight at once
+// anyway, and the deeper ring keeps all of them in flight.
+constexpr int kVeryShortItems = 2;
 
 // Alternative kernels for short launches (fewer than 8 items per resident CTA
 // of the table's plan):
@@ -551,6 +556,19 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
       occ = occ_s;  // unclustered here: the grid below follows the new residency
       ctas_per_sm = occ_s;
       break;
+    }
+  }
+  // A forward launch of fewer than two items per resident CTA: a third slot
+  // even at the cost of up to a third of the resident CTAs (see kVeryShortItems).
+  if (short_ok && !bwd && slots < 3 && p->num_items < kVeryShortItems * int64_t(occ) * d.sms) {
+    const int64_t smem_s = kSmemHeader + int64_t(3) * nin * slot_bytes + param_bytes;
+    int occ_s = 0;
+    if (smem_s <= d.smem_optin && occupancy(dev, *ke, int(smem_s), 0, &occ_s) == QK_OK &&
+        3 * occ_s >= 2 * occ && occ_s > 0) {
+      slots = 3;
+      smem_used = smem_s;
+      occ = occ_s;
+      ctas_per_sm = occ_s;
     }
   }
 

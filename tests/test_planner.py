@@ -4,7 +4,8 @@ plans those rules pick against the oracle:
   * a one-chunk, unclustered launch of few items per resident CTA gets a
     deeper ring: RMSNorm and LayerNorm three slots below 8 items per CTA,
     softmax three below 4 and two below 8, the others three below 4 -- and
-    never at the cost of a resident CTA;
+    never at the cost of a resident CTA, except below two items per resident
+    CTA, where a third slot may cost up to a third of them;
   * fp32 softmax rows of 4096 switch to 128-thread CTAs of 8 vectors a thread
     below 8 items per resident CTA; cross-entropy rows of 512 vectors to two
     64-thread rows per CTA below 4;
@@ -60,6 +61,10 @@ def test_ring_depth_follows_items_per_cta(op, dtype, N):
     long_ = plan(op, dtype, 1 << 20, N)  # many items per CTA: the table's slots
     for M in (256, 1024, 4096, 16384, 65536):
         p = plan(op, dtype, M, N)
+        ipc = items(p, M) / resident(long_)
+        if ipc < 2:  # very short: three slots, at most a third of the CTAs lost
+            assert p["slots"] >= 3 and 3 * p["ctas_per_sm"] >= 2 * long_["ctas_per_sm"], (M, p, long_)
+            continue
         assert p["ctas_per_sm"] == long_["ctas_per_sm"], "a deeper ring never costs a resident CTA"
         ipc = items(p, M) / resident(p)
         t3, t2 = (8, 0) if op in ("rmsnorm", "layernorm") else (4, 8)
@@ -141,3 +146,15 @@ def test_the_chosen_backward_plans_match_the_oracle(op, dtype, M, N):
     case = tb.make_case(op, dtype, M, N, 14000 + M)
     out = tb.run_gpu(op, dtype, case)
     tb.check(op, dtype, case, out, f"planner {op} bwd {dtype} {M}x{N}")
+
+
+@pytest.mark.parametrize("op,dtype,M,N", [("xent", "f32", 1024, 4096), ("xent", "bf16", 2048, 4096),
+                                          ("xent", "f32", 16384, 256), ("softmax", "f32", 2048, 2048)])
+def test_very_short_forward_launches_take_three_slots(op, dtype, M, N):
+    """Below two items per resident CTA a forward launch runs a ring of three
+    slots; its results against the oracle on every row."""
+    p = plan(op, dtype, M, N)
+    assert p["slots"] == 3, p
+    inp = syn.make_inputs(op, dtype, M, N, 15000 + M, "cpu")
+    out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, dtype)
+    check_against_oracle(op, dtype, inp, out, what=f"very short {op} {dtype} {M}x{N}")
