@@ -412,23 +412,33 @@ constexpr int kBwdDeepRingItems = 8;
 // anyway, and the deeper ring keeps all of them in flight.
 constexpr int kVeryShortItems = 2;
 
-// Alternative kernels for short launches (fewer than 8 items per resident CTA
-// of the table's plan):
-//  * fp32 softmax rows of 4096 elements in 128-thread CTAs of 8 vectors a
-//    thread, with 3 ring slots below 4 items per CTA and 2 above (1024 x 4096:
-//    86 % -> 88 %; 4096 x 4096: 90 % -> 92 %); the 256 x 4 plan beats it by
-//    1-2 points from 8192 rows on;
-//  * cross-entropy rows of 512 vectors below 4 items per CTA: two 64-thread
-//    rows of 8 vectors a thread per 128-thread CTA, six CTAs per SM (bf16
-//    2048 x 4096: 36 % -> 53 %, 4096 x 4096 64 % -> 68 %; fp32 2048 x 2048
-//    40 % -> 56 %).
-bool short_alternative(int op, int dt, int64_t NV, bool very_short, Choice* c) {
-  if (op == kSoftmax && dt == QK_F32 && NV > 512 && NV <= 1024) {
+// Alternative kernels for short launches, by items per resident CTA of the
+// table's plan (ipc):
+//  * fp32 softmax rows of 4096 elements below 8: 128-thread CTAs of 8 vectors
+//    a thread, with 3 ring slots below 4 and 2 above (1024 x 4096: 86 % ->
+//    88 %; 4096 x 4096: 90 % -> 92 %); the 256 x 4 plan beats it by 1-2
+//    points from 8192 rows on;
+//  * cross-entropy rows of 512 vectors below 4: two 64-thread rows of 8
+//    vectors a thread per 128-thread CTA, six CTAs per SM (bf16 2048 x 4096:
+//    36 % -> 53 %, 4096 x 4096 64 % -> 68 %; fp32 2048 x 2048 40 % -> 56 %);
+//  * RMSNorm rows of 512 vectors (bf16 4096, fp32 2048 elements) from 4 to
+//    12: four 64-thread rows of 8 vectors a thread per 256-thread CTA, three
+//    slots, two CTAs per SM (bf16 8192 x 4096: 89 % -> 97 %, 10240 x 4096
+//    90 % -> 96 %; fp32 10240 x 2048 91 % -> 97 %); below 4 and from about
+//    16 on the table's 128-thread plan measured as good or better.
+constexpr int kShortAltMaxItems = 12;
+bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
+  const bool very_short = items < 4 * resident;
+  if (op == kSoftmax && dt == QK_F32 && NV > 512 && NV <= 1024 && items < 8 * resident) {
     *c = Choice{1024, 128, 128, 8, 1, very_short ? 3 : 2};
     return true;
   }
   if (op == kXent && NV > 256 && NV <= 512 && very_short) {
     *c = Choice{512, 128, 64, 8, 1, 2};
+    return true;
+  }
+  if (op == kRmsNorm && NV > 256 && NV <= 512 && !very_short) {
+    *c = Choice{512, 256, 64, 8, 1, 3};
     return true;
   }
   return false;
@@ -531,9 +541,9 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   // 16384 x 1024: 90 % -> 98 %.)
   const bool short_ok = !ov.on && !two_pass && k == 1 && cl == 1;
   const int64_t resident = ctas_per_sm * d.sms;
-  if (short_ok && alt == nullptr && p->num_items < 8 * resident) {
+  if (short_ok && alt == nullptr && p->num_items < kShortAltMaxItems * resident) {
     Choice c;
-    if (short_alternative(op, dt, NV, p->num_items < 4 * resident, &c) &&
+    if (short_alternative(op, dt, NV, p->num_items, resident, &c) &&
         !(c.threads == th && c.row_threads == tpr && c.vec_per_thread == vpt))
       return plan_ring(dev, d, op, dt, M, N, p, &c);  // its slots as given
   }
