@@ -421,11 +421,12 @@ constexpr int kVeryShortItems = 2;
 //  * cross-entropy rows of 512 vectors below 4: two 64-thread rows of 8
 //    vectors a thread per 128-thread CTA, six CTAs per SM (bf16 2048 x 4096:
 //    36 % -> 53 %, 4096 x 4096 64 % -> 68 %; fp32 2048 x 2048 40 % -> 56 %);
-//  * RMSNorm rows of 512 vectors (bf16 4096, fp32 2048 elements) from 4 to
-//    12: four 64-thread rows of 8 vectors a thread per 256-thread CTA, three
-//    slots, two CTAs per SM (bf16 8192 x 4096: 89 % -> 97 %, 10240 x 4096
-//    90 % -> 96 %; fp32 10240 x 2048 91 % -> 97 %); below 4 and from about
-//    16 on the table's 128-thread plan measured as good or better.
+//  * RMSNorm (softmax) rows of 512 vectors (bf16 4096, fp32 2048 elements)
+//    from 4 to 12 (10): four 64-thread rows of 8 vectors a thread per
+//    256-thread CTA, three slots, two CTAs per SM (RMSNorm bf16 8192 x 4096:
+//    89 % -> 95 %, fp32 10240 x 2048 89 % -> 96 %; softmax fp32 6144 x 2048
+//    91 % -> 101 %, bf16 8192 x 4096 89 % -> 94 %); below 4 and from about 16
+//    on the table's 128-thread plan measured as good or better.
 constexpr int kShortAltMaxItems = 12;
 bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
   const bool very_short = items < 4 * resident;
@@ -437,7 +438,8 @@ bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t reside
     *c = Choice{512, 128, 64, 8, 1, 2};
     return true;
   }
-  if (op == kRmsNorm && NV > 256 && NV <= 512 && !very_short) {
+  if ((op == kRmsNorm || (op == kSoftmax && items < 10 * resident)) && NV > 256 && NV <= 512 &&
+      !very_short) {
     *c = Choice{512, 256, 64, 8, 1, 3};
     return true;
   }

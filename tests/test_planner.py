@@ -13,9 +13,9 @@ plans those rules pick against the oracle:
     same number of items;
   * cross-entropy rows of 512 vectors otherwise run one warp a row, 16
     vectors a lane; bf16 softmax rows of 8192 elements 128 x 8 vectors;
-  * RMSNorm rows of 512 vectors (bf16 4096, fp32 2048 elements) at 4-12
-    items per resident CTA run four 64-thread rows per 256-thread CTA with
-    three slots;
+  * RMSNorm (softmax) rows of 512 vectors (bf16 4096, fp32 2048 elements)
+    at 4-12 (4-10) items per resident CTA run four 64-thread rows per
+    256-thread CTA with three slots;
   * a one-chunk, unclustered backward launch of fewer than 8 items per
     resident CTA takes a ring of three slots if that costs no resident CTA,
     else two if that costs at most one per SM; the passes with two inputs
@@ -163,22 +163,24 @@ def test_very_short_forward_launches_take_three_slots(op, dtype, M, N):
     check_against_oracle(op, dtype, inp, out, what=f"very short {op} {dtype} {M}x{N}")
 
 
-def test_rmsnorm_rows_of_512_vectors():
-    """Between 4 and 12 items per resident CTA of the table's 128-thread plan:
-    256-thread CTAs of four 64-thread rows, three slots; outside it the table's
-    plan; the chosen plans against the oracle on every row."""
+@pytest.mark.parametrize("op,top", [("rmsnorm", 12), ("softmax", 10)])
+def test_rows_of_512_vectors(op, top):
+    """Between 4 and 12 (softmax 10) items per resident CTA of the table's
+    128-thread plan: 256-thread CTAs of four 64-thread rows, three slots;
+    outside it the table's plan; the chosen plans against the oracle on every
+    row."""
     for dtype, N in (("bf16", 4096), ("f32", 2048)):
-        table = plan("rmsnorm", dtype, 1 << 20, N)
+        table = plan(op, dtype, 1 << 20, N)
         assert (table["threads"], table["row_threads"], table["vec_per_thread"]) == (128, 128, 4), table
         res = resident(table)
-        for M in (2048, 4096, 6144, 8192, 10240, 12288, 16384, 32768):
-            p = plan("rmsnorm", dtype, M, N)
-            alt = 4 * res <= M < 12 * res
+        for M in (2048, 4096, 6144, 8192, 10240, 12288, 14336, 16384, 32768):
+            p = plan(op, dtype, M, N)
+            alt = 4 * res <= M < top * res
             got = (p["threads"], p["row_threads"], p["vec_per_thread"])
             assert got == ((256, 64, 8) if alt else (128, 128, 4)), (dtype, M, p)
             if alt:
                 assert p["slots"] == 3, p
     for dtype, M, N in (("bf16", 8192, 4096), ("f32", 10000, 2048)):
-        inp = syn.make_inputs("rmsnorm", dtype, M, N, 16000 + M, "cpu")
-        out = run_gpu("rmsnorm", {k: v.to(DEV) for k, v in inp.items()}, dtype)
-        check_against_oracle("rmsnorm", dtype, inp, out, what=f"planner rmsnorm {dtype} {M}x{N}")
+        inp = syn.make_inputs(op, dtype, M, N, 16000 + M, "cpu")
+        out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, dtype)
+        check_against_oracle(op, dtype, inp, out, what=f"planner {op} {dtype} {M}x{N}")
