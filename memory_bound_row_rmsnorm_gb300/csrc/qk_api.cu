@@ -251,13 +251,15 @@ const Choice kRmsNormTable[] = {
 // LayerNorm: from a sweep of every compiled configuration on GB300 (M = 16384,
 // N = 256 ... 262144, fp32 and bf16; rows of 512 and 2048 vectors again at
 // 8192-32768 rows).  Its parameters not held in registers take shared memory,
-// so long rows keep fewer ring slots than RMSNorm.  This table is bf16's; a
-// later sweep of 1-4 slots at 8192-32768 rows deepened its rows of 8192
-// elements to two slots (83-88 % -> 88-91 %) and of 16384 to three (94-97 %
-// -> 97-98 %).
+// so long rows keep fewer ring slots than RMSNorm.  This table is bf16's;
+// later sweeps at 4096-32768 rows deepened its rows of 16384 elements to
+// three slots (94-97 % -> 97-98 %), moved its rows of 8192 to 256-thread CTAs
+// of 4 vectors a thread with two slots (88-92 % -> 91-97 % from 6144 rows on)
+// and its rows of 2048 to four 64-thread rows per CTA with three slots
+// (64-91 % -> 63-93 %, +7 at 6144-8192 rows).
 const Choice kLayerNormTable[] = {
     {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 2},       {128, 256, 32, 4, 1, 2},
-    {256, 256, 32, 8, 1, 3},     {512, 256, 128, 4, 1, 2},     {1024, 128, 128, 8, 1, 2},
+    {256, 256, 64, 4, 1, 3},     {512, 256, 128, 4, 1, 2},     {1024, 256, 256, 4, 1, 2},
     {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 8, 8, 2},  {32768, 512, 512, 8, 8, 1},   {65536, 512, 512, 8, 16, 2},
 };
