@@ -323,9 +323,13 @@ const Choice kRmsNormBwdBf16Table[] = {
     {2048, 256, 256, 4, 2, 2}, {4096, 512, 512, 4, 2, 2}, {8192, 512, 512, 4, 4, 2},
     {16384, 512, 512, 4, 8, 2}, {32768, 512, 512, 4, 16, 2},
 };
+// Cross-entropy backward rows of 256 vectors (fp32 1024, bf16 2048 elements):
+// eight 32-thread rows of 8 vectors a thread per CTA, three slots (a row group
+// of 128 threads held twice the row: +4 to +18 points at 2048-16384 rows,
+// within a point from 24576 on).
 const Choice kXentBwdTable[] = {
     {32, 256, 8, 4, 1, 1},     {64, 256, 16, 4, 1, 2},    {128, 256, 32, 4, 1, 2},
-    {256, 128, 128, 4, 1, 2},  {512, 128, 128, 4, 1, 1},  {1024, 256, 256, 4, 1, 1},
+    {256, 256, 32, 8, 1, 3},   {512, 128, 128, 4, 1, 1},  {1024, 256, 256, 4, 1, 1},
     {2048, 256, 256, 8, 1, 1}, {kStream, 256, 256, 8, 1, 1},  // 32 KB chunks
 };
 
@@ -423,13 +427,18 @@ constexpr int kVeryShortItems = 2;
 //  * cross-entropy rows of 512 vectors below 4: two 64-thread rows of 8
 //    vectors a thread per 128-thread CTA, six CTAs per SM (bf16 2048 x 4096:
 //    36 % -> 53 %, 4096 x 4096 64 % -> 68 %; fp32 2048 x 2048 40 % -> 56 %);
+//  * backward passes (table plans tuned at 16384 rows and more): softmax
+//    rows of 256 vectors below 20, four 64-thread rows of 4 vectors a thread
+//    per CTA (+1 to +7 points at 2048-16384 rows); cross-entropy rows of 512
+//    vectors from 4 to 10, four 64-thread rows of 8 vectors a thread, three
+//    slots (+1 to +8 points at 6144-12288 rows);
 //  * RMSNorm (softmax) rows of 512 vectors (bf16 4096, fp32 2048 elements)
 //    from 4 to 12 (10): four 64-thread rows of 8 vectors a thread per
 //    256-thread CTA, three slots, two CTAs per SM (RMSNorm bf16 8192 x 4096:
 //    89 % -> 95 %, fp32 10240 x 2048 89 % -> 96 %; softmax fp32 6144 x 2048
 //    91 % -> 101 %, bf16 8192 x 4096 89 % -> 94 %); below 4 and from about 16
 //    on the table's 128-thread plan measured as good or better.
-constexpr int kShortAltMaxItems = 12;
+constexpr int kShortAltMaxItems = 20;
 bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
   const bool very_short = items < 4 * resident;
   if (op == kSoftmax && dt == QK_F32 && NV > 512 && NV <= 1024 && items < 8 * resident) {
@@ -440,8 +449,16 @@ bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t reside
     *c = Choice{512, 128, 64, 8, 1, 2};
     return true;
   }
-  if ((op == kRmsNorm || (op == kSoftmax && items < 10 * resident)) && NV > 256 && NV <= 512 &&
-      !very_short) {
+  if (op == kOpSoftmaxBwd && NV > 128 && NV <= 256) {
+    *c = Choice{256, 256, 64, 4, 1, items < 8 * resident ? 3 : 2};
+    return true;
+  }
+  if (op == kOpXentBwd && NV > 256 && NV <= 512 && !very_short && items < 10 * resident) {
+    *c = Choice{512, 256, 64, 8, 1, 3};
+    return true;
+  }
+  if (((op == kRmsNorm && items < 12 * resident) || (op == kSoftmax && items < 10 * resident)) &&
+      NV > 256 && NV <= 512 && !very_short) {
     *c = Choice{512, 256, 64, 8, 1, 3};
     return true;
   }
