@@ -243,7 +243,7 @@ struct Choice {
 };
 constexpr int64_t kStream = INT64_MAX;  // cross-entropy: any longer row is streamed
 const Choice kRmsNormTable[] = {
-    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 3},       {128, 256, 32, 4, 1, 2},
+    {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 3},       {128, 256, 32, 4, 1, 2},
     {256, 256, 64, 4, 1, 2},     {512, 128, 128, 4, 1, 1},     {1024, 128, 128, 8, 1, 1},
     {2048, 256, 256, 8, 1, 1},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 1},
     {16384, 256, 256, 8, 8, 3},  {32768, 256, 256, 8, 16, 2},  {65536, 512, 512, 8, 16, 2},
@@ -272,8 +272,11 @@ const Choice kLayerNormF32Table[] = {
     {2048, 512, 512, 4, 1, 2},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 8, 8, 2},  {32768, 256, 256, 8, 16, 2},  {65536, 512, 512, 8, 16, 2},
 };
+// Rows of 64 vectors (fp32 256, bf16 512 elements), RMSNorm and softmax:
+// sixteen 16-thread rows of 4 vectors a thread per CTA, three slots
+// (89-91 % -> 96-101 % at 24576-32768 rows, against eight 32-thread rows).
 const Choice kSoftmaxTable[] = {
-    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 3},       {128, 256, 32, 4, 1, 3},
+    {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 3},       {128, 256, 32, 4, 1, 3},
     {256, 256, 64, 4, 1, 2},     {512, 128, 128, 4, 1, 1},     {1024, 256, 256, 4, 1, 1},
     {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 16, 4, 2},  {32768, 256, 256, 16, 8, 1},  {65536, 256, 256, 16, 16, 1},
@@ -282,7 +285,7 @@ const Choice kSoftmaxTable[] = {
 // 8 vectors a thread, which keep four CTAs per SM where 256 x 4 keeps three
 // (85-98 % of peak against 80-90 % at 2048-32768 rows).
 const Choice kSoftmaxBf16Table[] = {
-    {32, 256, 8, 4, 1, 2},       {64, 256, 32, 2, 1, 3},       {128, 256, 32, 4, 1, 3},
+    {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 3},       {128, 256, 32, 4, 1, 3},
     {256, 256, 64, 4, 1, 2},     {512, 128, 128, 4, 1, 1},     {1024, 128, 128, 8, 1, 1},
     {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 16, 4, 2},  {32768, 256, 256, 16, 8, 1},  {65536, 256, 256, 16, 16, 1},
@@ -437,7 +440,17 @@ constexpr int kVeryShortItems = 2;
 //    256-thread CTA, three slots, two CTAs per SM (RMSNorm bf16 8192 x 4096:
 //    89 % -> 95 %, fp32 10240 x 2048 89 % -> 96 %; softmax fp32 6144 x 2048
 //    91 % -> 101 %, bf16 8192 x 4096 89 % -> 94 %); below 4 and from about 16
-//    on the table's 128-thread plan measured as good or better.
+//    on the table's 128-thread plan measured as good or better;
+//  * RMSNorm and softmax rows of 64 vectors (fp32 256, bf16 512 elements)
+//    below 1.5: eight 32-thread rows per CTA, three slots.  The table's
+//    sixteen-row CTAs halve the items, so in so short a launch the SMs' shares
+//    of the grid come out uneven (RMSNorm fp32 8192 x 256: 66 % eight-row,
+//    61 % sixteen-row); from 12288 rows on the sixteen-row plan is ahead
+//    (RMSNorm bf16 12288 x 512: 65 % -> 80 %, fp32 24576 x 256: 90 % -> 97 %);
+//  * fp32 LayerNorm rows of 128 vectors (512 elements) from 2 to 16: sixteen
+//    16-thread rows of 8 vectors a thread per CTA, three slots (8192 x 512:
+//    69 % -> 76 %, 24576 x 512: 87 % -> 100 %); at 65536 rows the table's
+//    plan measured 4 points ahead.
 constexpr int kShortAltMaxItems = 20;
 bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
   const bool very_short = items < 4 * resident;
@@ -460,6 +473,15 @@ bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t reside
   if (((op == kRmsNorm && items < 12 * resident) || (op == kSoftmax && items < 10 * resident)) &&
       NV > 256 && NV <= 512 && !very_short) {
     *c = Choice{512, 256, 64, 8, 1, 3};
+    return true;
+  }
+  if (2 * items < 3 * resident && (op == kRmsNorm || op == kSoftmax) && NV > 32 && NV <= 64) {
+    *c = Choice{64, 256, 32, 2, 1, 3};
+    return true;
+  }
+  if (op == kOpLayerNorm && dt == QK_F32 && NV > 64 && NV <= 128 && items >= 2 * resident &&
+      items < 16 * resident) {
+    *c = Choice{128, 256, 16, 8, 1, 3};
     return true;
   }
   return false;

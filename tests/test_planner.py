@@ -16,6 +16,10 @@ plans those rules pick against the oracle:
   * RMSNorm (softmax) rows of 512 vectors (bf16 4096, fp32 2048 elements)
     at 4-12 (4-10) items per resident CTA run four 64-thread rows per
     256-thread CTA with three slots;
+  * RMSNorm and softmax rows of 64 vectors run sixteen rows per CTA from 1.5
+    items per resident CTA on, eight below; fp32 LayerNorm rows of 128 run
+    sixteen rows per CTA from 2 to 16 items per resident CTA of the table's
+    eight-row plan;
   * a one-chunk, unclustered backward launch of fewer than 8 items per
     resident CTA takes a ring of three slots if that costs no resident CTA,
     else two if that costs at most one per SM; the passes with two inputs
@@ -24,6 +28,7 @@ import pytest
 import torch
 
 import test_backward as tb
+import test_layernorm as tl
 from memory_bound_row_rmsnorm_gb300 import binding as qb
 from memory_bound_row_rmsnorm_gb300 import synthetic as syn
 from test_parity import DEV, check_against_oracle, run_gpu
@@ -184,3 +189,43 @@ def test_rows_of_512_vectors(op, top):
         inp = syn.make_inputs(op, dtype, M, N, 16000 + M, "cpu")
         out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, dtype)
         check_against_oracle(op, dtype, inp, out, what=f"planner {op} {dtype} {M}x{N}")
+
+
+@pytest.mark.parametrize("op,dtype,N", [("rmsnorm", "f32", 256), ("rmsnorm", "bf16", 512),
+                                        ("softmax", "f32", 256), ("softmax", "bf16", 512)])
+def test_short_rows_of_sixteen_row_ctas(op, dtype, N):
+    """Rows of 64 vectors: the table's CTAs of sixteen 16-thread rows from 1.5
+    items per resident CTA on, eight 32-thread rows below; three slots either
+    way; the plans on both sides of the switch against the oracle on every
+    row."""
+    table = plan(op, dtype, 1 << 20, N)
+    assert (table["threads"], table["row_threads"], table["vec_per_thread"]) == (256, 16, 4), table
+    res = resident(table)
+    for M in (1024, 4096, 8192, 12288, 16384, 32768, 65536):
+        p = plan(op, dtype, M, N)
+        got = (p["threads"], p["row_threads"], p["vec_per_thread"])
+        assert got == ((256, 32, 2) if 2 * -(-M // 16) < 3 * res else (256, 16, 4)), (M, p, res)
+        assert p["slots"] == 3, p
+    edge = 24 * res  # 1.5 items per resident CTA of sixteen rows
+    for M in (edge - 16 * 37 - 5, edge + 3):  # ragged: not a multiple of the rows per CTA
+        inp = syn.make_inputs(op, dtype, M, N, 17000 + M, "cpu")
+        out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, dtype)
+        check_against_oracle(op, dtype, inp, out, what=f"short rows {op} {dtype} {M}x{N}")
+
+
+def test_layernorm_f32_rows_of_128_vectors():
+    """fp32 LayerNorm rows of 512 elements: sixteen 16-thread rows of 8 vectors
+    a thread per CTA, three slots, from 2 to 16 items per resident CTA of the
+    table's eight-row plan; the table's plan outside."""
+    table = plan("layernorm", "f32", 1 << 20, 512)
+    assert (table["threads"], table["row_threads"], table["vec_per_thread"]) == (256, 32, 4), table
+    res = resident(table)
+    for M in (1024, 4096, 8192, 16384, 32768, 65536, 131072):
+        p = plan("layernorm", "f32", M, 512)
+        got = (p["threads"], p["row_threads"], p["vec_per_thread"])
+        alt = 2 * res <= -(-M // 8) < 16 * res
+        assert got == ((256, 16, 8) if alt else (256, 32, 4)), (M, p, res)
+        if alt:
+            assert p["slots"] == 3, p
+    for M in (16 * res - 9, 16 * res + 5, 128 * res - 9):  # both sides of the lower edge, ragged
+        tl.full_check("f32", M, 512, 18000 + M, what=f"planner layernorm f32 {M}x512")
