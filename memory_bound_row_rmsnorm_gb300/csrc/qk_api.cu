@@ -640,8 +640,13 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   // two rows rather than 608 of one or two, 86 % -> 87 %; cross-entropy
   // backward fp32 1024 x 4096 +2 points).  At three or more items per CTA the
   // full grid measured better, and so it did for the backward passes that
-  // load two matrices per item (softmax, RMSNorm; see kBwdDeepRingItems).
-  if (short_ok && nin == 1 && p->num_items < 2 * units) {
+  // load two matrices per item (softmax, RMSNorm; see kBwdDeepRingItems) and
+  // for softmax, RMSNorm and LayerNorm CTAs of several rows, whose shrunken
+  // grid leaves some SMs one CTA and others two (same-GPU A/B: +4 to +11
+  // points, softmax bf16 4096 x 1024 52 % -> 63 %; cross-entropy, forward and
+  // backward, measured 1-3 points better with even shares).
+  const bool rows_per_cta = th > tpr && (op == kSoftmax || op == kRmsNorm || op == kOpLayerNorm);
+  if (short_ok && nin == 1 && !rows_per_cta && p->num_items < 2 * units) {
     const int64_t per = (p->num_items + units - 1) / units;
     units = (p->num_items + per - 1) / per;
   }

@@ -10,7 +10,8 @@ plans those rules pick against the oracle:
     below 8 items per resident CTA; cross-entropy rows of 512 vectors to two
     64-thread rows per CTA below 4;
   * a launch of fewer than two items per resident CTA gives every CTA the
-    same number of items;
+    same number of items, except softmax, RMSNorm and LayerNorm CTAs of
+    several rows, which keep the full grid;
   * cross-entropy rows of 512 vectors otherwise run one warp a row, 16
     vectors a lane; bf16 softmax rows of 8192 elements 128 x 8 vectors;
   * RMSNorm (softmax) rows of 512 vectors (bf16 4096, fp32 2048 elements)
@@ -98,6 +99,15 @@ def test_short_launches_give_every_cta_the_same_items():
     assert 1024 % p["grid"] == 0 and 1024 // p["grid"] == 2, p
     q = plan("softmax", "f32", 2048, 4096)  # three or more items per CTA: the full grid
     assert q["grid"] == resident(q), q
+    r = plan("rmsnorm", "bf16", 16384, 256)  # CTAs of 32 rows: the full grid
+    n = items(r, 16384)
+    assert r["threads"] > r["row_threads"] and n < 2 * resident(r), r
+    assert r["grid"] == min(n, resident(r)), r
+    x = plan("xent", "bf16", 16384, 256)  # cross-entropy keeps even shares
+    n = items(x, 16384)
+    assert x["threads"] > x["row_threads"] and n < 2 * resident(x), x
+    per = -(-n // min(n, resident(x)))
+    assert x["grid"] == -(-n // per), x
 
 
 def test_cross_entropy_rows_of_512_vectors():
