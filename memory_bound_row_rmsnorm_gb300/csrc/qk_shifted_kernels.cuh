@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         for (int e = 0; e < E; ++e) o[e] = (exp2_approx(fmaf(f[e], kLog2e, -g_lb)) * g_zf) * g_gv;
         unsigned char* dst = yb + (F0 + i0) * ES;  // 16-byte aligned: dlogits has the logits' alignment
         if (lo == 0 && hi == E) {
-          *reinterpret_cast<uint4*>(dst) = V::pack(o);
+          __stcs(reinterpret_cast<uint4*>(dst), V::pack(o));
         } else {
 #pragma unroll
           for (int e = 0; e < E; ++e)
@@ -702,7 +702,7 @@ __global__ void __launch_bounds__(THREADS, (shifted_min_blocks<OP, VPT>()))
         }
         unsigned char* dst = yb + (F0 + i0) * ES;  // 16-byte aligned: y has x's alignment
         if (lo == 0 && hi == E) {
-          *reinterpret_cast<uint4*>(dst) = V::pack(o);
+          __stcs(reinterpret_cast<uint4*>(dst), V::pack(o));
         } else {
 #pragma unroll
           for (int e = 0; e < E; ++e)
