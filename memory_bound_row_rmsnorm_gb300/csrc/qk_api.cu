@@ -452,36 +452,32 @@ constexpr int kVeryShortItems = 2;
 //    69 % -> 76 %, 24576 x 512: 87 % -> 100 %); at 65536 rows the table's
 //    plan measured 4 points ahead.
 constexpr int kShortAltMaxItems = 20;
+// One row of those rules: operator, dtype (-1: both), rows of (nv_lo, nv_hi]
+// vectors, a window [ipc_lo2, ipc_hi2) on 2 * ipc, the plan, and 2 * ipc below
+// which it takes three ring slots instead of its own count (0: never).
+struct ShortAlt {
+  int op, dt;
+  int64_t nv_lo, nv_hi;
+  int ipc_lo2, ipc_hi2, deep_below2;
+  Choice c;
+};
+const ShortAlt kShortAlts[] = {
+    {kSoftmax, QK_F32, 512, 1024, 0, 16, 8, {1024, 128, 128, 8, 1, 2}},
+    {kXent, -1, 256, 512, 0, 8, 0, {512, 128, 64, 8, 1, 2}},
+    {kOpSoftmaxBwd, -1, 128, 256, 0, 2 * kShortAltMaxItems, 16, {256, 256, 64, 4, 1, 2}},
+    {kOpXentBwd, -1, 256, 512, 8, 20, 0, {512, 256, 64, 8, 1, 3}},
+    {kRmsNorm, -1, 256, 512, 8, 24, 0, {512, 256, 64, 8, 1, 3}},
+    {kSoftmax, -1, 256, 512, 8, 20, 0, {512, 256, 64, 8, 1, 3}},
+    {kRmsNorm, -1, 32, 64, 0, 3, 0, {64, 256, 32, 2, 1, 3}},
+    {kSoftmax, -1, 32, 64, 0, 3, 0, {64, 256, 32, 2, 1, 3}},
+    {kOpLayerNorm, QK_F32, 64, 128, 4, 32, 0, {128, 256, 16, 8, 1, 3}},
+};
 bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
-  const bool very_short = items < 4 * resident;
-  if (op == kSoftmax && dt == QK_F32 && NV > 512 && NV <= 1024 && items < 8 * resident) {
-    *c = Choice{1024, 128, 128, 8, 1, very_short ? 3 : 2};
-    return true;
-  }
-  if (op == kXent && NV > 256 && NV <= 512 && very_short) {
-    *c = Choice{512, 128, 64, 8, 1, 2};
-    return true;
-  }
-  if (op == kOpSoftmaxBwd && NV > 128 && NV <= 256) {
-    *c = Choice{256, 256, 64, 4, 1, items < 8 * resident ? 3 : 2};
-    return true;
-  }
-  if (op == kOpXentBwd && NV > 256 && NV <= 512 && !very_short && items < 10 * resident) {
-    *c = Choice{512, 256, 64, 8, 1, 3};
-    return true;
-  }
-  if (((op == kRmsNorm && items < 12 * resident) || (op == kSoftmax && items < 10 * resident)) &&
-      NV > 256 && NV <= 512 && !very_short) {
-    *c = Choice{512, 256, 64, 8, 1, 3};
-    return true;
-  }
-  if (2 * items < 3 * resident && (op == kRmsNorm || op == kSoftmax) && NV > 32 && NV <= 64) {
-    *c = Choice{64, 256, 32, 2, 1, 3};
-    return true;
-  }
-  if (op == kOpLayerNorm && dt == QK_F32 && NV > 64 && NV <= 128 && items >= 2 * resident &&
-      items < 16 * resident) {
-    *c = Choice{128, 256, 16, 8, 1, 3};
+  for (const ShortAlt& a : kShortAlts) {
+    if (a.op != op || (a.dt >= 0 && a.dt != dt) || NV <= a.nv_lo || NV > a.nv_hi) continue;
+    if (2 * items < a.ipc_lo2 * resident || 2 * items >= a.ipc_hi2 * resident) continue;
+    *c = a.c;
+    if (2 * items < a.deep_below2 * resident) c->slots = 3;
     return true;
   }
   return false;
