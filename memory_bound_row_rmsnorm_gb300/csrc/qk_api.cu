@@ -254,12 +254,14 @@ const Choice kRmsNormTable[] = {
 // so long rows keep fewer ring slots than RMSNorm.  This table is bf16's;
 // later sweeps at 4096-32768 rows deepened its rows of 16384 elements to
 // three slots (94-97 % -> 97-98 %), moved its rows of 8192 to 256-thread CTAs
-// of 4 vectors a thread with two slots (88-92 % -> 91-97 % from 6144 rows on)
-// and its rows of 2048 to four 64-thread rows per CTA with three slots
-// (64-91 % -> 63-93 %, +7 at 6144-8192 rows).
+// of 4 vectors a thread with two slots (88-92 % -> 91-97 % from 6144 rows on),
+// its rows of 2048 to four 64-thread rows per CTA with three slots
+// (64-91 % -> 63-93 %, +7 at 6144-8192 rows), and its rows of 4096 to one
+// 128-thread row per CTA, four CTAs per SM where two 128-thread rows per CTA
+// held two (+1 to +3 points at 2048-32768 rows).
 const Choice kLayerNormTable[] = {
     {32, 256, 8, 4, 1, 2},       {64, 256, 16, 4, 1, 2},       {128, 256, 32, 4, 1, 2},
-    {256, 256, 64, 4, 1, 3},     {512, 256, 128, 4, 1, 2},     {1024, 256, 256, 4, 1, 2},
+    {256, 256, 64, 4, 1, 3},     {512, 128, 128, 4, 1, 2},     {1024, 256, 256, 4, 1, 2},
     {2048, 512, 512, 4, 1, 3},   {4096, 256, 256, 8, 2, 1},    {8192, 256, 256, 8, 4, 2},
     {16384, 256, 256, 8, 8, 2},  {32768, 512, 512, 8, 8, 1},   {65536, 512, 512, 8, 16, 2},
 };
