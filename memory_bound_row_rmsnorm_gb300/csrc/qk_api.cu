@@ -423,8 +423,9 @@ constexpr int kBwdDeepRingItems = 8;
 // anyway, and the deeper ring keeps all of them in flight.
 constexpr int kVeryShortItems = 2;
 
-// Alternative kernels for short launches, by items per resident CTA of the
-// table's plan (ipc):
+// Alternative kernels by the length of the launch, in items per resident CTA
+// of the table's plan (ipc).  The tables were tuned at 16384 rows; these rows
+// hold what measured better on shorter (and, twice, longer) launches:
 //  * fp32 softmax rows of 4096 elements below 8: 128-thread CTAs of 8 vectors
 //    a thread, with 3 ring slots below 4 and 2 above (1024 x 4096: 86 % ->
 //    88 %; 4096 x 4096: 90 % -> 92 %); the 256 x 4 plan beats it by 1-2
@@ -438,11 +439,14 @@ constexpr int kVeryShortItems = 2;
 //    vectors from 4 to 10, four 64-thread rows of 8 vectors a thread, three
 //    slots (+1 to +8 points at 6144-12288 rows);
 //  * RMSNorm (softmax) rows of 512 vectors (bf16 4096, fp32 2048 elements)
-//    from 4 to 12 (10): four 64-thread rows of 8 vectors a thread per
-//    256-thread CTA, three slots, two CTAs per SM (RMSNorm bf16 8192 x 4096:
-//    89 % -> 95 %, fp32 10240 x 2048 89 % -> 96 %; softmax fp32 6144 x 2048
-//    91 % -> 101 %, bf16 8192 x 4096 89 % -> 94 %); below 4 and from about 16
-//    on the table's 128-thread plan measured as good or better;
+//    from 4 to 12 (bf16 softmax 10, fp32 softmax 8): four 64-thread rows of 8
+//    vectors a thread per 256-thread CTA, three slots, two CTAs per SM
+//    (RMSNorm bf16 8192 x 4096: 89 % -> 95 %, fp32 10240 x 2048 89 % -> 96 %;
+//    softmax fp32 6144 x 2048 91 % -> 101 %, bf16 8192 x 4096 89 % -> 94 %);
+//    below 4 and from about 16 on the table's 128-thread plan measured as
+//    good or better, except for fp32 softmax, whose rows of 2048 elements
+//    take one 256-thread row of 2 vectors a thread with two slots from 8 on
+//    (16384 x 2048: 91 % -> 96 %, 32768 x 2048 91 % -> 95 %);
 //  * RMSNorm and softmax rows of 64 vectors (fp32 256, bf16 512 elements)
 //    below 1.5: eight 32-thread rows per CTA, three slots.  The table's
 //    sixteen-row CTAs halve the items, so in so short a launch the SMs' shares
@@ -452,30 +456,39 @@ constexpr int kVeryShortItems = 2;
 //  * fp32 LayerNorm rows of 128 vectors (512 elements) from 2 to 16: sixteen
 //    16-thread rows of 8 vectors a thread per CTA, three slots (8192 x 512:
 //    69 % -> 76 %, 24576 x 512: 87 % -> 100 %); at 65536 rows the table's
-//    plan measured 4 points ahead.
-constexpr int kShortAltMaxItems = 20;
+//    plan measured 4 points ahead;
+//  * RMSNorm rows of 2048 vectors (fp32 8192, bf16 16384 elements) from 10
+//    on: one 512-thread row of 4 vectors a thread per CTA, two slots, one CTA
+//    per SM, where the table's 256 x 8 plan holds two (fp32 16384 x 8192:
+//    98 % -> 100 %, 4096 x 8192 93 % -> 96 %; bf16 +1 point); the table's
+//    plan stays ahead on shorter launches (2048 rows: 97-98 % against 88-90 %).
 // One row of those rules: operator, dtype (-1: both), rows of (nv_lo, nv_hi]
-// vectors, a window [ipc_lo2, ipc_hi2) on 2 * ipc, the plan, and 2 * ipc below
-// which it takes three ring slots instead of its own count (0: never).
-struct ShortAlt {
+// vectors, a window [ipc_lo2, ipc_hi2) on 2 * ipc (kOpenEnd: no upper end),
+// the plan, and 2 * ipc below which it takes three ring slots instead of its
+// own count (0: never).
+constexpr int kOpenEnd = 1 << 30;
+struct LaunchAlt {
   int op, dt;
   int64_t nv_lo, nv_hi;
   int ipc_lo2, ipc_hi2, deep_below2;
   Choice c;
 };
-const ShortAlt kShortAlts[] = {
+const LaunchAlt kLaunchAlts[] = {
     {kSoftmax, QK_F32, 512, 1024, 0, 16, 8, {1024, 128, 128, 8, 1, 2}},
     {kXent, -1, 256, 512, 0, 8, 0, {512, 128, 64, 8, 1, 2}},
-    {kOpSoftmaxBwd, -1, 128, 256, 0, 2 * kShortAltMaxItems, 16, {256, 256, 64, 4, 1, 2}},
+    {kOpSoftmaxBwd, -1, 128, 256, 0, 40, 16, {256, 256, 64, 4, 1, 2}},
     {kOpXentBwd, -1, 256, 512, 8, 20, 0, {512, 256, 64, 8, 1, 3}},
     {kRmsNorm, -1, 256, 512, 8, 24, 0, {512, 256, 64, 8, 1, 3}},
-    {kSoftmax, -1, 256, 512, 8, 20, 0, {512, 256, 64, 8, 1, 3}},
+    {kSoftmax, QK_BF16, 256, 512, 8, 20, 0, {512, 256, 64, 8, 1, 3}},
+    {kSoftmax, QK_F32, 256, 512, 8, 16, 0, {512, 256, 64, 8, 1, 3}},
+    {kSoftmax, QK_F32, 256, 512, 16, kOpenEnd, 0, {512, 256, 256, 2, 1, 2}},
     {kRmsNorm, -1, 32, 64, 0, 3, 0, {64, 256, 32, 2, 1, 3}},
     {kSoftmax, -1, 32, 64, 0, 3, 0, {64, 256, 32, 2, 1, 3}},
     {kOpLayerNorm, QK_F32, 64, 128, 4, 32, 0, {128, 256, 16, 8, 1, 3}},
+    {kRmsNorm, -1, 1024, 2048, 20, kOpenEnd, 0, {2048, 512, 512, 4, 1, 2}},
 };
-bool short_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
-  for (const ShortAlt& a : kShortAlts) {
+bool launch_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
+  for (const LaunchAlt& a : kLaunchAlts) {
     if (a.op != op || (a.dt >= 0 && a.dt != dt) || NV <= a.nv_lo || NV > a.nv_hi) continue;
     if (2 * items < a.ipc_lo2 * resident || 2 * items >= a.ipc_hi2 * resident) continue;
     *c = a.c;
@@ -582,9 +595,9 @@ qk_status plan_ring(int dev, const DeviceInfo& d, int op, int dt, int64_t M, int
   // 16384 x 1024: 90 % -> 98 %.)
   const bool short_ok = !ov.on && !two_pass && k == 1 && cl == 1;
   const int64_t resident = ctas_per_sm * d.sms;
-  if (short_ok && alt == nullptr && p->num_items < kShortAltMaxItems * resident) {
+  if (short_ok && alt == nullptr) {
     Choice c;
-    if (short_alternative(op, dt, NV, p->num_items, resident, &c) &&
+    if (launch_alternative(op, dt, NV, p->num_items, resident, &c) &&
         !(c.threads == th && c.row_threads == tpr && c.vec_per_thread == vpt))
       return plan_ring(dev, d, op, dt, M, N, p, &c);  // its slots as given
   }

@@ -15,8 +15,10 @@ plans those rules pick against the oracle:
   * cross-entropy rows of 512 vectors otherwise run one warp a row, 16
     vectors a lane; bf16 softmax rows of 8192 elements 128 x 8 vectors;
   * RMSNorm (softmax) rows of 512 vectors (bf16 4096, fp32 2048 elements)
-    at 4-12 (4-10) items per resident CTA run four 64-thread rows per
-    256-thread CTA with three slots;
+    at 4-12 (bf16 4-10, fp32 4-8) items per resident CTA run four 64-thread
+    rows per 256-thread CTA with three slots, fp32 softmax rows one
+    256-thread row per CTA with two slots above that; RMSNorm rows of 2048
+    vectors one 512-thread row per CTA with two slots from 10 on;
   * RMSNorm and softmax rows of 64 vectors run sixteen rows per CTA from 1.5
     items per resident CTA on, eight below; fp32 LayerNorm rows of 128 run
     sixteen rows per CTA from 2 to 16 items per resident CTA of the table's
@@ -64,7 +66,21 @@ def resident(p):
     return p["ctas_per_sm"] * torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("op,dtype,N", [("rmsnorm", "bf16", 1024), ("rmsnorm", "f32", 8192),
+def table_resident(op, dtype, N, table_plan):
+    """Resident CTAs of the table's own plan (threads, row_threads,
+    vec_per_thread, slots), read back with that plan forced: the rules by
+    launch length count items per resident CTA of it."""
+    th, tpr, vpt, slots = table_plan
+    forced = {"path": 1, "threads": th, "row_threads": tpr, "vec_per_thread": vpt, "cluster": 1, "slots": slots,
+              "chunks": 0, "ctas_per_sm": 0, "grid": 0, "smem_bytes": 0}
+    qb.qk_set_plan_override(OP[op], DT[dtype], forced)
+    try:
+        return resident(plan(op, dtype, 1 << 20, N))
+    finally:
+        qb.qk_set_plan_override(OP[op], DT[dtype], None)
+
+
+@pytest.mark.parametrize("op,dtype,N", [("rmsnorm", "bf16", 1024), ("rmsnorm", "f32", 4096),
                                         ("layernorm", "f32", 2048), ("softmax", "bf16", 4096)])
 def test_ring_depth_follows_items_per_cta(op, dtype, N):
     long_ = plan(op, dtype, 1 << 20, N)  # many items per CTA: the table's slots
@@ -178,24 +194,27 @@ def test_very_short_forward_launches_take_three_slots(op, dtype, M, N):
     check_against_oracle(op, dtype, inp, out, what=f"very short {op} {dtype} {M}x{N}")
 
 
-@pytest.mark.parametrize("op,top", [("rmsnorm", 12), ("softmax", 10)])
-def test_rows_of_512_vectors(op, top):
-    """Between 4 and 12 (softmax 10) items per resident CTA of the table's
-    128-thread plan: 256-thread CTAs of four 64-thread rows, three slots;
-    outside it the table's plan; the chosen plans against the oracle on every
-    row."""
+@pytest.mark.parametrize("op,top,top_f32", [("rmsnorm", 12, 12), ("softmax", 10, 8)])
+def test_rows_of_512_vectors(op, top, top_f32):
+    """Between 4 and 12 (bf16 softmax 10, fp32 softmax 8) items per resident
+    CTA of the table's 128-thread plan: 256-thread CTAs of four 64-thread
+    rows, three slots; below it the table's plan; above it the table's plan
+    too, except for fp32 softmax: one 256-thread row of 2 vectors a thread,
+    two slots; the chosen plans against the oracle on every row."""
     for dtype, N in (("bf16", 4096), ("f32", 2048)):
-        table = plan(op, dtype, 1 << 20, N)
-        assert (table["threads"], table["row_threads"], table["vec_per_thread"]) == (128, 128, 4), table
-        res = resident(table)
-        for M in (2048, 4096, 6144, 8192, 10240, 12288, 14336, 16384, 32768):
+        hi = top_f32 if dtype == "f32" else top
+        long_alt = op == "softmax" and dtype == "f32"
+        res = table_resident(op, dtype, N, (128, 128, 4, 1))
+        for M in (2048, 4096, 6144, 8192, 10240, 12288, 14336, 16384, 32768, 1 << 20):
             p = plan(op, dtype, M, N)
-            alt = 4 * res <= M < top * res
             got = (p["threads"], p["row_threads"], p["vec_per_thread"])
-            assert got == ((256, 64, 8) if alt else (128, 128, 4)), (dtype, M, p)
-            if alt:
-                assert p["slots"] == 3, p
-    for dtype, M, N in (("bf16", 8192, 4096), ("f32", 10000, 2048)):
+            if 4 * res <= M < hi * res:
+                assert got == (256, 64, 8) and p["slots"] == 3, (dtype, M, p, res)
+            elif M >= hi * res and long_alt:
+                assert got == (256, 256, 2) and p["slots"] == 2, (dtype, M, p, res)
+            else:
+                assert got == (128, 128, 4), (dtype, M, p, res)
+    for dtype, M, N in (("bf16", 8192, 4096), ("f32", 10000, 2048), ("f32", 30000, 2048)):
         inp = syn.make_inputs(op, dtype, M, N, 16000 + M, "cpu")
         out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, dtype)
         check_against_oracle(op, dtype, inp, out, what=f"planner {op} {dtype} {M}x{N}")
@@ -221,6 +240,26 @@ def test_short_rows_of_sixteen_row_ctas(op, dtype, N):
         inp = syn.make_inputs(op, dtype, M, N, 17000 + M, "cpu")
         out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, dtype)
         check_against_oracle(op, dtype, inp, out, what=f"short rows {op} {dtype} {M}x{N}")
+
+
+def test_rmsnorm_rows_of_2048_vectors():
+    """RMSNorm rows of 2048 vectors (fp32 8192, bf16 16384 elements) from 10
+    items per resident CTA of the table's 256 x 8 plan on: one 512-thread row
+    of 4 vectors a thread per CTA, two slots; the table's plan below; the
+    plans on both sides against the oracle on every row."""
+    for dtype, N in (("f32", 8192), ("bf16", 16384)):
+        res = table_resident("rmsnorm", dtype, N, (256, 256, 8, 1))
+        for M in (1024, 2048, 4096, 8192, 16384, 65536):
+            p = plan("rmsnorm", dtype, M, N)
+            got = (p["threads"], p["row_threads"], p["vec_per_thread"])
+            if M >= 10 * res:
+                assert got == (512, 512, 4) and p["slots"] == 2, (dtype, M, p, res)
+            else:
+                assert got == (256, 256, 8), (dtype, M, p, res)
+        for M in (10 * res - 3, 10 * res + 5):
+            inp = syn.make_inputs("rmsnorm", dtype, M, N, 19000 + M, "cpu")
+            out = run_gpu("rmsnorm", {k: v.to(DEV) for k, v in inp.items()}, dtype)
+            check_against_oracle("rmsnorm", dtype, inp, out, what=f"planner rmsnorm {dtype} {M}x{N}")
 
 
 def test_layernorm_f32_rows_of_128_vectors():

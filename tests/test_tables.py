@@ -66,42 +66,48 @@ def test_backward_tables(kernels, name):
             assert key in kernels, f"{name} entry {max_nv}: no {key}"
 
 
-def short_alternatives():
+def launch_alternatives():
     text = open(API).read()
-    m = re.search(r"\bkShortAlts\[\]\s*=\s*\{(.*?)\n\};", text, re.S)
-    assert m, "kShortAlts"
+    m = re.search(r"\bkLaunchAlts\[\]\s*=\s*\{(.*?)\n\};", text, re.S)
+    assert m, "kLaunchAlts"
     pat = r"\{(k\w+), (-1|QK_F32|QK_BF16), (\d+), (\d+), (\d+), ([^,]+), (\d+), \{([^{}]*)\}\}"
     return [(g[0], g[1], tuple(x.strip() for x in g[7].split(",")), (int(g[2]), int(g[3])), g[4], g[5])
             for g in re.findall(pat, m.group(1))]
 
 
-def test_short_alternatives(kernels):
-    """The planner's alternative plans for short launches (kShortAlts) have
+def test_launch_alternatives(kernels):
+    """The planner's alternative plans by launch length (kLaunchAlts) have
     their kernels too, for the dtypes each row applies to."""
     ops = {"kSoftmax": ("row_kernel", 0), "kRmsNorm": ("row_kernel", 1), "kXent": ("row_kernel", 2),
            "kOpLayerNorm": ("row_kernel", 3), "kOpSoftmaxBwd": ("bwd_kernel", 10), "kOpXentBwd": ("bwd_kernel", 12)}
-    rows = short_alternatives()
-    assert len(rows) == open(API).read().split("kShortAlts[] = {", 1)[1].split("\n};", 1)[0].count("{k")
+    rows = launch_alternatives()
+    assert len(rows) == open(API).read().split("kLaunchAlts[] = {", 1)[1].split("\n};", 1)[0].count("{k")
     for op, dt, (max_nv, th, tpr, vpt, cl, slots), _, _, _ in rows:
         kind, code = ops[op]
         for d in ({"QK_F32": ("float",), "QK_BF16": ("__nv_bfloat16",)}.get(dt, DTYPES)):
             key = (kind, str(code), d, th, tpr, vpt, b(int(cl) > 1))
             if kind == "row_kernel":
                 key += ("false",)
-            assert key in kernels, f"kShortAlts {op} {dt}: no {key}"
+            assert key in kernels, f"kLaunchAlts {op} {dt}: no {key}"
 
 
-def test_short_alternatives_do_not_overlap():
+def test_launch_alternatives_do_not_overlap():
     """The planner takes the first row that matches; no two rows may match the
     same operator, dtype and row length, so the order of the rows decides
     nothing."""
-    rows = short_alternatives()
+    rows = launch_alternatives()
     assert rows
-    for i, (op, dt, _, (lo, hi), _, _) in enumerate(rows):
+    big = 1 << 30
+    win = lambda lo2, hi2: (int(lo2), big if hi2 == "kOpenEnd" else int(hi2))
+    for i, (op, dt, _, (lo, hi), lo2, hi2) in enumerate(rows):
         assert lo < hi
-        for op2, dt2, _, (lo2, hi2), _, _ in rows[i + 1:]:
-            same_dt = dt == dt2 or "-1" in (dt, dt2)
-            assert not (op == op2 and same_dt and lo < hi2 and lo2 < hi), (op, dt, lo, hi, dt2, lo2, hi2)
+        w = win(lo2, hi2)
+        assert w[0] < w[1], (op, dt, lo2, hi2)
+        for op_b, dt_b, _, (lo_b, hi_b), lo2_b, hi2_b in rows[i + 1:]:
+            same_dt = dt == dt_b or "-1" in (dt, dt_b)
+            wb = win(lo2_b, hi2_b)
+            overlap = lo < hi_b and lo_b < hi and w[0] < wb[1] and wb[0] < w[1]
+            assert not (op == op_b and same_dt and overlap), (op, dt, lo, hi, w, dt_b, lo_b, hi_b, wb)
 
 
 def test_two_pass_kernels(kernels):
