@@ -315,7 +315,9 @@ const Choice kSoftmaxBwdTable[] = {
 // 8192-32768 rows.  fp32 rows of 2048 take four slots (three CTAs per SM
 // instead of five: 76 % -> 88 %, 86 % -> 95 %, 92 % -> 98 %; fewer CTAs also
 // means fewer dw partial rows to sum), bf16 rows of 8192 three (82 % -> 88 %,
-// 86 % -> 93 %, 90 % -> 97 %); the other rows measured best at two.
+// 86 % -> 93 %, 90 % -> 97 %); the other rows measured best at two, except
+// bf16 rows of 2048, which a later search on the streaming-store kernels gave
+// three (+2 to +6 points from 8192 rows on, level below).
 const Choice kRmsNormBwdTable[] = {
     {32, 256, 32, 2, 1, 2},    {64, 256, 64, 2, 1, 2},    {128, 256, 64, 2, 1, 2},
     {256, 256, 128, 2, 1, 2},  {512, 128, 128, 4, 1, 4},  {1024, 256, 256, 4, 1, 2},
@@ -324,7 +326,7 @@ const Choice kRmsNormBwdTable[] = {
 };
 const Choice kRmsNormBwdBf16Table[] = {
     {32, 256, 32, 2, 1, 2},    {64, 256, 64, 2, 1, 2},    {128, 256, 64, 2, 1, 2},
-    {256, 256, 128, 2, 1, 2},  {512, 128, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 3},
+    {256, 256, 128, 2, 1, 3},  {512, 128, 128, 4, 1, 2},  {1024, 256, 256, 4, 1, 3},
     {2048, 256, 256, 4, 2, 2}, {4096, 512, 512, 4, 2, 2}, {8192, 512, 512, 4, 4, 2},
     {16384, 512, 512, 4, 8, 2}, {32768, 512, 512, 4, 16, 2},
 };
@@ -461,7 +463,11 @@ constexpr int kVeryShortItems = 2;
 //    on: one 512-thread row of 4 vectors a thread per CTA, two slots, one CTA
 //    per SM, where the table's 256 x 8 plan holds two (fp32 16384 x 8192:
 //    98 % -> 100 %, 4096 x 8192 93 % -> 96 %; bf16 +1 point); the table's
-//    plan stays ahead on shorter launches (2048 rows: 97-98 % against 88-90 %).
+//    plan stays ahead on shorter launches (2048 rows: 97-98 % against 88-90 %);
+//  * fp32 RMSNorm backward rows of 512 vectors (2048 elements) from 32 on:
+//    two 128-thread rows per 256-thread CTA, two slots, where the table's
+//    plan runs one row per CTA with four (16384 x 2048 90 % -> 92 %, 65536 x
+//    2048 96 % -> 100 %; the table's plan 3-7 points ahead at 1024-4096 rows).
 // One row of those rules: operator, dtype (-1: both), rows of (nv_lo, nv_hi]
 // vectors, a window [ipc_lo2, ipc_hi2) on 2 * ipc (kOpenEnd: no upper end),
 // the plan, and 2 * ipc below which it takes three ring slots instead of its
@@ -486,6 +492,7 @@ const LaunchAlt kLaunchAlts[] = {
     {kSoftmax, -1, 32, 64, 0, 3, 0, {64, 256, 32, 2, 1, 3}},
     {kOpLayerNorm, QK_F32, 64, 128, 4, 32, 0, {128, 256, 16, 8, 1, 3}},
     {kRmsNorm, -1, 1024, 2048, 20, kOpenEnd, 0, {2048, 512, 512, 4, 1, 2}},
+    {kOpRmsNormBwd, QK_F32, 256, 512, 64, kOpenEnd, 0, {512, 256, 128, 4, 1, 2}},
 };
 bool launch_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
   for (const LaunchAlt& a : kLaunchAlts) {

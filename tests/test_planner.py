@@ -71,7 +71,8 @@ def table_resident(op, dtype, N, table_plan):
     vec_per_thread, slots), read back with that plan forced: the rules by
     launch length count items per resident CTA of it."""
     th, tpr, vpt, slots = table_plan
-    forced = {"path": 1, "threads": th, "row_threads": tpr, "vec_per_thread": vpt, "cluster": 1, "slots": slots,
+    forced = {"path": 3 if op.endswith("_bwd") else 1, "threads": th, "row_threads": tpr, "vec_per_thread": vpt,
+              "cluster": 1, "slots": slots,
               "chunks": 0, "ctas_per_sm": 0, "grid": 0, "smem_bytes": 0}
     qb.qk_set_plan_override(OP[op], DT[dtype], forced)
     try:
@@ -260,6 +261,24 @@ def test_rmsnorm_rows_of_2048_vectors():
             inp = syn.make_inputs("rmsnorm", dtype, M, N, 19000 + M, "cpu")
             out = run_gpu("rmsnorm", {k: v.to(DEV) for k, v in inp.items()}, dtype)
             check_against_oracle("rmsnorm", dtype, inp, out, what=f"planner rmsnorm {dtype} {M}x{N}")
+
+
+def test_rmsnorm_backward_f32_rows_of_512_vectors():
+    """fp32 RMSNorm backward rows of 2048 elements from 32 items per resident
+    CTA of the table's plan (one 128-thread row per CTA, four slots) on: two
+    128-thread rows per 256-thread CTA, two slots; the plans on both sides
+    against the oracle (dx and dw)."""
+    res = table_resident("rmsnorm_bwd", "f32", 2048, (128, 128, 4, 4))
+    for M in (1024, 4096, 8192, 16384, 65536):
+        p = plan("rmsnorm_bwd", "f32", M, 2048)
+        got = (p["threads"], p["row_threads"], p["vec_per_thread"])
+        if M >= 32 * res:
+            assert got == (256, 128, 4) and p["slots"] == 2, (M, p, res)
+        else:
+            assert got == (128, 128, 4), (M, p, res)
+    for M in (32 * res - 1, 32 * res + 3):
+        case = tb.make_case("rmsnorm", "f32", M, 2048, 19500 + M)
+        tb.check("rmsnorm", "f32", case, tb.run_gpu("rmsnorm", "f32", case), f"planner rmsnorm bwd f32 {M}x2048")
 
 
 def test_layernorm_f32_rows_of_128_vectors():

@@ -79,7 +79,8 @@ def test_launch_alternatives(kernels):
     """The planner's alternative plans by launch length (kLaunchAlts) have
     their kernels too, for the dtypes each row applies to."""
     ops = {"kSoftmax": ("row_kernel", 0), "kRmsNorm": ("row_kernel", 1), "kXent": ("row_kernel", 2),
-           "kOpLayerNorm": ("row_kernel", 3), "kOpSoftmaxBwd": ("bwd_kernel", 10), "kOpXentBwd": ("bwd_kernel", 12)}
+           "kOpLayerNorm": ("row_kernel", 3), "kOpSoftmaxBwd": ("bwd_kernel", 10), "kOpRmsNormBwd": ("bwd_kernel", 11),
+           "kOpXentBwd": ("bwd_kernel", 12)}
     rows = launch_alternatives()
     assert len(rows) == open(API).read().split("kLaunchAlts[] = {", 1)[1].split("\n};", 1)[0].count("{k")
     for op, dt, (max_nv, th, tpr, vpt, cl, slots), _, _, _ in rows:
