@@ -467,7 +467,14 @@ constexpr int kVeryShortItems = 2;
 //  * fp32 RMSNorm backward rows of 512 vectors (2048 elements) from 32 on:
 //    two 128-thread rows per 256-thread CTA, two slots, where the table's
 //    plan runs one row per CTA with four (16384 x 2048 90 % -> 92 %, 65536 x
-//    2048 96 % -> 100 %; the table's plan 3-7 points ahead at 1024-4096 rows).
+//    2048 96 % -> 100 %; the table's plan 3-7 points ahead at 1024-4096 rows);
+//  * fp32 softmax rows of 256 vectors (1024 elements) from 10 on: two
+//    128-thread rows of 2 vectors a thread per CTA, two slots (32768 x 1024
+//    90 % -> 96 %, 65536 x 1024 91 % -> 94 %; 1-14 points behind below 16384
+//    rows);
+//  * fp32 LayerNorm rows of 64 vectors (256 elements) from 3 on: thirty-two
+//    8-thread rows of 8 vectors a thread per CTA, three slots (16384 x 256
+//    72 % -> 78 %, 32768 x 256 87 % -> 93 %; 2-5 points behind below).
 // One row of those rules: operator, dtype (-1: both), rows of (nv_lo, nv_hi]
 // vectors, a window [ipc_lo2, ipc_hi2) on 2 * ipc (kOpenEnd: no upper end),
 // the plan, and 2 * ipc below which it takes three ring slots instead of its
@@ -493,6 +500,8 @@ const LaunchAlt kLaunchAlts[] = {
     {kOpLayerNorm, QK_F32, 64, 128, 4, 32, 0, {128, 256, 16, 8, 1, 3}},
     {kRmsNorm, -1, 1024, 2048, 20, kOpenEnd, 0, {2048, 512, 512, 4, 1, 2}},
     {kOpRmsNormBwd, QK_F32, 256, 512, 64, kOpenEnd, 0, {512, 256, 128, 4, 1, 2}},
+    {kSoftmax, QK_F32, 128, 256, 20, kOpenEnd, 0, {256, 256, 128, 2, 1, 2}},
+    {kOpLayerNorm, QK_F32, 32, 64, 6, kOpenEnd, 0, {64, 256, 8, 8, 1, 3}},
 };
 bool launch_alternative(int op, int dt, int64_t NV, int64_t items, int64_t resident, Choice* c) {
   for (const LaunchAlt& a : kLaunchAlts) {

@@ -281,6 +281,33 @@ def test_rmsnorm_backward_f32_rows_of_512_vectors():
         tb.check("rmsnorm", "f32", case, tb.run_gpu("rmsnorm", "f32", case), f"planner rmsnorm bwd f32 {M}x2048")
 
 
+@pytest.mark.parametrize("op,N,table_plan,long_plan,ipc", [
+    ("softmax", 1024, (256, 64, 4, 2), (256, 128, 2, 2), 10),
+    ("layernorm", 256, (256, 16, 4, 2), (256, 8, 8, 3), 3)])
+def test_fp32_long_launch_rows(op, N, table_plan, long_plan, ipc):
+    """fp32 softmax rows of 1024 elements and LayerNorm rows of 256: the long
+    plan from `ipc` items per resident CTA of the table's plan on, the table's
+    plan (or a short-launch rule) below; the plans on both sides against the
+    oracle on every row."""
+    res = table_resident(op, "f32", N, table_plan)
+    rows = table_plan[0] // table_plan[1]
+    edge = ipc * res * rows
+    for M in (edge // 2, edge - rows, edge + rows, 2 * edge, 4 * edge):
+        p = plan(op, "f32", M, N)
+        got = (p["threads"], p["row_threads"], p["vec_per_thread"], p["slots"])
+        if -(-M // rows) >= ipc * res:
+            assert got == long_plan, (M, p, res)
+        else:
+            assert got[:3] != long_plan[:3], (M, p, res)
+    for M in (edge - rows - 3, edge + 5):
+        if op == "layernorm":
+            tl.full_check("f32", M, N, 20000 + M, what=f"planner layernorm f32 {M}x{N}")
+        else:
+            inp = syn.make_inputs(op, "f32", M, N, 20000 + M, "cpu")
+            out = run_gpu(op, {k: v.to(DEV) for k, v in inp.items()}, "f32")
+            check_against_oracle(op, "f32", inp, out, what=f"planner {op} f32 {M}x{N}")
+
+
 def test_layernorm_f32_rows_of_128_vectors():
     """fp32 LayerNorm rows of 512 elements: sixteen 16-thread rows of 8 vectors
     a thread per CTA, three slots, from 2 to 16 items per resident CTA of the
